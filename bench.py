@@ -1,0 +1,394 @@
+#!/usr/bin/env python3
+"""Benchmark of the exact-sum GEMM on GB300.
+
+Workload (one "step"): the exact GEMM C = RNE_f32(A B^T) at M = N = K = 4096,
+f32, A and B iid N(0,1) from seed 0 (rank r uses seed r), with inputs resident
+in HBM; between steps a 256 MiB buffer is written to flush the 129 MB L2.
+Metric: exact-GEMM GFLOP/s = 2 M N K / t (whole job, summed over ranks).
+
+Printed as one JSON line on rank 0, with:
+  roofline      dominant kernel vs the integer-ALU issue peak
+  cpu_baseline  the CPU oracle on a bounded row sample of the same workload
+  e2e           the same metric through the public API from pinned host
+                buffers, copies included
+  clocks        nvidia-smi SM clocks and throttle reasons during the timed region
+  sharded       2-way K-sharded partial/combine/finalize of the same GEMM, with
+                the combine and finalize kernels' HBM rooflines
+
+``--impl reference`` times the CPU oracle instead (the reference arm).
+Multi-GPU: launched with torchrun, every rank runs its own independent
+problem (weak scaling, no collective on the data path).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "exact-GEMM GFLOP/s (2MNK/s) at 4096^3 f32"
+UNIT = "GFLOP/s"
+M = N = K = 4096
+FLUSH_BYTES = 256 << 20
+SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--workload", choices=["normal", "wide"], default="normal",
+                   help="normal: N(0,1) (the headline); wide: |x| = 2^U[-40,40]")
+    p.add_argument("--cpu-rows", type=int, default=64,
+                   help="rows of the 4096^3 problem the CPU baseline samples")
+    p.add_argument("--no-extras", action="store_true",
+                   help="skip the e2e, sharded and CPU-baseline measurements")
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_inputs(seed, workload):
+    from exact_sum_gemm_gb300 import workloads as wl
+    if workload == "normal":
+        return wl.normal_f32((M, K), seed, 0), wl.normal_f32((N, K), seed, 1)
+    return (wl.loguniform_f32((M, K), seed, 0, lo=-40, hi=40),
+            wl.loguniform_f32((N, K), seed, 1, lo=-40, hi=40))
+
+
+def workload_config(workload, extra=None):
+    cfg = {"workload": f"det_gemm f32 M=N=K=4096, A,B "
+                       f"{'iid N(0,1)' if workload == 'normal' else '|x|=2^U[-40,40]'}, seed 0",
+           "M": M, "N": N, "K": K, "dtype_in": "f32", "dtype_out": "f32",
+           "l2": "flushed: 256 MiB write between steps (inside the timed region)",
+           "inputs": "resident in HBM (e2e: copied from pinned host memory every step)"}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    def __init__(self, uuid=None):
+        self.proc = None
+        self.uuid = uuid
+
+    def start(self):
+        cmd = ["nvidia-smi", f"--query-gpu={SMI_FIELDS}", "--format=csv,noheader,nounits",
+               "-lms", "200"]
+        if self.uuid:
+            cmd += ["-i", self.uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(REASON_NAMES, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def cpu_baseline(workload, rows, seed=0):
+    """The oracle, as it stands, on `rows` rows of the same problem (all host cores)."""
+    import oracle
+    oracle.build()
+    A, B = make_inputs(seed, workload)
+    sel = np.linspace(0, M - 1, rows).astype(np.int64)
+    A_s = np.ascontiguousarray(A[sel])
+    cores = os.cpu_count() or 1
+    t0 = time.perf_counter()
+    oracle.gemm(A_s, B, nthreads=cores)
+    dt = time.perf_counter() - t0
+    return {"value": round(2.0 * rows * N * K / dt / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{rows} evenly spaced rows of the 4096^3 problem ({rows}x4096x4096 "
+                      f"exact MACs), {dt:.2f} s wall on {cores} threads"}
+
+
+def alu_peak_gops(sm_count, clock_mhz):
+    """Integer-ALU issue peak: SMs x 128 lanes x clock, one instruction per exact
+    multiply-add counted as 2 ops (the same convention as 2MNK)."""
+    return 2.0 * sm_count * 128 * clock_mhz * 1e6 / 1e9
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    A, B = make_inputs(0, args.workload)
+    rows = max(1, args.cpu_rows // 4)
+    cores = os.cpu_count() or 1
+    g = np.random.default_rng(1234)
+
+    def step():
+        sel = np.sort(g.choice(M, size=rows, replace=False))
+        oracle.gemm(np.ascontiguousarray(A[sel]), B, nthreads=cores)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    value = 2.0 * rows * N * K / dt / 1e9
+    line = {"metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "impl": "reference",
+            "config": workload_config(args.workload, {"parallelism": "host cores"}),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
+                             "kind": "oracle",
+                             "sample": f"each step: {rows} random rows of the 4096^3 problem"},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    import exact_sum_gemm_gb300 as dg
+    lib = dg.library()
+
+    A, B = make_inputs(rank, args.workload)
+    a = torch.from_numpy(A).to(dev)
+    b = torch.from_numpy(B).to(dev)
+    c = torch.empty((M, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        dg.det_gemm(a, b, out=c)
+    torch.cuda.synchronize(dev)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(props.uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    launches0 = lib.det_kernel_launches()
+    barrier()
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for s in range(args.steps):
+        flush.zero_()
+        ev[s][0].record(stream)
+        dg.det_gemm(a, b, out=c)
+        ev[s][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    launches = lib.det_kernel_launches() - launches0
+    clocks = sampler.stop()
+    elapsed_ms = start.elapsed_time(end)
+    kern_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    if dist is not None:
+        t = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    flops = 2.0 * M * N * K
+    value = flops * world / (ms_per_step * 1e-3) / 1e9
+
+    extras = {}
+    if rank == 0 and not args.no_extras:
+        extras = measure_extras(args, dg, a, b, c, A, B, dev, stream)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks = measured_peaks()
+    kern_avg = statistics.mean(kern_ms)
+    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    peak = alu_peak_gops(props.multi_processor_count, clock_mhz)
+    achieved = flops / (kern_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+        "data": "synthetic",
+        "config": workload_config(args.workload, {"parallelism": f"{world} independent replicas"
+                                                  if world > 1 else "single GPU"}),
+        "gpu_launches": int(launches),
+        "roofline": {
+            "kernel": "kulisch_smem_kernel (det_gemm, fused finalize)",
+            "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1),
+            "unit": "Gop/s", "frac": round(achieved / peak, 5), "traffic": None,
+            "peak_source": f"derived: {props.multi_processor_count} SMs x 128 INT32 lanes x "
+                           f"{clock_mhz:.0f} MHz x 2 ops per exact MAC",
+            "kernel_ms": round(kern_avg, 4),
+        },
+        "clocks": clocks,
+    }
+    line.update(extras)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def measure_extras(args, dg, a, b, c, A, B, dev, stream):
+    import torch
+    out = {}
+    peaks = measured_peaks()
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    # ---- e2e: pinned host buffers, copies inside the timed region
+    hA = torch.from_numpy(A).pin_memory()
+    hB = torch.from_numpy(B).pin_memory()
+    hC = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    steps = max(2, min(args.steps, 5))
+    for _ in range(1):
+        a.copy_(hA, non_blocking=True)
+        b.copy_(hB, non_blocking=True)
+        dg.det_gemm(a, b, out=c)
+        hC.copy_(c, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        a.copy_(hA, non_blocking=True)
+        b.copy_(hB, non_blocking=True)
+        dg.det_gemm(a, b, out=c)
+        hC.copy_(c, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    t = e0.elapsed_time(e1) / steps
+    out["e2e"] = {"value": round(2.0 * M * N * K / (t * 1e-3) / 1e9, 3), "unit": UNIT,
+                  "h2d_bytes_per_step": int(A.nbytes + B.nbytes), "d2h_bytes_per_step": int(hC.nbytes),
+                  "ms_per_step": round(t, 4)}
+    # ---- sharded: 2-way K split through partial / combine / finalize
+    full_bits = c.clone()
+    cuts = [(0, K // 2), (K // 2, K)]
+    P = [torch.empty((20, M, N), dtype=torch.int64, device=dev) for _ in cuts]
+    acc = torch.empty((20, M, N), dtype=torch.int64, device=dev)
+    y = torch.empty((M, N), dtype=torch.float32, device=dev)
+    times = {"partial": [], "combine": [], "finalize": []}
+    for rep in range(3):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        evs[0].record(stream)
+        for (k0, k1), p in zip(cuts, P):
+            dg.det_gemm_partial(a[:, k0:k1], b[:, k0:k1], out=p)
+        evs[1].record(stream)
+        dg.det_combine(P, out=acc)
+        evs[2].record(stream)
+        dg.det_finalize(acc, out=y)
+        evs[3].record(stream)
+        torch.cuda.synchronize(dev)
+        if rep > 0:
+            times["partial"].append(evs[0].elapsed_time(evs[1]))
+            times["combine"].append(evs[1].elapsed_time(evs[2]))
+            times["finalize"].append(evs[2].elapsed_time(evs[3]))
+    equal = bool(torch.equal(y.view(torch.int32), full_bits.view(torch.int32)))
+    tc = statistics.mean(times["combine"])
+    tf = statistics.mean(times["finalize"])
+    tp = statistics.mean(times["partial"])
+    comb_bytes = 3 * 20 * 8 * M * N            # read 2 partials, write 1
+    fin_bytes = (19 * 8 + 4) * M * N           # read 18 digits + non-finite plane, write fp32
+    out["sharded"] = {
+        "equal_to_full_k": equal, "shards": 2,
+        "ms": {"partials": round(tp, 3), "combine": round(tc, 3), "finalize": round(tf, 3)},
+        "value": round(2.0 * M * N * K / ((tp + tc + tf) * 1e-3) / 1e9, 3), "unit": UNIT,
+        "combine_roofline": {"bound": "hbm", "achieved": round(comb_bytes / (tc * 1e-3) / 1e9, 1),
+                             "peak": hbm, "unit": "GB/s",
+                             "frac": round(comb_bytes / (tc * 1e-3) / 1e9 / hbm, 4),
+                             "algorithmic_bytes": comb_bytes},
+        "finalize_roofline": {"bound": "hbm", "achieved": round(fin_bytes / (tf * 1e-3) / 1e9, 1),
+                              "peak": hbm, "unit": "GB/s",
+                              "frac": round(fin_bytes / (tf * 1e-3) / 1e9 / hbm, 4),
+                              "algorithmic_bytes": fin_bytes},
+    }
+    del P, acc
+    torch.cuda.empty_cache()
+    # ---- CPU oracle baseline (bounded sample)
+    out["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_rows)
+    return out
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

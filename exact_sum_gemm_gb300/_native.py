@@ -1,0 +1,80 @@
+"""ctypes binding of the C ABI in ``include/det_gemm.h``.
+
+Loads the in-tree ``_lib/libdetgemm.so`` (building it with nvcc if it is
+missing or stale) and declares every exported ``det_*`` symbol.  There is no
+fallback: if the library cannot be built or loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+from . import _build
+
+DET_OK = 0
+DET_F32 = 0
+DET_BF16 = 1
+DET_DIGITS = 18
+DET_PLANES = 20
+DET_K_MAX = 1 << 19
+DET_MAX_COMBINE = 1 << 20
+
+STATUS_NAMES = {
+    0: "DET_OK", 1: "DET_ERR_INVALID_ARG", 2: "DET_ERR_DTYPE", 3: "DET_ERR_SHAPE",
+    4: "DET_ERR_K_LIMIT", 5: "DET_ERR_OVERFLOW", 6: "DET_ERR_ALIGNMENT", 7: "DET_ERR_CUDA",
+}
+
+# symbol -> (restype, argtypes); mirrors include/det_gemm.h
+_i64, _i32, _vp = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p
+SIGNATURES = {
+    "det_abi_version": (_i32, []),
+    "det_status_string": (ctypes.c_char_p, [_i32]),
+    "det_kernel_launches": (ctypes.c_uint64, []),
+    "det_gemm": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _vp]),
+    "det_gemm_partial": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _vp]),
+    "det_combine": (_i32, [_i64, _i64, ctypes.POINTER(_vp), _i32, _vp, _vp]),
+    "det_finalize": (_i32, [_i64, _i64, _vp, _vp, _i64, _vp]),
+    "det_linear_forward": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "det_linear_dgrad": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "det_linear_wgrad": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class DetError(RuntimeError):
+    """A det_* call returned a non-OK status."""
+
+    def __init__(self, fn, status):
+        self.status = status
+        name = STATUS_NAMES.get(status, f"status {status}")
+        msg = lib().det_status_string(status).decode() if status in STATUS_NAMES else name
+        super().__init__(f"{fn}: {msg}")
+
+
+def lib_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib(build: bool = True):
+    """The loaded library (built on first use)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.build() if build else _build.LIB_PATH
+            handle = ctypes.CDLL(path)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = handle
+    return _lib
+
+
+def check(fn_name: str, status: int) -> None:
+    if status != DET_OK:
+        if status in (1, 2, 3, 4, 5, 6):
+            err = DetError(fn_name, status)
+            raise ValueError(str(err)) from err
+        raise DetError(fn_name, status)

@@ -1,0 +1,39 @@
+// Internal launch interface between the C ABI (capi.cu) and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace det {
+
+// Count one enqueued kernel (diagnostic; see det_kernel_launches).
+void note_launch(int n = 1);
+
+struct GemmArgs {
+  const void* A;
+  int64_t lda;
+  int opA;            // 0: element (m,k) at A[m*lda+k]; 1: at A[k*lda+m]
+  const void* B;
+  int64_t ldb;
+  int opB;            // 0: element (n,k) at B[n*ldb+k]; 1: at B[k*ldb+n]
+  int64_t M, N, K;
+  int bf16;           // operand dtype: 0 = f32, 1 = bf16
+  float* C;           // fused-finalize output (det_gemm), or null
+  int64_t ldc;
+  int64_t* P;         // canonical digit planes [20][M][N] (det_gemm_partial), or null
+};
+
+// Exact GEMM; writes C (if args.C) or the digit planes P (if args.P).
+cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+
+constexpr int kMaxPartsPerLaunch = 16;
+
+// out = canonical(sum of parts), over count = M*N outputs of 20 planes each.
+cudaError_t launch_combine(const int64_t* const* parts, int n, int64_t count, int64_t* out,
+                           cudaStream_t stream);
+
+// C[m*ldc+n] = RNE_f32(value of P[:, m, n]).
+cudaError_t launch_finalize(const int64_t* P, int64_t M, int64_t N, float* C, int64_t ldc,
+                            cudaStream_t stream);
+
+}  // namespace det

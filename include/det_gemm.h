@@ -1,0 +1,148 @@
+/*
+ * det_gemm.h -- C ABI of the exact-sum (Kulisch long-accumulator) GEMM.
+ *
+ * What the library computes (det-train page, section "Method"): each output
+ * of C = A * B^T owns a fixed array of signed int64 digits of radix 2^32 that
+ * spans the whole range of an fp32 x fp32 product.  Every bf16/f32 product is
+ * formed exactly, its base-2^32 limbs are added into those digits with exact
+ * integer additions, and the final digits are carry-normalised and rounded
+ * ONCE to fp32 with round-to-nearest-even.  Integer addition is associative,
+ * so the result does not depend on tiling, K-sharding, fold order or
+ * repetition ("Sharded partials compose by adding digit arrays").
+ * The call names follow the page's usage section: det_gemm, det_gemm_partial,
+ * det_combine, det_finalize, and the forward/dgrad/wgrad of DetLinear.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - All data pointers are DEVICE pointers (CUDA), owned by the caller.  The
+ *    library never frees or retains them, and never synchronises the stream:
+ *    every call only enqueues work on `stream` (a cudaStream_t; NULL means the
+ *    legacy default stream) and returns.
+ *  - Operands: A is logically [M, K] and B is logically [N, K] ("x" and "w" of
+ *    the page, w laid out like nn.Linear.weight).  op = 0: the operand is
+ *    stored row-major as [rows, K] with K contiguous, element (r, k) at
+ *    X[r * ld + k], ld >= K.  op = 1: it is stored as [K, rows] with rows
+ *    contiguous, element (r, k) at X[k * ld + r], ld >= rows.
+ *    Both operands have the same dtype (DET_F32 or DET_BF16 bit patterns).
+ *  - Output C is fp32 [M, N] row-major, element (m, n) at C[m * ldc + n].
+ *  - K <= DET_K_MAX per call (det-train page, "Requirements and limits").
+ *    K = 0 is allowed: every digit is zero and every output is +0.0f.
+ *  - Digit arrays ("partials") are int64, planar [DET_PLANES][M][N],
+ *    contiguous: planes 0..17 are the digits (digit j weighs 2^(32j-298);
+ *    the smallest nonzero |product| is 2^-298 and the largest is below
+ *    2^256), plane 18 counts the products summed, plane 19 counts products
+ *    with a non-finite operand.  Arrays written by this library are canonical:
+ *    digits 0..16 in [0, 2^32), digit 17 signed.
+ *  - Rounding: exact zero -> +0.0f; a nonzero sum that rounds to zero keeps
+ *    its sign; overflow -> +-inf; an output with any non-finite product is the
+ *    canonical NaN 0x7FC00000 (the page does not treat Inf/NaN inputs).
+ *  - Errors: argument errors are detected on the host and returned before
+ *    anything is enqueued.  DET_ERR_CUDA reports a failed launch or CUDA call;
+ *    nothing throws across the ABI.
+ */
+#ifndef DET_GEMM_H
+#define DET_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DET_OK = 0,
+  DET_ERR_INVALID_ARG = 1, /* null pointer, bad op flag or leading dimension */
+  DET_ERR_DTYPE = 2,       /* dtype is not DET_F32 / DET_BF16 */
+  DET_ERR_SHAPE = 3,       /* negative or too large M, N, K or part count */
+  DET_ERR_K_LIMIT = 4,     /* K > DET_K_MAX */
+  DET_ERR_OVERFLOW = 5,    /* digit headroom would be exceeded (combine of too many parts) */
+  DET_ERR_ALIGNMENT = 6,   /* a pointer is not aligned to its element size */
+  DET_ERR_CUDA = 7         /* a CUDA call or kernel launch failed */
+} det_status;
+
+typedef enum { DET_F32 = 0, DET_BF16 = 1 } det_dtype;
+
+enum {
+  DET_DIGITS = 18,             /* radix-2^32 digits per output */
+  DET_PLANES = 20,             /* digits + product count + non-finite count */
+  DET_K_MAX = 1 << 19,         /* largest K of one GEMM call */
+  DET_MAX_COMBINE = 1 << 20    /* most partials one det_combine call accepts */
+};
+
+/* Version of this ABI (bumped on any incompatible change). */
+int det_abi_version(void);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* det_status_string(det_status s);
+
+/* Number of kernels this library has enqueued in this process so far (all
+ * devices, all threads).  A diagnostic for benchmarks and tests. */
+uint64_t det_kernel_launches(void);
+
+/*
+ * det_gemm -- C = RNE_f32( sum_k A(m,k) * B(n,k) ), computed exactly.
+ * det-train page, usage section ("det_gemm(x, w)") and section "Method".
+ * Enqueues the exponent pre-pass and the accumulate kernel on `stream`; the
+ * digits are never written to memory (finalize is fused).  A and B must be
+ * aligned to their element size, C to 4 bytes.
+ */
+det_status det_gemm(det_dtype dtype, int64_t M, int64_t N, int64_t K,
+                    const void* A, int64_t lda, int opA,
+                    const void* B, int64_t ldb, int opB,
+                    float* C, int64_t ldc, void* stream);
+
+/*
+ * det_gemm_partial -- the same exact accumulation, written out unrounded as a
+ * canonical digit array P [DET_PLANES][M][N] (8-byte aligned, contiguous,
+ * M*N*160 bytes).  det-train page, usage section ("det_gemm_partial") and
+ * section "Method" ("Sharded partials compose by adding digit arrays").
+ * Plane 18 is set to K.
+ */
+det_status det_gemm_partial(det_dtype dtype, int64_t M, int64_t N, int64_t K,
+                            const void* A, int64_t lda, int opA,
+                            const void* B, int64_t ldb, int opB,
+                            int64_t* P, void* stream);
+
+/*
+ * det_combine -- out = sum_i parts[i], elementwise over all DET_PLANES planes,
+ * then carry-normalised to canonical form.  det-train page, usage section
+ * ("det_combine([a1, a2])") and section "Method".  `parts` is a HOST array of
+ * n >= 1 device pointers, each to a [DET_PLANES][M][N] int64 array; `out` may
+ * alias any of them.  Inputs need not be canonical, but the per-digit sums
+ * must stay below 2^62 in magnitude (always true for up to DET_MAX_COMBINE
+ * canonical parts).  n > DET_MAX_COMBINE returns DET_ERR_OVERFLOW.
+ */
+det_status det_combine(int64_t M, int64_t N, const int64_t* const* parts, int n,
+                       int64_t* out, void* stream);
+
+/*
+ * det_finalize -- round a digit array once to fp32.  det-train page, usage
+ * section ("det_finalize(acc)") and section "Method" (carry-normalise, round
+ * once, round-to-nearest-even).  P is [DET_PLANES][M][N] int64 with digits of
+ * magnitude below 2^62; C is fp32 [M, N] with leading dimension ldc >= N.
+ */
+det_status det_finalize(int64_t M, int64_t N, const int64_t* P, float* C, int64_t ldc,
+                        void* stream);
+
+/*
+ * DetLinear (det-train page, usage section: "DetLinear(4096, 4096)",
+ * "y = layer(x); y.square().mean().backward()  # deterministic fwd and bwd").
+ * Bias-free; every GEMM is an exact det_gemm:
+ *   forward: y[b,o]  = sum_i x[b,i]  W[o,i]   x [batch,in], W [out,in], y [batch,out]
+ *   dgrad:   dx[b,i] = sum_o dy[b,o] W[o,i]   dy [batch,out], dx [batch,in]
+ *   wgrad:   dW[o,i] = sum_b dy[b,o] x[b,i]   dW [out,in]  (K = batch <= DET_K_MAX)
+ * All tensors are contiguous row-major; gradients are fp32.
+ */
+det_status det_linear_forward(det_dtype dtype, int64_t batch, int64_t in_features,
+                              int64_t out_features, const void* x, const void* W, float* y,
+                              void* stream);
+det_status det_linear_dgrad(int64_t batch, int64_t in_features, int64_t out_features,
+                            const float* dy, const float* W, float* dx, void* stream);
+det_status det_linear_wgrad(int64_t batch, int64_t in_features, int64_t out_features,
+                            const float* dy, const float* x, float* dW, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DET_GEMM_H */

@@ -1,0 +1,76 @@
+"""CPU checks of the C-ABI library: it builds, loads without a GPU, exports every
+function that include/det_gemm.h declares, and rejects bad arguments on the
+host before touching CUDA.  No compute call is made here."""
+import os
+import re
+
+import pytest
+
+import exact_sum_gemm_gb300 as dg
+from exact_sum_gemm_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "det_gemm.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(det_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_pages_calls():
+    names = declared_functions()
+    for want in ["det_gemm", "det_gemm_partial", "det_combine", "det_finalize",
+                 "det_linear_forward", "det_linear_dgrad", "det_linear_wgrad"]:
+        assert want in names
+
+
+def test_library_loads_and_exports_every_declared_symbol():
+    lib = dg.library()
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _native.SIGNATURES, f"{name} has no ctypes signature"
+    assert lib.det_abi_version() == 1
+
+
+def test_status_strings():
+    lib = dg.library()
+    for code, name in _native.STATUS_NAMES.items():
+        assert lib.det_status_string(code).decode().startswith(name)
+
+
+def test_host_side_validation_without_gpu():
+    lib = dg.library()
+    S = None
+    # K limit (det-train page, "Requirements and limits": K <= 2^19 per call)
+    assert lib.det_gemm(0, 1, 1, (1 << 19) + 1, 4, 1 << 20, 0, 4, 1 << 20, 0, 4, 1, S) == 4
+    assert lib.det_gemm_partial(1, 1, 1, (1 << 19) + 1, 4, 1 << 20, 0, 4, 1 << 20, 0, 8, S) == 4
+    assert lib.det_gemm(7, 1, 1, 1, 4, 1, 0, 4, 1, 0, 4, 1, S) == 2          # dtype
+    assert lib.det_gemm(0, -1, 1, 1, 4, 1, 0, 4, 1, 0, 4, 1, S) == 3         # shape
+    assert lib.det_gemm(0, 2, 2, 4, None, 4, 0, 4, 4, 0, 4, 2, S) == 1       # null A
+    assert lib.det_gemm(0, 2, 2, 4, 4, 3, 0, 4, 4, 0, 4, 2, S) == 1          # lda < K
+    assert lib.det_gemm(0, 2, 2, 4, 4, 1, 1, 4, 4, 0, 4, 2, S) == 1          # op 1, lda < M
+    assert lib.det_gemm(0, 2, 2, 4, 4, 4, 2, 4, 4, 0, 4, 2, S) == 1          # bad op
+    assert lib.det_gemm(0, 2, 2, 4, 6, 4, 0, 4, 4, 0, 4, 2, S) == 6          # misaligned f32
+    assert lib.det_gemm(1, 2, 2, 4, 5, 4, 0, 4, 4, 0, 4, 2, S) == 6          # misaligned bf16
+    assert lib.det_gemm(0, 2, 2, 4, 4, 4, 0, 4, 4, 0, 4, 1, S) == 1          # ldc < N
+    assert lib.det_gemm(0, 2, 2, 4, 4, 4, 0, 4, 4, 0, 6, 2, S) == 6          # misaligned C
+    assert lib.det_gemm(0, 0, 5, 4, None, 4, 0, None, 4, 0, None, 5, S) == 0  # empty: no-op
+    assert lib.det_gemm_partial(0, 2, 2, 4, 4, 4, 0, 4, 4, 0, 12, S) == 6    # misaligned P
+    import ctypes
+    arr = (ctypes.c_void_p * 2)(8, 16)
+    assert lib.det_combine(2, 2, arr, 0, 8, S) == 3                          # no parts
+    assert lib.det_combine(2, 2, arr, (1 << 20) + 1, 8, S) == 5              # too many parts
+    assert lib.det_combine(2, 2, arr, 2, 12, S) == 6                         # misaligned out
+    bad = (ctypes.c_void_p * 2)(8, None)
+    assert lib.det_combine(2, 2, bad, 2, 8, S) == 1
+    assert lib.det_finalize(2, 2, 8, 4, 1, S) == 1                           # ldc < N
+    assert lib.det_finalize(2, 2, 12, 4, 2, S) == 6
+    assert lib.det_linear_wgrad((1 << 19) + 1, 4, 4, 4, 4, 4, S) == 4        # K = batch
+
+
+def test_python_layer_rejects_host_tensors():
+    import torch
+    with pytest.raises(ValueError, match="CUDA"):
+        dg.det_gemm(torch.ones(2, 3), torch.ones(2, 3))

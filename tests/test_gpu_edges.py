@@ -1,0 +1,208 @@
+"""GPU edge cases against the oracle: worked cases, tiny/ragged/empty shapes,
+operand layouts, subnormals, non-finite inputs, raw digit arrays, errors."""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import exact_sum_gemm_gb300 as dg
+from exact_sum_gemm_gb300 import workloads as wl
+from gpu_util import assert_bits_equal, bits_of, dev_bf16, dev_f32, np_bits
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "worked_cases.json")
+
+
+def _hexf(s):
+    return float.fromhex(s) if s not in ("inf", "-inf", "nan") else float(s)
+
+
+def _cases():
+    with open(GOLDEN) as f:
+        for case in json.load(f)["cases"]:
+            for dt in case["dtypes"]:
+                yield pytest.param(case, dt, id=f"{case['name']}-{dt}")
+
+
+@pytest.mark.parametrize("case,dtype", list(_cases()))
+def test_worked_cases_on_gpu(case, dtype):
+    a = np.array([[_hexf(v) for v in case["a"]]], np.float32)
+    b = np.array([[_hexf(v) for v in case["b"]]], np.float32)
+    want = int(case["expected"], 16)
+    # replicate into a ragged 35x33 tile so several CTAs and positions see it
+    A = np.repeat(a, 35, axis=0)
+    B = np.repeat(b, 33, axis=0)
+    if dtype == "bf16":
+        ta = dev_bf16((A.view(np.uint32) >> 16).astype(np.uint16))
+        tb = dev_bf16((B.view(np.uint32) >> 16).astype(np.uint16))
+    else:
+        ta, tb = dev_f32(A), dev_f32(B)
+    got = bits_of(dg.det_gemm(ta, tb))
+    assert np.all(got == want), f"got {got.ravel()[0]:#010x} want {want:#010x}"
+    got_p = bits_of(dg.det_finalize(dg.det_gemm_partial(ta, tb)))
+    assert np.all(got_p == want)
+
+
+def _rand(g, shape, mode):
+    if mode == "normal":
+        return g.standard_normal(shape).astype(np.float32)
+    if mode == "wide":
+        e = g.integers(-149, 128, size=shape)
+        x = np.ldexp(g.random(shape) + 1.0, e).astype(np.float32)
+        return np.where(g.random(shape) < 0.5, -x, x).astype(np.float32)
+    if mode == "subnormal":
+        bits = g.integers(0, 1 << 23, size=shape).astype(np.uint32)
+        bits |= g.integers(0, 2, size=shape).astype(np.uint32) << 31
+        return bits.view(np.float32)
+    if mode == "zeros":
+        x = g.standard_normal(shape).astype(np.float32)
+        x[g.random(shape) < 0.6] = 0.0
+        return x
+    raise ValueError(mode)
+
+
+SHAPES = [(1, 1, 1), (1, 1, 0), (3, 2, 0), (2, 3, 7), (7, 33, 3), (33, 7, 33), (33, 33, 65),
+          (65, 31, 100), (31, 97, 129), (100, 1, 1000)]
+
+
+@pytest.mark.parametrize("mode", ["normal", "wide", "subnormal", "zeros"])
+def test_tiny_and_ragged_shapes(oracle_mod, mode):
+    g = np.random.default_rng(hash(mode) % 1000)
+    for M, N, K in SHAPES:
+        A = _rand(g, (M, K), mode)
+        B = _rand(g, (N, K), mode)
+        a, b = dev_f32(A), dev_f32(B)
+        want = np_bits(oracle_mod.gemm(A, B))
+        assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, f"{mode} {M}x{N}x{K}")
+        np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(),
+                                      oracle_mod.gemm_digits(A, B), err_msg=f"{mode} {M}x{N}x{K}")
+
+
+def test_k_zero_gives_positive_zero():
+    a = torch.empty((5, 0), device="cuda")
+    b = torch.empty((4, 0), device="cuda")
+    assert np.all(bits_of(dg.det_gemm(a, b)) == 0)
+    P = dg.det_gemm_partial(a, b).cpu().numpy()
+    assert np.all(P == 0)
+
+
+def test_empty_m_or_n():
+    a = torch.empty((0, 8), device="cuda")
+    b = torch.ones((4, 8), device="cuda")
+    assert dg.det_gemm(a, b).shape == (0, 4)
+    assert dg.det_gemm(b, a).shape == (4, 0)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_operand_layouts_and_strides(oracle_mod, dtype):
+    g = np.random.default_rng(21)
+    M, N, K = 70, 45, 130
+    if dtype == "f32":
+        A = _rand(g, (M, K), "wide")
+        B = _rand(g, (N, K), "normal")
+        to_dev = dev_f32
+        want = np_bits(oracle_mod.gemm(A, B))
+    else:
+        A, B, _ = wl.bf16_wide_with_cancellation(M, N, K, seed=4)
+        to_dev = dev_bf16
+        want = np_bits(oracle_mod.gemm(A, B, dtype="bf16"))
+    a, b = to_dev(A), to_dev(B)
+    at = to_dev(np.ascontiguousarray(A.T)).t()          # [M,K] view with unit row stride: op 1
+    bt = to_dev(np.ascontiguousarray(B.T)).t()
+    for x, w, tag in [(a, b, "NN"), (at, b, "TN"), (a, bt, "NT"), (at, bt, "TT")]:
+        assert_bits_equal(bits_of(dg.det_gemm(x, w)), want, tag)
+    # padded leading dimensions (slices of wider buffers)
+    big_a = to_dev(np.concatenate([A, A[:, :17]], axis=1))[:, :K]
+    big_b = to_dev(np.concatenate([B.T, B.T[:, :5]], axis=1)).t()[:N]
+    assert big_a.stride() != a.stride()
+    assert_bits_equal(bits_of(dg.det_gemm(big_a, big_b)), want, "padded ld")
+
+
+def test_bf16_subnormals_and_extremes(oracle_mod):
+    g = np.random.default_rng(31)
+    a = g.integers(0, 1 << 16, size=(40, 300)).astype(np.uint16)
+    b = g.integers(0, 1 << 16, size=(36, 300)).astype(np.uint16)
+    a[(a & 0x7F80) == 0x7F80] &= 0xBFFF          # finite patterns only
+    b[(b & 0x7F80) == 0x7F80] &= 0xBFFF
+    a[:, :50] &= 0x807F                           # a band of subnormals / zeros
+    want = np_bits(oracle_mod.gemm(a, b, dtype="bf16"))
+    assert_bits_equal(bits_of(dg.det_gemm(dev_bf16(a), dev_bf16(b))), want, "bf16 all patterns")
+
+
+def test_nonfinite_inputs(oracle_mod):
+    g = np.random.default_rng(41)
+    A = g.standard_normal((40, 90)).astype(np.float32)
+    B = g.standard_normal((50, 90)).astype(np.float32)
+    A[3, 7] = np.inf
+    A[10, 80] = np.nan
+    B[5, 7] = -np.inf
+    B[20, 1] = np.nan
+    B[21, 2] = 0.0
+    A[:, 2] = np.inf                              # inf * 0 for column 21
+    a, b = dev_f32(A), dev_f32(B)
+    want = np_bits(oracle_mod.gemm(A, B))
+    got = bits_of(dg.det_gemm(a, b))
+    assert_bits_equal(got, want, "non-finite")
+    assert np.all(got[:, 21] == 0x7FC00000)
+    np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(),
+                                  oracle_mod.gemm_digits(A, B))
+
+
+def test_finalize_and_combine_raw_digit_arrays(oracle_mod):
+    g = np.random.default_rng(51)
+    M, N = 37, 29                                  # odd count: scalar kernels
+    parts = []
+    for i in range(19):                            # more than one combine launch
+        P = np.zeros((20, M, N), np.int64)
+        P[:18] = g.integers(-(2 ** 40), 2 ** 40, size=(18, M, N))
+        P[17] = g.integers(-(2 ** 8), 2 ** 8, size=(M, N))
+        P[:, :3] = g.integers(-2, 3, size=(20, 3, N))
+        P[18] = g.integers(0, 1000, size=(M, N))
+        P[19] = (g.random((M, N)) < 0.02).astype(np.int64)
+        parts.append(P)
+    dparts = [torch.from_numpy(p).cuda() for p in parts]
+    for P, dP in zip(parts, dparts):
+        assert_bits_equal(bits_of(dg.det_finalize(dP)), np_bits(oracle_mod.finalize(P)), "finalize")
+    total = np.sum(np.stack(parts), axis=0)
+    want = oracle_mod.canonicalize(total)
+    got = dg.det_combine(dparts).cpu().numpy()
+    np.testing.assert_array_equal(got, want)
+    assert_bits_equal(bits_of(dg.det_finalize(torch.from_numpy(got).cuda())),
+                      np_bits(oracle_mod.finalize(total)), "finalize of combined")
+    # out aliasing the first input
+    alias = dparts[0].clone()
+    dg.det_combine([alias] + dparts[1:4], out=alias)
+    np.testing.assert_array_equal(alias.cpu().numpy(),
+                                  oracle_mod.canonicalize(np.sum(np.stack(parts[:4]), axis=0)))
+    # even count, 16-byte aligned: vector kernels; strided output for finalize
+    P2 = np.ascontiguousarray(np.stack(parts)[:, :, :36, :28].sum(axis=0))
+    out = torch.zeros((36, 40), device="cuda")
+    dg.det_finalize(torch.from_numpy(P2).cuda(), out=out[:, :28])
+    assert_bits_equal(bits_of(out[:, :28]), np_bits(oracle_mod.finalize(P2)), "strided finalize")
+    assert np.all(bits_of(out[:, 28:]) == 0)
+
+
+def test_argument_errors():
+    a = torch.ones((4, 8), device="cuda")
+    b = torch.ones((3, 8), device="cuda")
+    with pytest.raises(ValueError, match="K mismatch"):
+        dg.det_gemm(a, torch.ones((3, 9), device="cuda"))
+    with pytest.raises(ValueError):
+        dg.det_gemm(a.half(), b.half())
+    with pytest.raises(ValueError):
+        dg.det_gemm(a, b.bfloat16())
+    big = torch.zeros((1, (1 << 19) + 1), device="cuda")
+    with pytest.raises(ValueError, match="K_LIMIT"):
+        dg.det_gemm(big, big)
+    ok = torch.zeros((1, 1 << 19), device="cuda")
+    assert bits_of(dg.det_gemm(ok, ok))[0, 0] == 0
+    # misaligned f32 pointer through the raw C ABI
+    raw = torch.zeros(64, device="cuda")
+    lib = dg.library()
+    st = lib.det_gemm(0, 2, 2, 4, raw.data_ptr() + 2, 4, 0, raw.data_ptr(), 4, 0,
+                      raw.data_ptr(), 2, torch.cuda.current_stream().cuda_stream)
+    assert st == 6
+    torch.cuda.synchronize()
