@@ -7,7 +7,7 @@ in HBM; between steps a 256 MiB buffer is written to flush the 129 MB L2.
 Metric: exact-GEMM GFLOP/s = 2 M N K / t (whole job, summed over ranks).
 
 Printed as one JSON line on rank 0, with:
-  roofline      dominant kernel vs the integer-ALU issue peak (see DESIGN.md)
+  roofline      dominant kernel vs the integer-ALU issue peak
   cpu_baseline  the CPU oracle on a bounded row sample of the same workload
   e2e           the same metric through the public API from pinned host
                 buffers, copies included
@@ -53,11 +53,17 @@ def parse_args():
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--workload", choices=["normal", "wide"], default="normal",
                    help="normal: N(0,1) (the headline); wide: |x| = 2^U[-40,40]")
-    p.add_argument("--cpu-rows", type=int, default=64,
+    p.add_argument("--cpu-rows", type=int, default=512,
                    help="rows of the 4096^3 problem the CPU baseline samples")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the e2e, sharded and CPU-baseline measurements")
-    return p.parse_args()
+    p.add_argument("--mnk", type=int, nargs=3, default=None, metavar=("M", "N", "K"),
+                   help="override the problem size (profiling of small cases only)")
+    args = p.parse_args()
+    if args.mnk:
+        global M, N, K
+        M, N, K = args.mnk
+    return args
 
 
 def dist_env():

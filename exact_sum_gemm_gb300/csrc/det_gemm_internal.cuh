@@ -1,0 +1,38 @@
+// Shared constants and launch plumbing of the exact GEMM kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "det_kernels.h"
+
+namespace det {
+
+constexpr int kTile = 64;                 // band kernel output tile (and routing unit)
+constexpr int kDeepGap = 15;              // "deep" element: more than 15 binades below its row max
+constexpr int kDeepRouteDen = 64;         // route a tile to the general kernel if deep > K/64
+constexpr int kEmaxEmpty = static_cast<int>(0x80808080u);   // memset(0x80) pattern: no live element
+
+// Device scratch of one det_gemm / det_gemm_partial call.
+struct Scratch {
+  int* emaxA;          // [M]   (emaxB follows contiguously)
+  int* emaxB;          // [N]
+  int* deepA;          // [M]   (deepB follows contiguously)
+  int* deepB;          // [N]
+  uint8_t* route;      // [tiles of 64x64]: 1 = general kernel
+  int64_t* fallback;   // [slots][kPlanes][kTile*kTile] band-kernel fallback digits (det_gemm only)
+  int64_t slots;       // resident band-kernel CTAs (fallback regions)
+};
+
+// Bytes of scratch a call needs, and how to carve it out of one allocation.
+size_t scratch_bytes(const GemmArgs& g, int64_t slots);
+Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots);
+
+cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
+cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
+cudaError_t launch_kulisch(const GemmArgs& g, const uint8_t* route, cudaStream_t stream);
+
+// Band-kernel CTAs resident on the current device (persistent grid size).
+int64_t band_slots(const GemmArgs& g);
+
+}  // namespace det

@@ -1,0 +1,372 @@
+// Band kernel of the exact GEMM: the fast path for operands whose exponents
+// sit within ~31 binades of their row maxima (N(0,1)-like data, activations,
+// gradients).
+//
+// det-train page, section "Method": every product is formed exactly and its
+// base-2^32 limbs are added with exact integer additions into the output's
+// digits.  Here each output keeps, in three registers, a 96-bit two's-
+// complement window ("band") of its digit array anchored at
+//     base(m,n) = emaxA[m] + emaxB[n] - 31        (bit weight of band bit 0),
+// where emax is the largest last-bit exponent of the operand's row (from the
+// pre-pass).  A product mA*mB*2^(eA+eB) (|mA*mB| < 2^48) lands at band bit
+//     t = (eA - emaxA[m]) + (eB - emaxB[n] + 31)  <=  31.
+// If 0 <= t <= 31 it is added to the band exactly: (mA*mB) << t split into
+// three 32-bit words by funnel shifts, then one 3-word carry chain
+// (IMAD.WIDE + 3 SHF + 1 sign + 3 IADD-with-carry).  The band holds 2^16
+// such products without overflow, and is flushed into the digits every 2^15
+// products.  A product with t < 0 (an operand more than 31 binades below its
+// row max, rare by routing) or a non-finite operand takes an exact fallback:
+// its two limbs are added to the output's int64 digits kept in global memory
+// (the det_gemm_partial output itself, or a per-CTA scratch region for
+// det_gemm), zeroed on first touch.  No product is ever dropped or rounded.
+//
+// Tiles: 64x64 outputs per 256-thread CTA, 4x4 outputs per thread, K staged in
+// chunks of 32 through double-buffered shared memory as decoded (signed
+// significand, exponent offset) pairs.  The grid is persistent: one CTA per
+// resident slot loops over the tiles that routing gave to this kernel.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "det_arith.cuh"
+#include "det_gemm_internal.cuh"
+#include "det_kernels.h"
+
+namespace det {
+namespace {
+
+constexpr int kBK = 32;
+constexpr int kThreads = 256;
+constexpr int kStride = kTile + 2;                 // int2 per staged k-row (16-byte aligned rows)
+constexpr int kSent = -(1 << 28);                  // exponent offset marking a non-finite operand
+constexpr int kSentCheck = -(1 << 27);
+constexpr int kFlushChunks = (1 << 15) / kBK;      // band -> digits every 2^15 products
+constexpr int kTileOut = kTile * kTile;
+constexpr int kLoads = kTile * kBK / kThreads;     // elements per thread per operand per chunk
+
+struct BandSmem {
+  int2 a[2][kBK][kStride];
+  int2 b[2][kBK][kStride];
+  int emaxA[kTile];
+  int emaxB[kTile];
+};
+
+// Where the fallback digits of one output live: plane p at base[p * stride].
+struct DigitRef {
+  int64_t* base;
+  int64_t stride;
+};
+
+__device__ __forceinline__ void add_product_digits(DigitRef d, int off, int64_t prod) {
+  const uint32_t p0 = static_cast<uint32_t>(prod);
+  const uint32_t p1 = static_cast<uint32_t>(static_cast<uint64_t>(prod) >> 32);
+  const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(p1) >> 31);
+  const uint32_t lo = __funnelshift_l(0u, p0, off);
+  const uint32_t h0 = __funnelshift_l(p0, p1, off);
+  const uint32_t h1 = __funnelshift_l(p1, sx, off);
+  int64_t* q = d.base + (off >> 5) * d.stride;
+  q[0] += static_cast<int64_t>(lo);
+  q[d.stride] += static_cast<int64_t>((static_cast<uint64_t>(h1) << 32) | h0);
+}
+
+// The band (b0,b1,b2: a signed 96-bit value whose bit 0 weighs 2^(base-298))
+// as four signed pieces of the digit array starting at digit *j.
+__device__ __forceinline__ void band_pieces(uint32_t b0, uint32_t b1, uint32_t b2, int base,
+                                            int& j, int64_t (&y)[4]) {
+  if (base < 0) {                       // the band's low bits are zero (products are
+    const int s = -base;                // multiples of 2^-298): shift them out exactly
+    b0 = __funnelshift_r(b0, b1, s);
+    b1 = __funnelshift_r(b1, b2, s);
+    b2 = static_cast<uint32_t>(static_cast<int32_t>(b2) >> s);
+    base = 0;
+  }
+  const int sh = base & 31;
+  const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(b2) >> 31);
+  j = base >> 5;
+  y[0] = static_cast<int64_t>(b0 << sh);
+  y[1] = static_cast<int64_t>(__funnelshift_l(b0, b1, sh));
+  y[2] = static_cast<int64_t>(__funnelshift_l(b1, b2, sh));
+  y[3] = static_cast<int64_t>(static_cast<int32_t>(__funnelshift_l(b2, sx, sh)));
+}
+
+static_assert(sizeof(uint32_t) * 48 * kThreads <= sizeof(int2) * 4 * kBK * kStride,
+              "epilogue band staging must fit in the operand staging buffers");
+
+template <int kBf16>
+__global__ void __launch_bounds__(kThreads, 2) band_kernel(GemmArgs p, Scratch s) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  BandSmem& sm = *reinterpret_cast<BandSmem*>(smem_raw);
+  const int tid = threadIdx.x;
+  const int ty = tid >> 4, tx = tid & 15;
+  const int64_t tiles_n = (p.N + kTile - 1) / kTile;
+  const int64_t tiles = ((p.M + kTile - 1) / kTile) * tiles_n;
+  const int64_t nchunks = (p.K + kBK - 1) / kBK;
+  const int64_t MN = p.M * p.N;
+  int64_t* slot_digits = s.fallback ? s.fallback + int64_t(blockIdx.x) * kPlanes * kTileOut : nullptr;
+
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+    if (s.route[tile]) continue;                       // tile belongs to the general kernel
+    const int64_t tm = tile / tiles_n, tn = tile - tm * tiles_n;
+    const int64_t m0 = tm * kTile, n0 = tn * kTile;
+
+    __syncthreads();                                   // previous tile done with smem
+    if (tid < kTile) {
+      const int64_t m = m0 + tid;
+      const int v = m < p.M ? s.emaxA[m] : kEmaxEmpty;
+      sm.emaxA[tid] = v == kEmaxEmpty ? 0 : v;
+    } else if (tid < 2 * kTile) {
+      const int64_t n = n0 + tid - kTile;
+      const int v = n < p.N ? s.emaxB[n] : kEmaxEmpty;
+      sm.emaxB[tid - kTile] = v == kEmaxEmpty ? 0 : v;
+    }
+    __syncthreads();
+
+    uint32_t band[16][3];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) band[q][0] = band[q][1] = band[q][2] = 0u;
+    uint32_t touched = 0;                              // bit q: output q has fallback digits
+
+    // fallback digit location of output q (only called for in-range outputs)
+    auto digit_ref = [&](int q) -> DigitRef {
+      const int r = ty * 4 + (q >> 2), c = tx * 4 + (q & 3);
+      if (p.P) return DigitRef{p.P + (m0 + r) * p.N + (n0 + c), MN};
+      return DigitRef{slot_digits + r * kTile + c, kTileOut};
+    };
+    auto in_range = [&](int q) -> bool {
+      return (m0 + ty * 4 + (q >> 2)) < p.M && (n0 + tx * 4 + (q & 3)) < p.N;
+    };
+    auto touch = [&](int q) -> DigitRef {
+      DigitRef d = digit_ref(q);
+      if (!((touched >> q) & 1u)) {
+#pragma unroll 1
+        for (int pl = 0; pl < kPlanes; ++pl) d.base[pl * d.stride] = 0;
+        touched |= 1u << q;
+      }
+      return d;
+    };
+    auto band_base = [&](int q) -> int {
+      return sm.emaxA[ty * 4 + (q >> 2)] + sm.emaxB[tx * 4 + (q & 3)] - 31 + kLsbBias;
+    };
+    auto fallback = [&](int q, int ea, int eb, int64_t prod) {
+      if (!in_range(q)) return;
+      if (ea < kSentCheck || eb < kSentCheck) {
+        DigitRef d = touch(q);
+        d.base[(kPlanes - 1) * d.stride] += 1;         // non-finite product count
+      } else if (prod != 0) {
+        DigitRef d = touch(q);
+        add_product_digits(d, ea + eb + band_base(q), prod);
+      }
+    };
+    // add one band (by value) into its output's digits and renormalise them
+    auto flush_band = [&](int q, uint32_t b0, uint32_t b1, uint32_t b2) {
+      if (!in_range(q)) return;
+      DigitRef d = touch(q);
+      int j;
+      int64_t y[4];
+      band_pieces(b0, b1, b2, band_base(q), j, y);
+      int64_t* dj = d.base + j * d.stride;
+#pragma unroll
+      for (int u = 0; u < 4; ++u) dj[u * d.stride] += y[u];
+      int64_t carry = 0;                               // keep the digits well inside int64
+#pragma unroll 1
+      for (int pl = 0; pl < kDigits - 1; ++pl) {
+        const int64_t v = d.base[pl * d.stride] + carry;
+        d.base[pl * d.stride] = static_cast<int64_t>(static_cast<uint32_t>(v));
+        carry = v >> 32;
+      }
+      d.base[(kDigits - 1) * d.stride] += carry;
+    };
+
+    uint32_t ra[kLoads], rb[kLoads];
+    auto load_chunk = [&](int64_t k0) {
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int idx = tid + kThreads * u;
+        {
+          const int r = p.opA ? (idx & 63) : (idx >> 5);
+          const int k = p.opA ? (idx >> 6) : (idx & 31);
+          const int64_t gm = m0 + r, gk = k0 + k;
+          ra[u] = (gm < p.M && gk < p.K)
+                      ? load_bits<kBf16>(p.A, p.opA ? gk * p.lda + gm : gm * p.lda + gk)
+                      : 0u;
+        }
+        {
+          const int r = p.opB ? (idx & 63) : (idx >> 5);
+          const int k = p.opB ? (idx >> 6) : (idx & 31);
+          const int64_t gn = n0 + r, gk = k0 + k;
+          rb[u] = (gn < p.N && gk < p.K)
+                      ? load_bits<kBf16>(p.B, p.opB ? gk * p.ldb + gn : gn * p.ldb + gk)
+                      : 0u;
+        }
+      }
+    };
+    auto store_chunk = [&](int buf) {
+#pragma unroll
+      for (int u = 0; u < kLoads; ++u) {
+        const int idx = tid + kThreads * u;
+        {
+          const int r = p.opA ? (idx & 63) : (idx >> 5);
+          const int k = p.opA ? (idx >> 6) : (idx & 31);
+          const Decoded d = decode_f32_bits(ra[u]);
+          const int e = d.nonfinite ? kSent : (d.m == 0 ? 0 : d.e - sm.emaxA[r]);
+          sm.a[buf][k][r] = make_int2(d.m, e);
+        }
+        {
+          const int r = p.opB ? (idx & 63) : (idx >> 5);
+          const int k = p.opB ? (idx >> 6) : (idx & 31);
+          const Decoded d = decode_f32_bits(rb[u]);
+          const int e = d.nonfinite ? kSent : (d.m == 0 ? 31 : d.e - sm.emaxB[r] + 31);
+          sm.b[buf][k][r] = make_int2(d.m, e);
+        }
+      }
+    };
+
+    if (nchunks > 0) {
+      load_chunk(0);
+      store_chunk(0);
+    }
+    __syncthreads();
+
+    for (int64_t c = 0; c < nchunks; ++c) {
+      const int buf = static_cast<int>(c & 1);
+      if (c + 1 < nchunks) load_chunk((c + 1) * kBK);
+#pragma unroll 2
+      for (int kk = 0; kk < kBK; ++kk) {
+        const int4 a01 = *reinterpret_cast<const int4*>(&sm.a[buf][kk][ty * 4]);
+        const int4 a23 = *reinterpret_cast<const int4*>(&sm.a[buf][kk][ty * 4 + 2]);
+        const int4 b01 = *reinterpret_cast<const int4*>(&sm.b[buf][kk][tx * 4]);
+        const int4 b23 = *reinterpret_cast<const int4*>(&sm.b[buf][kk][tx * 4 + 2]);
+        const int am[4] = {a01.x, a01.z, a23.x, a23.z};
+        const int ae[4] = {a01.y, a01.w, a23.y, a23.w};
+        const int bm[4] = {b01.x, b01.z, b23.x, b23.z};
+        const int be[4] = {b01.y, b01.w, b23.y, b23.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const int q = i * 4 + jj;
+            const int t = ae[i] + be[jj];
+            const int64_t prod = static_cast<int64_t>(am[i]) * static_cast<int64_t>(bm[jj]);
+            if (__builtin_expect(static_cast<unsigned>(t) <= 31u, 1)) {
+              const uint32_t p0 = static_cast<uint32_t>(prod);
+              const uint32_t p1 = static_cast<uint32_t>(static_cast<uint64_t>(prod) >> 32);
+              const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(p1) >> 31);
+              const uint32_t x0 = p0 << t;
+              const uint32_t x1 = __funnelshift_l(p0, p1, t);
+              const uint32_t x2 = __funnelshift_l(p1, sx, t);
+              asm("add.cc.u32 %0, %0, %3;\n\t"
+                  "addc.cc.u32 %1, %1, %4;\n\t"
+                  "addc.u32 %2, %2, %5;"
+                  : "+r"(band[q][0]), "+r"(band[q][1]), "+r"(band[q][2])
+                  : "r"(x0), "r"(x1), "r"(x2));
+            } else {
+              fallback(q, ae[i], be[jj], prod);
+            }
+          }
+        }
+      }
+      if ((c + 1) % kFlushChunks == 0 && c + 1 < nchunks) {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) {
+          flush_band(q, band[q][0], band[q][1], band[q][2]);
+          band[q][0] = band[q][1] = band[q][2] = 0u;
+        }
+      }
+      if (c + 1 < nchunks) store_chunk(buf ^ 1);
+      __syncthreads();
+    }
+
+    // epilogue: band (+ fallback digits) -> normalise -> round once, or digits out.
+    // The bands go through shared memory (the staging buffers are free after the
+    // last barrier) so that the per-output loop below need not be unrolled.
+    uint32_t* bandbuf = reinterpret_cast<uint32_t*>(smem_raw);
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+#pragma unroll
+      for (int w = 0; w < 3; ++w) bandbuf[(q * 3 + w) * kThreads + tid] = band[q][w];
+    }
+#pragma unroll 1
+    for (int q = 0; q < 16; ++q) {
+      if (!in_range(q)) continue;
+      const int64_t m = m0 + ty * 4 + (q >> 2), n = n0 + tx * 4 + (q & 3);
+      int j;
+      int64_t y[4];
+      band_pieces(bandbuf[(q * 3) * kThreads + tid], bandbuf[(q * 3 + 1) * kThreads + tid],
+                  bandbuf[(q * 3 + 2) * kThreads + tid], band_base(q), j, y);
+      int64_t d[kDigits];
+      int64_t nf = 0;
+      if ((touched >> q) & 1u) {
+        const DigitRef r = digit_ref(q);
+#pragma unroll
+        for (int pl = 0; pl < kDigits; ++pl) d[pl] = r.base[pl * r.stride];
+        nf = r.base[(kPlanes - 1) * r.stride];
+      } else {
+#pragma unroll
+        for (int pl = 0; pl < kDigits; ++pl) d[pl] = 0;
+      }
+#pragma unroll
+      for (int pl = 0; pl < kDigits; ++pl) {
+        const int u = pl - j;
+        d[pl] += u == 0 ? y[0] : u == 1 ? y[1] : u == 2 ? y[2] : u == 3 ? y[3] : 0;
+      }
+      uint32_t w[kDigits - 1];
+      int64_t top;
+      normalise_digits(d, w, top);
+      if (p.P) {
+        int64_t* out = p.P + m * p.N + n;
+#pragma unroll
+        for (int pl = 0; pl < kDigits - 1; ++pl) out[pl * MN] = static_cast<int64_t>(w[pl]);
+        out[(kDigits - 1) * MN] = top;
+        out[kDigits * MN] = p.K;
+        out[(kDigits + 1) * MN] = nf;
+      } else {
+        reinterpret_cast<uint32_t*>(p.C)[m * p.ldc + n] =
+            nf ? kNanBits : round_to_f32_bits(w, top);
+      }
+    }
+  }
+}
+
+constexpr size_t kSmemBytes = sizeof(BandSmem);
+
+template <int kBf16>
+cudaError_t configure_t(int* per_sm) {
+  static int cached = 0;
+  if (cached == 0) {
+    cudaError_t e = cudaFuncSetAttribute(band_kernel<kBf16>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, band_kernel<kBf16>, kThreads, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    cached = n > 0 ? n : 1;
+  }
+  *per_sm = cached;
+  return cudaSuccess;
+}
+
+}  // namespace
+
+int64_t band_slots(const GemmArgs& g) {
+  int dev = 0, sms = 0, per_sm = 1;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  if ((g.bf16 ? configure_t<1>(&per_sm) : configure_t<0>(&per_sm)) != cudaSuccess) per_sm = 1;
+  const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
+  const int64_t cap = int64_t(sms) * per_sm;
+  return tiles < cap ? tiles : cap;
+}
+
+cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
+  if (s.slots <= 0) return cudaSuccess;
+  int per_sm = 1;
+  cudaError_t e = g.bf16 ? configure_t<1>(&per_sm) : configure_t<0>(&per_sm);
+  if (e != cudaSuccess) return e;
+  if (g.bf16) band_kernel<1><<<static_cast<unsigned>(s.slots), kThreads, kSmemBytes, stream>>>(g, s);
+  else band_kernel<0><<<static_cast<unsigned>(s.slots), kThreads, kSmemBytes, stream>>>(g, s);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace det

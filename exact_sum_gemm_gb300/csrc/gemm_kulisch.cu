@@ -19,6 +19,7 @@
 #include <stdint.h>
 
 #include "det_arith.cuh"
+#include "det_gemm_internal.cuh"
 #include "det_kernels.h"
 
 namespace det {
@@ -70,8 +71,11 @@ __device__ __forceinline__ void normalise_in_place(int64_t* acc_o) {
   acc_o[(kDigits - 1) * kOutputs] += carry;
 }
 
+// Persistent: each CTA loops over 32x32 tiles.  With a route table, a tile is
+// processed here only if its 64x64 parent tile was routed to this kernel.
 template <int kBf16>
-__global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p) {
+__global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
+                                                                    const uint8_t* route) {
   extern __shared__ __align__(16) unsigned char smem[];
   int64_t* acc = reinterpret_cast<int64_t*>(smem);
   int2* As = reinterpret_cast<int2*>(smem + kAccBytes);
@@ -80,12 +84,18 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p) {
   uint8_t* nfB = nfA + kFlagBytes;
 
   const int64_t tiles_n = (p.N + kBN - 1) / kBN;
-  const int64_t tm = blockIdx.x / tiles_n;
-  const int64_t tn = blockIdx.x - tm * tiles_n;
-  const int64_t m0 = tm * kBM, n0 = tn * kBN;
+  const int64_t tiles = ((p.M + kBM - 1) / kBM) * tiles_n;
+  const int64_t parents_n = (p.N + 2 * kBN - 1) / (2 * kBN);
   const int tid = threadIdx.x;
   const int ty = tid >> 4, tx = tid & 15;
 
+  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
+  const int64_t tm = tile / tiles_n;
+  const int64_t tn = tile - tm * tiles_n;
+  if (route != nullptr && !route[(tm >> 1) * parents_n + (tn >> 1)]) continue;
+  const int64_t m0 = tm * kBM, n0 = tn * kBN;
+
+  __syncthreads();                                    // previous tile done with smem
   for (int i = tid; i < kDigits * kOutputs; i += kThreads) acc[i] = 0;
 
   // global -> registers (raw bits) for one K chunk
@@ -216,10 +226,11 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p) {
       reinterpret_cast<uint32_t*>(p.C)[m * p.ldc + n] = bits;
     }
   }
+  }  // tile loop
 }
 
 template <int kBf16>
-cudaError_t launch_kulisch_t(const GemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_kulisch_t(const GemmArgs& a, const uint8_t* route, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kulisch_smem_kernel<kBf16>,
@@ -228,17 +239,21 @@ cudaError_t launch_kulisch_t(const GemmArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured = true;
   }
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
-  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(tiles), kThreads, kSmemBytes, stream>>>(a);
+  const int64_t grid = tiles < sms ? tiles : (sms > 0 ? sms : 1);
+  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, route);
   note_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_gemm(const GemmArgs& a, cudaStream_t stream) {
+cudaError_t launch_kulisch(const GemmArgs& a, const uint8_t* route, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
-  return a.bf16 ? launch_kulisch_t<1>(a, stream) : launch_kulisch_t<0>(a, stream);
+  return a.bf16 ? launch_kulisch_t<1>(a, route, stream) : launch_kulisch_t<0>(a, route, stream);
 }
 
 }  // namespace det

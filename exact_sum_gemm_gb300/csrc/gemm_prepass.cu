@@ -1,0 +1,161 @@
+// Exponent pre-pass of the exact GEMM, and per-tile routing.
+//
+// For every row r of an operand (a row of A, or a row of B = a column of C):
+//   emax[r] = the largest exponent e (weight of the last significand bit, see
+//             det_arith.cuh) over the row's nonzero finite elements;
+//   deep[r] = how many nonzero finite elements lie more than kDeepGap
+//             binades below emax[r].
+// The band kernel anchors each output's register window at emax_A + emax_B,
+// so a product leaves the window only if its operands are together more than
+// 31 binades below their rows' maxima, which needs a deep element on one
+// side.  A 64x64 output tile whose worst row plus worst column hold more
+// than K/64 deep elements is routed to the general kernel instead.  Routing
+// changes speed only: both kernels return the same exact digits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "det_arith.cuh"
+#include "det_gemm_internal.cuh"
+#include "det_kernels.h"
+
+namespace det {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowChunk = kThreads * 16;     // op 0: elements of one row per block
+constexpr int kColChunk = 64;                // op 1: k values per block
+
+struct StatOperand {
+  const void* X;
+  int64_t ld;
+  int op;
+  int64_t rows;
+  int* emax;
+  int* deep;
+  int64_t blocks;
+};
+
+__device__ __forceinline__ int row_emax(const int* emax, int64_t r) {
+  const int v = emax[r];
+  return v == kEmaxEmpty ? 0 : v;
+}
+
+// pass 0: emax; pass 1: deep counts (needs emax complete)
+template <int kBf16, int kPass>
+__device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
+  const int tid = threadIdx.x;
+  if (o.op == 0) {
+    const int64_t nkc = (K + kRowChunk - 1) / kRowChunk;
+    const int64_t r = b / nkc;
+    const int64_t k0 = (b - r * nkc) * kRowChunk;
+    const int ref = kPass ? row_emax(o.emax, r) - kDeepGap : 0;
+    int acc = kPass ? 0 : kEmaxEmpty;
+    for (int u = 0; u < kRowChunk / kThreads; ++u) {
+      const int64_t k = k0 + u * kThreads + tid;
+      if (k < K) {
+        const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, r * o.ld + k));
+        const bool live = d.m != 0;
+        if (kPass) acc += (live && d.e < ref) ? 1 : 0;
+        else acc = live ? max(acc, d.e) : acc;
+      }
+    }
+    __shared__ int red[kThreads / 32];
+    acc = kPass ? __reduce_add_sync(0xFFFFFFFFu, acc) : __reduce_max_sync(0xFFFFFFFFu, acc);
+    if ((tid & 31) == 0) red[tid >> 5] = acc;
+    __syncthreads();
+    if (tid == 0) {
+      int v = red[0];
+      for (int w = 1; w < kThreads / 32; ++w) v = kPass ? v + red[w] : max(v, red[w]);
+      if (kPass) {
+        if (v) atomicAdd(o.deep + r, v);
+      } else if (v != kEmaxEmpty) {
+        atomicMax(o.emax + r, v);
+      }
+    }
+  } else {
+    const int64_t nrc = (o.rows + kThreads - 1) / kThreads;
+    const int64_t kc = b / nrc;
+    const int64_t r = (b - kc * nrc) * kThreads + tid;
+    if (r >= o.rows) return;
+    const int ref = kPass ? row_emax(o.emax, r) - kDeepGap : 0;
+    int acc = kPass ? 0 : kEmaxEmpty;
+    const int64_t k0 = kc * kColChunk;
+    for (int u = 0; u < kColChunk; ++u) {
+      const int64_t k = k0 + u;
+      if (k < K) {
+        const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, k * o.ld + r));
+        const bool live = d.m != 0;
+        if (kPass) acc += (live && d.e < ref) ? 1 : 0;
+        else acc = live ? max(acc, d.e) : acc;
+      }
+    }
+    if (kPass) {
+      if (acc) atomicAdd(o.deep + r, acc);
+    } else if (acc != kEmaxEmpty) {
+      atomicMax(o.emax + r, acc);
+    }
+  }
+}
+
+template <int kBf16, int kPass>
+__global__ void __launch_bounds__(kThreads) rowstat_kernel(StatOperand a, StatOperand b, int64_t K) {
+  const int64_t blk = blockIdx.x;
+  if (blk < a.blocks) stat_block<kBf16, kPass>(a, K, blk);
+  else stat_block<kBf16, kPass>(b, K, blk - a.blocks);
+}
+
+// One thread per 64x64 tile: 1 = general kernel, 0 = band kernel.
+__global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, const int* deepB,
+                                                             int64_t M, int64_t N, int64_t K,
+                                                             uint8_t* route) {
+  const int64_t tiles_n = (N + kTile - 1) / kTile;
+  const int64_t tiles = ((M + kTile - 1) / kTile) * tiles_n;
+  for (int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x; t < tiles;
+       t += int64_t(gridDim.x) * kThreads) {
+    const int64_t tm = t / tiles_n, tn = t - (t / tiles_n) * tiles_n;
+    int da = 0, db = 0;
+    for (int64_t m = tm * kTile; m < min(M, tm * kTile + kTile); ++m) da = max(da, deepA[m]);
+    for (int64_t n = tn * kTile; n < min(N, tn * kTile + kTile); ++n) db = max(db, deepB[n]);
+    route[t] = (static_cast<int64_t>(da) + db) * kDeepRouteDen > K ? 1 : 0;
+  }
+}
+
+StatOperand make_op(const void* X, int64_t ld, int op, int64_t rows, int64_t K, int* emax,
+                    int* deep) {
+  StatOperand o{X, ld, op, rows, emax, deep, 0};
+  if (K == 0 || rows == 0) return o;
+  if (op == 0) o.blocks = rows * ((K + kRowChunk - 1) / kRowChunk);
+  else o.blocks = ((rows + kThreads - 1) / kThreads) * ((K + kColChunk - 1) / kColChunk);
+  return o;
+}
+
+template <int kBf16>
+cudaError_t prepass_t(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
+  StatOperand a = make_op(g.A, g.lda, g.opA, g.M, g.K, s.emaxA, s.deepA);
+  StatOperand b = make_op(g.B, g.ldb, g.opB, g.N, g.K, s.emaxB, s.deepB);
+  const int64_t blocks = a.blocks + b.blocks;
+  if (blocks > 0) {
+    rowstat_kernel<kBf16, 0><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, b, g.K);
+    rowstat_kernel<kBf16, 1><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, b, g.K);
+    note_launch(2);
+  }
+  const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
+  const int64_t grid = (tiles + kThreads - 1) / kThreads;
+  classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
+      s.deepA, s.deepB, g.M, g.N, g.K, s.route);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
+  // emax starts at kEmaxEmpty (every byte 0x80), deep counts at 0
+  cudaError_t e = cudaMemsetAsync(s.emaxA, 0x80, sizeof(int) * (g.M + g.N), stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(s.deepA, 0, sizeof(int) * (g.M + g.N), stream);
+  if (e != cudaSuccess) return e;
+  return g.bf16 ? prepass_t<1>(g, s, stream) : prepass_t<0>(g, s, stream);
+}
+
+}  // namespace det
