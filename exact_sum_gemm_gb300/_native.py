@@ -22,6 +22,7 @@ DET_MAX_COMBINE = 1 << 20
 STATUS_NAMES = {
     0: "DET_OK", 1: "DET_ERR_INVALID_ARG", 2: "DET_ERR_DTYPE", 3: "DET_ERR_SHAPE",
     4: "DET_ERR_K_LIMIT", 5: "DET_ERR_OVERFLOW", 6: "DET_ERR_ALIGNMENT", 7: "DET_ERR_CUDA",
+    8: "DET_ERR_NOALLOC_LIMIT",
 }
 
 # symbol -> (restype, argtypes); mirrors include/det_gemm.h
@@ -32,6 +33,8 @@ SIGNATURES = {
     "det_kernel_launches": (ctypes.c_uint64, []),
     "det_gemm": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _vp]),
     "det_gemm_partial": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _vp]),
+    "det_gemm_partial_noalloc": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32,
+                                        _vp, _vp]),
     "det_combine": (_i32, [_i64, _i64, ctypes.POINTER(_vp), _i32, _vp, _vp]),
     "det_finalize": (_i32, [_i64, _i64, _vp, _vp, _i64, _vp]),
     "det_linear_forward": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
@@ -74,7 +77,7 @@ def lib(build: bool = True):
 
 def check(fn_name: str, status: int) -> None:
     if status != DET_OK:
-        if status in (1, 2, 3, 4, 5, 6):
+        if status in (1, 2, 3, 4, 5, 6, 8):
             err = DetError(fn_name, status)
             raise ValueError(str(err)) from err
         raise DetError(fn_name, status)

@@ -9,6 +9,7 @@
 #include <atomic>
 
 #include "det_gemm.h"
+#include "det_gemm_internal.cuh"
 #include "det_kernels.h"
 
 namespace det {
@@ -83,6 +84,9 @@ const char* det_status_string(det_status s) {
     case DET_ERR_OVERFLOW: return "DET_ERR_OVERFLOW: too many partials for int64 digit headroom";
     case DET_ERR_ALIGNMENT: return "DET_ERR_ALIGNMENT: pointer not aligned to its element size";
     case DET_ERR_CUDA: return "DET_ERR_CUDA: a CUDA call or kernel launch failed";
+    case DET_ERR_NOALLOC_LIMIT:
+      return "DET_ERR_NOALLOC_LIMIT: problem needs more scratch than det_gemm_partial_noalloc's "
+             "fixed array (DET_NOALLOC_SCRATCH_BYTES)";
   }
   return "DET_ERR_UNKNOWN";
 }
@@ -112,6 +116,20 @@ det_status det_gemm_partial(det_dtype dtype, int64_t M, int64_t N, int64_t K, co
   det::GemmArgs a = make_args(dtype, M, N, K, A, lda, opA, B, ldb, opB);
   a.P = P;
   return from_cuda(det::launch_gemm(a, static_cast<cudaStream_t>(stream)));
+}
+
+det_status det_gemm_partial_noalloc(det_dtype dtype, int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, int opA, const void* B,
+                                    int64_t ldb, int opB, int64_t* P, void* stream) {
+  det_status s = validate_gemm(dtype, M, N, K, A, lda, opA, B, ldb, opB);
+  if (s != DET_OK) return s;
+  if (M == 0 || N == 0) return DET_OK;
+  if (P == nullptr) return DET_ERR_INVALID_ARG;
+  if (!aligned(P, 8)) return DET_ERR_ALIGNMENT;
+  det::GemmArgs a = make_args(dtype, M, N, K, A, lda, opA, B, ldb, opB);
+  a.P = P;
+  if (!det::noalloc_fits(a)) return DET_ERR_NOALLOC_LIMIT;
+  return from_cuda(det::launch_gemm_partial_noalloc(a, static_cast<cudaStream_t>(stream)));
 }
 
 det_status det_combine(int64_t M, int64_t N, const int64_t* const* parts, int n, int64_t* out,

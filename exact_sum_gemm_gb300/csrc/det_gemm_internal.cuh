@@ -32,6 +32,15 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 cudaError_t launch_kulisch(const GemmArgs& g, const uint8_t* route, cudaStream_t stream);
 
+// Pre-pass + band + general kernels with caller-provided scratch of at least
+// scratch_bytes(g, slots) bytes (256-byte aligned).
+cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slots,
+                                  cudaStream_t stream);
+
+// det_gemm_partial_noalloc: scratch from a fixed static device array.
+bool noalloc_fits(const GemmArgs& g);
+cudaError_t launch_gemm_partial_noalloc(const GemmArgs& g, cudaStream_t stream);
+
 // Band-kernel CTAs resident on the current device (persistent grid size).
 int64_t band_slots(const GemmArgs& g);
 

@@ -57,7 +57,8 @@ typedef enum {
   DET_ERR_K_LIMIT = 4,     /* K > DET_K_MAX */
   DET_ERR_OVERFLOW = 5,    /* digit headroom would be exceeded (combine of too many parts) */
   DET_ERR_ALIGNMENT = 6,   /* a pointer is not aligned to its element size */
-  DET_ERR_CUDA = 7         /* a CUDA call or kernel launch failed */
+  DET_ERR_CUDA = 7,        /* a CUDA call or kernel launch failed */
+  DET_ERR_NOALLOC_LIMIT = 8 /* problem too large for det_gemm_partial_noalloc's fixed scratch */
 } det_status;
 
 typedef enum { DET_F32 = 0, DET_BF16 = 1 } det_dtype;
@@ -123,6 +124,35 @@ det_status det_combine(int64_t M, int64_t N, const int64_t* const* parts, int n,
  */
 det_status det_finalize(int64_t M, int64_t N, const int64_t* P, float* C, int64_t ldc,
                         void* stream);
+
+/*
+ * det_gemm_partial_noalloc -- det_gemm_partial that allocates no memory.
+ * The det-train page has no counterpart: this entry point exists for callers
+ * that cannot call cudaMalloc -- for example a plug-in inside a host framework
+ * that owns all device memory and forbids allocations behind its back, or
+ * latency-critical code that must not enter the CUDA allocator (which may
+ * synchronise the device).  Arguments, output and result are exactly those of
+ * det_gemm_partial; the caller still provides A, B and P.
+ *
+ * The working memory (per-row exponent maxima, deep-element counts and the
+ * tile routing table) lives in one fixed array of DET_NOALLOC_SCRATCH_BYTES
+ * bytes that is a static device variable of this library: every GPU that
+ * loads the library holds it until the process exits.  A call needs
+ * 8 * (M + N) bytes plus one byte per 64x64 output tile (each part rounded up
+ * to 256 bytes); larger problems (M = N = 32768 fits, M = N = 49152 does not)
+ * return DET_ERR_NOALLOC_LIMIT before anything is enqueued.
+ *
+ * The first call on each device looks up the array's device address (with
+ * that device current); make that first call before any stream capture.
+ * Every call uses the same array and clears what must start at zero; two calls
+ * whose work overlaps on the GPU (e.g. on different streams without ordering)
+ * race on it and give undefined results.
+ */
+enum { DET_NOALLOC_SCRATCH_BYTES = 1 << 20 };
+det_status det_gemm_partial_noalloc(det_dtype dtype, int64_t M, int64_t N, int64_t K,
+                                    const void* A, int64_t lda, int opA,
+                                    const void* B, int64_t ldb, int opB,
+                                    int64_t* P, void* stream);
 
 /*
  * DetLinear (det-train page, usage section: "DetLinear(4096, 4096)",
