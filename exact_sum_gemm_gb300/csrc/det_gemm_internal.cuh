@@ -10,7 +10,6 @@ namespace det {
 
 constexpr int kTile = 64;                 // band kernel output tile (and routing unit)
 constexpr int kDeepGap = 15;              // "deep" element: more than 15 binades below its row max
-constexpr int kDeepRouteDen = 64;         // route a tile to the general kernel if deep > K/64
 constexpr int kEmaxEmpty = static_cast<int>(0x80808080u);   // memset(0x80) pattern: no live element
 
 // Device scratch of one det_gemm / det_gemm_partial call.
@@ -28,6 +27,9 @@ struct Scratch {
 size_t scratch_bytes(const GemmArgs& g, int64_t slots);
 Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots);
 
+// Capacity of a row's deep-element list; a 64x64 tile whose worst row plus
+// worst column hold more deep elements goes to the general kernel.
+int deep_list_cap(int64_t K);
 cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 cudaError_t launch_kulisch(const GemmArgs& g, const uint8_t* route, cudaStream_t stream);

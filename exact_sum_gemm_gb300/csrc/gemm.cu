@@ -1,10 +1,13 @@
 // Orchestration of one exact GEMM call:
 //   1. exponent pre-pass (row maxima and deep-element counts) + tile routing;
-//   2. band kernel on the tiles routed to it (narrow exponent spread);
+//   2. residue path on the tiles with few deep elements: bf16 residue planes,
+//      residue GEMM on tcgen05 tensor cores, CRT reconstruction + deep
+//      products, round once (or digits out);
 //   3. general Kulisch kernel on the remaining tiles (any exponent spread).
-// Both kernels produce the same exact digits, so routing never changes a bit
-// of the result (det-train page, "Method": the result does not depend on how
-// the computation is split).
+// With K = 0 (or a grid beyond the tensor-core kernel's limits) the band
+// kernel takes the place of step 2.  Every path produces the same exact
+// digits, so routing never changes a bit of the result (det-train page,
+// "Method": the result does not depend on how the computation is split).
 //
 // Scratch: one stream-ordered allocation per call from a memory pool owned by
 // this library (one pool per device, which keeps its memory reserved so that
@@ -18,6 +21,7 @@
 #include "det_arith.cuh"
 #include "det_gemm_internal.cuh"
 #include "det_kernels.h"
+#include "det_residue.cuh"
 
 namespace det {
 namespace {
@@ -89,16 +93,97 @@ cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slot
   return launch_kulisch(g, s.route, stream);
 }
 
-cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
-  if (g.M == 0 || g.N == 0) return cudaSuccess;
-  const int64_t slots = band_slots(g);
+namespace {
+
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream) {
   cudaMemPool_t pool;
   cudaError_t e = device_pool(&pool);
   if (e != cudaSuccess) return e;
+  return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
+  const int64_t slots = band_slots(g);
   void* scratch = nullptr;
-  e = cudaMallocFromPoolAsync(&scratch, scratch_bytes(g, slots), pool, stream);
+  cudaError_t e = pool_alloc(&scratch, scratch_bytes(g, slots), stream);
   if (e != cudaSuccess) return e;
   e = run_gemm_with_scratch(g, scratch, slots, stream);
+  cudaError_t f = cudaFreeAsync(scratch, stream);
+  return e != cudaSuccess ? e : f;
+}
+
+struct ResidueScratch {
+  size_t bytes;
+  size_t off_counts, off_listA, off_listB, off_planesA, off_planesB, off_res;
+};
+
+ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int cap) {
+  ResidueScratch r{};
+  size_t b = align_up(scratch_bytes(g, 0), 1024);
+  r.off_counts = b;                                                   // countA, countB, error
+  b = align_up(b + sizeof(int) * size_t(g.M + g.N + 1), 1024);
+  r.off_listA = b;
+  b = align_up(b + sizeof(uint2) * size_t(g.M) * cap, 1024);
+  r.off_listB = b;
+  b = align_up(b + sizeof(uint2) * size_t(g.N) * cap, 1024);
+  r.off_planesA = b;
+  b = align_up(b + size_t(2) * nplanes * size_t(g.M) * size_t(Kp), 1024);
+  r.off_planesB = b;
+  b = align_up(b + size_t(2) * nplanes * size_t(g.N) * size_t(Kp), 1024);
+  r.off_res = b;
+  b = align_up(b + size_t(nplanes) * size_t(g.M) * size_t(g.N), 1024);
+  r.bytes = b;
+  return r;
+}
+
+cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch& L, int nplanes,
+                             int64_t Kp, int cap, cudaStream_t stream) {
+  const Scratch s = carve_scratch(base, g, 0);
+  int* counts = reinterpret_cast<int*>(base + L.off_counts);
+  int* error = counts + g.M + g.N;
+  uint2* listA = reinterpret_cast<uint2*>(base + L.off_listA);
+  uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
+  __nv_bfloat16* planesA = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesA);
+  __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
+  uint8_t* res = reinterpret_cast<uint8_t*>(base + L.off_res);
+
+  cudaError_t e = launch_prepass(g, s, stream);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 1), stream);
+  if (e != cudaSuccess) return e;
+  ResidueOperand ra{g.A, g.lda, g.opA, g.M, g.K, Kp, s.emaxA, planesA, counts, listA, cap};
+  ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
+  e = launch_residues(ra, g.bf16, nplanes, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_residues(rb, g.bf16, nplanes, stream);
+  if (e != cudaSuccess) return e;
+  ResGemmArgs rg{planesA, planesB, g.M, g.N, Kp, nplanes, res, error};
+  e = launch_residue_gemm(rg, stream);
+  if (e != cudaSuccess) return e;
+  ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
+               error};
+  e = launch_reconstruct(g, rc, stream);
+  if (e != cudaSuccess) return e;
+  return launch_kulisch(g, s.route, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
+  if (g.M == 0 || g.N == 0) return cudaSuccess;
+  const int nplanes = residue_planes_needed(g);
+  // grid limits: the residue kernel puts 32-row blocks, the tensor-core
+  // kernel 128-row tiles, in gridDim.y (at most 65535)
+  const bool residue_ok = g.K > 0 && nplanes > 0 && (g.M + 31) / 32 <= 65535 &&
+                          (g.N + 31) / 32 <= 65535;
+  if (!residue_ok) return launch_band_path(g, stream);
+  const int64_t Kp = (g.K + kStageK - 1) / kStageK * kStageK;
+  const int cap = deep_list_cap(g.K);
+  const ResidueScratch L = residue_layout(g, nplanes, Kp, cap);
+  void* scratch = nullptr;
+  cudaError_t e = pool_alloc(&scratch, L.bytes, stream);
+  if (e != cudaSuccess) return e;
+  e = run_residue_path(g, static_cast<char*>(scratch), L, nplanes, Kp, cap, stream);
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }

@@ -3,14 +3,15 @@
 // For every row r of an operand (a row of A, or a row of B = a column of C):
 //   emax[r] = the largest exponent e (weight of the last significand bit, see
 //             det_arith.cuh) over the row's nonzero finite elements;
-//   deep[r] = how many nonzero finite elements lie more than kDeepGap
-//             binades below emax[r].
-// The band kernel anchors each output's register window at emax_A + emax_B,
-// so a product leaves the window only if its operands are together more than
-// 31 binades below their rows' maxima, which needs a deep element on one
-// side.  A 64x64 output tile whose worst row plus worst column hold more
-// than K/64 deep elements is routed to the general kernel instead.  Routing
-// changes speed only: both kernels return the same exact digits.
+//   deep[r] = how many elements are non-finite or lie more than kDeepGap
+//             binades below emax[r] ("deep" elements).
+// The residue path turns the other ("shallow") elements into integers on a
+// common per-row grid and handles deep elements one by one from short
+// per-row lists of capacity `cap`; the band kernel anchors each output's
+// register window at emax_A + emax_B.  A 64x64 output tile whose worst row
+// plus worst column hold more than `cap` deep elements is routed to the
+// general kernel instead.  Routing changes speed only: every kernel returns
+// the same exact digits.
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -55,7 +56,7 @@ __device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
       if (k < K) {
         const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, r * o.ld + k));
         const bool live = d.m != 0;
-        if (kPass) acc += (live && d.e < ref) ? 1 : 0;
+        if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
         else acc = live ? max(acc, d.e) : acc;
       }
     }
@@ -85,7 +86,7 @@ __device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
       if (k < K) {
         const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, k * o.ld + r));
         const bool live = d.m != 0;
-        if (kPass) acc += (live && d.e < ref) ? 1 : 0;
+        if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
         else acc = live ? max(acc, d.e) : acc;
       }
     }
@@ -104,9 +105,9 @@ __global__ void __launch_bounds__(kThreads) rowstat_kernel(StatOperand a, StatOp
   else stat_block<kBf16, kPass>(b, K, blk - a.blocks);
 }
 
-// One thread per 64x64 tile: 1 = general kernel, 0 = band kernel.
+// One thread per 64x64 tile: 1 = general kernel, 0 = residue path / band kernel.
 __global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, const int* deepB,
-                                                             int64_t M, int64_t N, int64_t K,
+                                                             int64_t M, int64_t N, int cap,
                                                              uint8_t* route) {
   const int64_t tiles_n = (N + kTile - 1) / kTile;
   const int64_t tiles = ((M + kTile - 1) / kTile) * tiles_n;
@@ -116,7 +117,7 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, co
     int da = 0, db = 0;
     for (int64_t m = tm * kTile; m < min(M, tm * kTile + kTile); ++m) da = max(da, deepA[m]);
     for (int64_t n = tn * kTile; n < min(N, tn * kTile + kTile); ++n) db = max(db, deepB[n]);
-    route[t] = (static_cast<int64_t>(da) + db) * kDeepRouteDen > K ? 1 : 0;
+    route[t] = static_cast<int64_t>(da) + db > cap ? 1 : 0;
   }
 }
 
@@ -130,7 +131,7 @@ StatOperand make_op(const void* X, int64_t ld, int op, int64_t rows, int64_t K, 
 }
 
 template <int kBf16>
-cudaError_t prepass_t(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
+cudaError_t prepass_t(const GemmArgs& g, const Scratch& s, int cap, cudaStream_t stream) {
   StatOperand a = make_op(g.A, g.lda, g.opA, g.M, g.K, s.emaxA, s.deepA);
   StatOperand b = make_op(g.B, g.ldb, g.opB, g.N, g.K, s.emaxB, s.deepB);
   const int64_t blocks = a.blocks + b.blocks;
@@ -142,12 +143,17 @@ cudaError_t prepass_t(const GemmArgs& g, const Scratch& s, cudaStream_t stream) 
   const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
   const int64_t grid = (tiles + kThreads - 1) / kThreads;
   classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
-      s.deepA, s.deepB, g.M, g.N, g.K, s.route);
+      s.deepA, s.deepB, g.M, g.N, cap, s.route);
   note_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
+
+int deep_list_cap(int64_t K) {
+  const int64_t c = K / 256;
+  return static_cast<int>(c > 8 ? c : 8);
+}
 
 cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
   // emax starts at kEmaxEmpty (every byte 0x80), deep counts at 0
@@ -155,7 +161,8 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(s.deepA, 0, sizeof(int) * (g.M + g.N), stream);
   if (e != cudaSuccess) return e;
-  return g.bf16 ? prepass_t<1>(g, s, stream) : prepass_t<0>(g, s, stream);
+  const int cap = deep_list_cap(g.K);
+  return g.bf16 ? prepass_t<1>(g, s, cap, stream) : prepass_t<0>(g, s, cap, stream);
 }
 
 }  // namespace det

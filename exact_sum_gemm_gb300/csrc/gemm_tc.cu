@@ -1,0 +1,320 @@
+// Residue GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// For every modulus p_u (u < nplanes) it computes, exactly,
+//     res[u][m][n] = (sum_k A_u[m,k] * B_u[n,k]) mod p_u,
+// where A_u, B_u are bf16 planes of balanced residues (|r| <= 127, see
+// residue.cu).  Each product is an integer of magnitude <= 16129, exact in the
+// MMA; fp32 accumulation of integers is exact while the running sum stays
+// below 2^24, so the accumulator is reduced modulo p_u in TMEM after every
+// 1024 values of K (1024 * 16129 + a reduced carry < 2^24), and the MMA keeps
+// accumulating on top of the reduced value.  The result is the exact integer
+// dot product modulo p_u; the CRT in residue.cu rebuilds the exact sum.
+//
+// Structure (one CTA per 128x256 output tile, 1 CTA per SM):
+//   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
+//               rows), 128-byte swizzled, 4-stage mbarrier ring
+//   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
+//               and the single MMA-issuing thread (UMMA 128x256x16, bf16)
+//   warps 2-5   epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
+//               lanes = 32 rows), reduce modulo p_u with exact fp32
+//               arithmetic, tcgen05.st it back (or, after the last chunk,
+//               store the residues to global memory)
+// Two moduli are interleaved chunk by chunk on the two accumulators, so the
+// MMA of one modulus overlaps the in-TMEM reduction of the other.
+// Every mbarrier wait is bounded (about 2 s): on expiry the kernel records an
+// error flag (the reconstruction then emits NaN), drains its copies in flight,
+// frees TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "det_kernels.h"
+#include "det_residue.cuh"
+#include "tc_ptx.cuh"
+
+namespace det {
+namespace {
+
+constexpr int kBlockM = 128;
+constexpr int kBlockN = 256;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;
+constexpr int kABytes = kBlockM * kStageK * 2;               // 16 KB
+constexpr int kBBytes = kBlockN * kStageK * 2;               // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;               // 48 KB
+constexpr int kKbPerChunk = kChunkK / kStageK;               // 16
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
+constexpr uint32_t kTmemCols = 512;
+constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (ptx::mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 1;; ++i) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// Job J -> (modulus u, K chunk c).  Moduli are taken in pairs (2q, 2q+1);
+// within a pair the chunks alternate between the two moduli.
+__device__ __forceinline__ void job_at(int J, int P, int nch, int& u, int& c) {
+  const int pair_jobs = 2 * nch;
+  const int full = (P / 2) * pair_jobs;
+  if (J < full) {
+    const int q = J / pair_jobs, rem = J - q * pair_jobs;
+    c = rem >> 1;
+    u = 2 * q + (rem & 1);
+  } else {
+    c = J - full;
+    u = P - 1;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, ResGemmArgs a) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* smem = reinterpret_cast<unsigned char*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* acc_ready = empty + kStages;
+  uint64_t* acc_free = acc_ready + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_free + 2);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t m0 = int64_t(blockIdx.y) * kBlockM;
+  const int64_t n0 = int64_t(blockIdx.x) * kBlockN;
+  const int P = a.nplanes;
+  const int nkb = static_cast<int>(a.Kp / kStageK);
+  const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
+  const int njobs = P * nch;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      ptx::mbar_init(&full[s], 1);
+      ptx::mbar_init(&empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      ptx::mbar_init(&acc_ready[i], 1);
+      ptx::mbar_init(&acc_free[i], 4);      // one arrival per epilogue warp
+    }
+    ptx::fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    ptx::tma_prefetch_desc(&tmA);
+    ptx::tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(tmem_holder, kTmemCols);
+    ptx::tmem_relinquish();
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t it = 0;
+      for (int J = 0; J < njobs && ok; ++J) {
+        int u, c;
+        job_at(J, P, nch, u, c);
+        const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
+        for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!wait_bounded(&empty[s], ph ^ 1u)) {
+            ok = false;
+            break;
+          }
+          ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
+          unsigned char* st = smem + s * kStageBytes;
+          ptx::tma_load_3d(st, &tmA, &full[s], kb * kStageK, static_cast<int>(m0), u);
+          ptx::tma_load_3d(st + kABytes, &tmB, &full[s], kb * kStageK, static_cast<int>(n0), u);
+          ++it;
+        }
+      }
+      // drain before the CTA may exit: the copies still in flight, then (on the
+      // normal path) the MMA's release of the last stages, whose commits
+      // arrive on barriers in this CTA's shared memory
+      const uint32_t first = it > uint32_t(kStages) ? it - kStages : 0u;
+      for (uint32_t j = first; j < it; ++j) wait_bounded(&full[j % kStages], (j / kStages) & 1u);
+      if (ok) {
+        for (uint32_t j = first; j < it; ++j) {
+          if (!wait_bounded(&empty[j % kStages], (j / kStages) & 1u)) ok = false;
+        }
+      }
+      if (!ok) atomicExch(a.error, 1);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      uint32_t it = 0;
+      uint32_t uses[2] = {0u, 0u};
+      for (int J = 0; J < njobs && ok; ++J) {
+        int u, c;
+        job_at(J, P, nch, u, c);
+        const int acc = u & 1;
+        if (!wait_bounded(&acc_free[acc], (uses[acc] & 1u) ^ 1u)) {
+          ok = false;
+          break;
+        }
+        ++uses[acc];
+        ptx::tc_fence_after();
+        const uint32_t tmem_d = tmem_base + static_cast<uint32_t>(acc * kBlockN);
+        const int kb_begin = c * kKbPerChunk;
+        const int kb_end = min(nkb, kb_begin + kKbPerChunk);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
+          const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
+          if (!wait_bounded(&full[s], ph)) {
+            ok = false;
+            break;
+          }
+          ptx::tc_fence_after();
+          const uint32_t a_addr = ptx::smem_addr(smem + s * kStageBytes);
+          const uint32_t b_addr = a_addr + kABytes;
+#pragma unroll
+          for (int kk = 0; kk < kStageK / 16; ++kk) {
+            const uint64_t ad = ptx::smem_desc_sw128(a_addr + kk * 32);
+            const uint64_t bd = ptx::smem_desc_sw128(b_addr + kk * 32);
+            const uint32_t accumulate = (c > 0 || kb > kb_begin || kk > 0) ? 1u : 0u;
+            ptx::mma_bf16(tmem_d, ad, bd, kIdesc, accumulate);
+          }
+          ptx::mma_commit(&empty[s]);      // stage s is free once these MMAs finish
+          ++it;
+        }
+        if (!ok) break;
+        ptx::mma_commit(&acc_ready[acc]);  // chunk c of modulus u is in TMEM
+      }
+      if (!ok) atomicExch(a.error, 1);
+    }
+  } else {
+    const int g = warp & 3;                // TMEM lanes 32g .. 32g+31
+    const int64_t row = m0 + 32 * g + lane;
+    const int64_t MN = a.M * a.N;
+    bool ok = true;
+    uint32_t uses[2] = {0u, 0u};
+    for (int J = 0; J < njobs; ++J) {
+      int u, c;
+      job_at(J, P, nch, u, c);
+      const int acc = u & 1;
+      if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
+        ok = false;
+        break;
+      }
+      ++uses[acc];
+      ptx::tc_fence_after();
+      const bool last = c == nch - 1;
+      const int pm = modulus(u);
+      const float p = static_cast<float>(pm);
+      const float inv_p = 1.0f / p;
+#pragma unroll 1
+      for (int cb = 0; cb < kBlockN / 32; ++cb) {
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(32 * g) << 16) +
+                               static_cast<uint32_t>(acc * kBlockN + cb * 32);
+        uint32_t v[32];
+        ptx::tmem_ld32(taddr, v);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          // v is an exact integer below 2^24 in magnitude; reduce it exactly
+          const float f = __uint_as_float(v[j]);
+          const float q = rintf(f * inv_p);
+          v[j] = __float_as_uint(fmaf(-q, p, f));
+        }
+        if (!last) {
+          ptx::tmem_st32(taddr, v);
+        } else if (row < a.M) {
+          uint8_t* out = a.res + u * MN + row * a.N;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int64_t n = n0 + cb * 32 + j;
+            int r = static_cast<int>(__uint_as_float(v[j])) % pm;
+            if (r < 0) r += pm;
+            if (n < a.N) out[n] = static_cast<uint8_t>(r);
+          }
+        }
+      }
+      if (!last) ptx::tmem_wait_st();
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(&acc_free[acc]);
+    }
+    if (!ok && lane == 0) atomicExch(a.error, 1);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::mutex mu;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+// 3-D map over planes [P][rows][Kp] of bf16, boxes of 64 (K) x box_rows x 1.
+bool make_plane_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp, int planes,
+                    int box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+  if (enc == nullptr) return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(planes)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(Kp) * 2,
+                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(Kp) * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(box_rows), 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
+  if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
+  static bool configured = false;
+  if (!configured) {
+    cudaError_t e = cudaFuncSetAttribute(residue_gemm_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    configured = true;
+  }
+  CUtensorMap tmA, tmB;
+  if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kBlockM) ||
+      !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kBlockN))
+    return cudaErrorInvalidValue;
+  dim3 grid(static_cast<unsigned>((a.N + kBlockN - 1) / kBlockN),
+            static_cast<unsigned>((a.M + kBlockM - 1) / kBlockM));
+  residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  note_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace det
