@@ -31,6 +31,10 @@ SIGNATURES = {
     "det_abi_version": (_i32, []),
     "det_status_string": (ctypes.c_char_p, [_i32]),
     "det_kernel_launches": (ctypes.c_uint64, []),
+    "det_stage_timing": (_i32, [_i32]),
+    "det_residue_moduli": (_i32, [_i32, _i64]),
+    "det_stage_report": (_i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                ctypes.POINTER(_i32), _i32]),
     "det_gemm": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _vp]),
     "det_gemm_partial": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _vp]),
     "det_gemm_partial_noalloc": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32,
@@ -73,6 +77,16 @@ def lib(build: bool = True):
                 fn.argtypes = args
             _lib = handle
     return _lib
+
+
+def stage_report():
+    """{stage name: (total ms, launches)} recorded since det_stage_timing(1)."""
+    n_max = 16
+    names = (ctypes.c_char_p * n_max)()
+    ms = (ctypes.c_double * n_max)()
+    counts = (ctypes.c_int * n_max)()
+    n = lib().det_stage_report(names, ms, counts, n_max)
+    return {names[i].decode(): (ms[i], counts[i]) for i in range(n)}
 
 
 def check(fn_name: str, status: int) -> None:

@@ -11,6 +11,7 @@
 #include "det_gemm.h"
 #include "det_gemm_internal.cuh"
 #include "det_kernels.h"
+#include "det_residue.cuh"
 
 namespace det {
 namespace {
@@ -71,6 +72,15 @@ det::GemmArgs make_args(det_dtype dtype, int64_t M, int64_t N, int64_t K, const 
 extern "C" {
 
 int det_abi_version(void) { return 1; }
+
+int det_residue_moduli(det_dtype dtype, int64_t K) {
+  if ((dtype != DET_F32 && dtype != DET_BF16) || K < 0 || K > DET_K_MAX) return -1;
+  if (K == 0) return 0;
+  det::GemmArgs a{};
+  a.K = K;
+  a.bf16 = dtype == DET_BF16 ? 1 : 0;
+  return det::residue_planes_needed(a);
+}
 
 uint64_t det_kernel_launches(void) { return det::g_launches.load(std::memory_order_relaxed); }
 

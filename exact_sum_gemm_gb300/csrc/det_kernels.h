@@ -9,6 +9,25 @@ namespace det {
 // Count one enqueued kernel (diagnostic; see det_kernel_launches).
 void note_launch(int n = 1);
 
+// Stages timed by det_stage_timing / det_stage_report.
+enum Stage { kStagePrepass = 0, kStageResiduePlanes, kStageResidueGemm, kStageReconstruct,
+             kStageGeneral, kStageBand, kNumStages };
+
+// Records a CUDA event pair around its scope on `stream` while stage timing is on.
+class StageScope {
+ public:
+  StageScope(int stage, cudaStream_t stream);
+  ~StageScope();
+  StageScope(const StageScope&) = delete;
+  StageScope& operator=(const StageScope&) = delete;
+
+ private:
+  int stage_;
+  cudaStream_t stream_;
+  cudaEvent_t start_{}, stop_{};
+  bool active_ = false;
+};
+
 struct GemmArgs {
   const void* A;
   int64_t lda;

@@ -86,10 +86,18 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots) {
 cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slots,
                                   cudaStream_t stream) {
   const Scratch s = carve_scratch(scratch, g, slots);
-  cudaError_t e = launch_prepass(g, s, stream);
+  cudaError_t e;
+  {
+    StageScope t(kStagePrepass, stream);
+    e = launch_prepass(g, s, stream);
+  }
   if (e != cudaSuccess) return e;
-  e = launch_band(g, s, stream);
+  {
+    StageScope t(kStageBand, stream);
+    e = launch_band(g, s, stream);
+  }
   if (e != cudaSuccess) return e;
+  StageScope t(kStageGeneral, stream);
   return launch_kulisch(g, s.route, stream);
 }
 
@@ -147,23 +155,36 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
   uint8_t* res = reinterpret_cast<uint8_t*>(base + L.off_res);
 
-  cudaError_t e = launch_prepass(g, s, stream);
+  cudaError_t e;
+  {
+    StageScope t(kStagePrepass, stream);
+    e = launch_prepass(g, s, stream);
+    if (e == cudaSuccess)
+      e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 1), stream);
+  }
   if (e != cudaSuccess) return e;
-  e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 1), stream);
+  {
+    StageScope t(kStageResiduePlanes, stream);
+    ResidueOperand ra{g.A, g.lda, g.opA, g.M, g.K, Kp, s.emaxA, planesA, counts, listA, cap};
+    ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
+    e = launch_residues(ra, g.bf16, nplanes, stream);
+    if (e == cudaSuccess) e = launch_residues(rb, g.bf16, nplanes, stream);
+  }
   if (e != cudaSuccess) return e;
-  ResidueOperand ra{g.A, g.lda, g.opA, g.M, g.K, Kp, s.emaxA, planesA, counts, listA, cap};
-  ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
-  e = launch_residues(ra, g.bf16, nplanes, stream);
+  {
+    StageScope t(kStageResidueGemm, stream);
+    ResGemmArgs rg{planesA, planesB, g.M, g.N, Kp, nplanes, res, error};
+    e = launch_residue_gemm(rg, stream);
+  }
   if (e != cudaSuccess) return e;
-  e = launch_residues(rb, g.bf16, nplanes, stream);
+  {
+    StageScope t(kStageReconstruct, stream);
+    ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
+                 error};
+    e = launch_reconstruct(g, rc, stream);
+  }
   if (e != cudaSuccess) return e;
-  ResGemmArgs rg{planesA, planesB, g.M, g.N, Kp, nplanes, res, error};
-  e = launch_residue_gemm(rg, stream);
-  if (e != cudaSuccess) return e;
-  ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
-               error};
-  e = launch_reconstruct(g, rc, stream);
-  if (e != cudaSuccess) return e;
+  StageScope t(kStageGeneral, stream);
   return launch_kulisch(g, s.route, stream);
 }
 

@@ -10,7 +10,7 @@
 // accumulating on top of the reduced value.  The result is the exact integer
 // dot product modulo p_u; the CRT in residue.cu rebuilds the exact sum.
 //
-// Structure (one CTA per 128x256 output tile, 1 CTA per SM):
+// Structure (one CTA per 128x256 output tile and pair of moduli, 1 CTA per SM):
 //   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
 //               rows), 128-byte swizzled, 4-stage mbarrier ring
 //   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
@@ -97,7 +97,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int64_t m0 = int64_t(blockIdx.y) * kBlockM;
   const int64_t n0 = int64_t(blockIdx.x) * kBlockN;
-  const int P = a.nplanes;
+  // this CTA's moduli: the pair (2z, 2z+1), or the last one alone
+  const int u_base = 2 * static_cast<int>(blockIdx.z);
+  const int P = min(2, a.nplanes - u_base);
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   const int njobs = P * nch;
@@ -133,6 +135,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int J = 0; J < njobs && ok; ++J) {
         int u, c;
         job_at(J, P, nch, u, c);
+        u += u_base;
         const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
         for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -167,6 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int J = 0; J < njobs && ok; ++J) {
         int u, c;
         job_at(J, P, nch, u, c);
+        u += u_base;
         const int acc = u & 1;
         if (!wait_bounded(&acc_free[acc], (uses[acc] & 1u) ^ 1u)) {
           ok = false;
@@ -210,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int J = 0; J < njobs; ++J) {
       int u, c;
       job_at(J, P, nch, u, c);
+      u += u_base;
       const int acc = u & 1;
       if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
         ok = false;
@@ -238,13 +243,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!last) {
           ptx::tmem_st32(taddr, v);
         } else if (row < a.M) {
-          uint8_t* out = a.res + u * MN + row * a.N;
+          uint8_t* out = a.res + u * MN + row * a.N + n0 + cb * 32;
+          uint32_t packed[8];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int64_t n = n0 + cb * 32 + j;
             int r = static_cast<int>(__uint_as_float(v[j])) % pm;
             if (r < 0) r += pm;
-            if (n < a.N) out[n] = static_cast<uint8_t>(r);
+            if (j % 4 == 0) packed[j / 4] = 0;
+            packed[j / 4] |= static_cast<uint32_t>(r) << (8 * (j % 4));
+          }
+          const int64_t n_left = a.N - (n0 + cb * 32);
+          if (n_left >= 32 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+            reinterpret_cast<uint4*>(out)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            reinterpret_cast<uint4*>(out)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < n_left) out[j] = static_cast<uint8_t>(packed[j / 4] >> (8 * (j % 4)));
           }
         }
       }
@@ -311,7 +326,8 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
       !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kBlockN))
     return cudaErrorInvalidValue;
   dim3 grid(static_cast<unsigned>((a.N + kBlockN - 1) / kBlockN),
-            static_cast<unsigned>((a.M + kBlockM - 1) / kBlockM));
+            static_cast<unsigned>((a.M + kBlockM - 1) / kBlockM),
+            static_cast<unsigned>((a.nplanes + 1) / 2));
   residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   note_launch();
   return cudaGetLastError();

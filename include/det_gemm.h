@@ -80,6 +80,23 @@ const char* det_status_string(det_status s);
  * devices, all threads).  A diagnostic for benchmarks and tests. */
 uint64_t det_kernel_launches(void);
 
+/* Per-stage device timing, a diagnostic for benchmarks.  det_stage_timing(1)
+ * brackets every stage of the following det_gemm / det_gemm_partial calls
+ * (exponent pre-pass, residue planes, residue GEMM on the tensor cores,
+ * reconstruction, general kernel, band kernel) with CUDA events recorded on
+ * the call's stream; det_stage_timing(0) stops.  Returns the previous
+ * setting.  After the caller has synchronised those streams,
+ * det_stage_report writes up to `max` entries (stage name -- a static string
+ * --, total milliseconds, number of timed launches), clears the record and
+ * returns the number of entries.  Any output pointer may be NULL. */
+int det_stage_timing(int enable);
+
+/* Number of moduli (bf16 tensor-core GEMMs) the residue path of det_gemm uses
+ * for this dtype and K: enough that their product exceeds twice the largest
+ * possible |sum of shallow products| (0 for K = 0; -1 for bad arguments). */
+int det_residue_moduli(det_dtype dtype, int64_t K);
+int det_stage_report(const char** names, double* total_ms, int* counts, int max);
+
 /*
  * det_gemm -- C = RNE_f32( sum_k A(m,k) * B(n,k) ), computed exactly.
  * det-train page, usage section ("det_gemm(x, w)") and section "Method".
