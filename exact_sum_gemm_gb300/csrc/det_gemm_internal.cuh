@@ -9,7 +9,7 @@
 namespace det {
 
 constexpr int kTile = 64;                 // band kernel output tile (and routing unit)
-constexpr int kDeepGap = 15;              // "deep" element: more than 15 binades below its row max
+constexpr int kDeepGap = 19;              // "deep" element: more than 19 binades below its row max
 constexpr int kEmaxEmpty = static_cast<int>(0x80808080u);   // memset(0x80) pattern: no live element
 
 // Device scratch of one det_gemm / det_gemm_partial call.
@@ -31,6 +31,11 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots);
 // worst column hold more deep elements goes to the general kernel.
 int deep_list_cap(int64_t K);
 cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
+// The residue path's pieces of the pre-pass: row maxima only, and routing from
+// deep counts produced elsewhere (the residue kernel's list counters).
+cudaError_t launch_emax(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
+cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
+                            cudaStream_t stream);
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 cudaError_t launch_kulisch(const GemmArgs& g, const uint8_t* route, cudaStream_t stream);
 

@@ -12,12 +12,13 @@ namespace det {
 // Odd, pairwise coprime moduli <= 255: balanced residues lie in [-127, 127]
 // (exact in bf16), products of two in [-16129, 16129], and 1024 such products
 // plus a reduced carry stay below 2^24, where fp32 accumulation is exact.
-// The product of all 13 exceeds 2^102, enough for |S| < 2^19 * 2^78 * 2.
-constexpr int kNumModuli = 13;
+// The product of all 14 exceeds 2^109, enough for |S| < 2^19 * 2^86 * 2
+// (f32 shallow integers are below 2^(24+19)).
+constexpr int kNumModuli = 14;
 __host__ __device__ constexpr int modulus(int i) {
   return i == 0 ? 255 : i == 1 ? 253 : i == 2 ? 251 : i == 3 ? 247 : i == 4 ? 241 : i == 5 ? 239
        : i == 6 ? 233 : i == 7 ? 229 : i == 8 ? 227 : i == 9 ? 223 : i == 10 ? 217 : i == 11 ? 211
-       : 199;
+       : i == 12 ? 199 : 197;
 }
 // (p_0 * ... * p_{i-1})^{-1} mod p_i, for Garner's CRT (compile-time use).
 __host__ __device__ constexpr int garner_inverse(int i) {
@@ -61,7 +62,9 @@ struct ReconArgs {
 
 int residue_planes_needed(const GemmArgs& g);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
-cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream);
+// deep_lists: scratch of M + N ints; deep_counters: 2 ints, zero at launch.
+cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
+                               int* deep_counters, cudaStream_t stream);
 
 struct ResGemmArgs {
   const __nv_bfloat16* A;     // [nplanes][M][Kp]

@@ -122,14 +122,16 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
 
 struct ResidueScratch {
   size_t bytes;
-  size_t off_counts, off_listA, off_listB, off_planesA, off_planesB, off_res;
+  size_t off_counts, off_deep_idx, off_listA, off_listB, off_planesA, off_planesB, off_res;
 };
 
 ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int cap) {
   ResidueScratch r{};
   size_t b = align_up(scratch_bytes(g, 0), 1024);
-  r.off_counts = b;                                                   // countA, countB, error
-  b = align_up(b + sizeof(int) * size_t(g.M + g.N + 1), 1024);
+  r.off_counts = b;                     // countA [M], countB [N], error, deep-row/col counters [2]
+  b = align_up(b + sizeof(int) * size_t(g.M + g.N + 3), 1024);
+  r.off_deep_idx = b;                    // deep rows [M], deep columns [N] (+ the 2 counters above)
+  b = align_up(b + sizeof(int) * size_t(g.M + g.N), 1024);
   r.off_listA = b;
   b = align_up(b + sizeof(uint2) * size_t(g.M) * cap, 1024);
   r.off_listB = b;
@@ -158,17 +160,20 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   cudaError_t e;
   {
     StageScope t(kStagePrepass, stream);
-    e = launch_prepass(g, s, stream);
+    e = launch_emax(g, s, stream);
     if (e == cudaSuccess)
-      e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 1), stream);
+      e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 3), stream);
   }
   if (e != cudaSuccess) return e;
   {
+    // residue planes; the deep-list counters double as the rows' deep counts,
+    // from which the tiles are routed
     StageScope t(kStageResiduePlanes, stream);
     ResidueOperand ra{g.A, g.lda, g.opA, g.M, g.K, Kp, s.emaxA, planesA, counts, listA, cap};
     ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
     e = launch_residues(ra, g.bf16, nplanes, stream);
     if (e == cudaSuccess) e = launch_residues(rb, g.bf16, nplanes, stream);
+    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s.route, stream);
   }
   if (e != cudaSuccess) return e;
   {
@@ -181,7 +186,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageReconstruct, stream);
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
                  error};
-    e = launch_reconstruct(g, rc, stream);
+    // deep-row/column lists, and their two counters right after the error flag
+    e = launch_reconstruct(g, rc, reinterpret_cast<int*>(base + L.off_deep_idx), error + 1, stream);
   }
   if (e != cudaSuccess) return e;
   StageScope t(kStageGeneral, stream);

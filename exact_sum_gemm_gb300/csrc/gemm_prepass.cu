@@ -51,14 +51,18 @@ __device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
     const int64_t k0 = (b - r * nkc) * kRowChunk;
     const int ref = kPass ? row_emax(o.emax, r) - kDeepGap : 0;
     int acc = kPass ? 0 : kEmaxEmpty;
-    for (int u = 0; u < kRowChunk / kThreads; ++u) {
+    uint32_t v[kRowChunk / kThreads];
+#pragma unroll
+    for (int u = 0; u < kRowChunk / kThreads; ++u) {      // all loads in flight at once
       const int64_t k = k0 + u * kThreads + tid;
-      if (k < K) {
-        const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, r * o.ld + k));
-        const bool live = d.m != 0;
-        if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
-        else acc = live ? max(acc, d.e) : acc;
-      }
+      v[u] = k < K ? load_bits<kBf16>(o.X, r * o.ld + k) : 0u;
+    }
+#pragma unroll
+    for (int u = 0; u < kRowChunk / kThreads; ++u) {
+      const Decoded d = decode_f32_bits(v[u]);
+      const bool live = d.m != 0;
+      if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
+      else acc = live ? max(acc, d.e) : acc;
     }
     __shared__ int red[kThreads / 32];
     acc = kPass ? __reduce_add_sync(0xFFFFFFFFu, acc) : __reduce_max_sync(0xFFFFFFFFu, acc);
@@ -81,14 +85,14 @@ __device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
     const int ref = kPass ? row_emax(o.emax, r) - kDeepGap : 0;
     int acc = kPass ? 0 : kEmaxEmpty;
     const int64_t k0 = kc * kColChunk;
+#pragma unroll 16
     for (int u = 0; u < kColChunk; ++u) {
       const int64_t k = k0 + u;
-      if (k < K) {
-        const Decoded d = decode_f32_bits(load_bits<kBf16>(o.X, k * o.ld + r));
-        const bool live = d.m != 0;
-        if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
-        else acc = live ? max(acc, d.e) : acc;
-      }
+      const uint32_t bits = k < K ? load_bits<kBf16>(o.X, k * o.ld + r) : 0u;
+      const Decoded d = decode_f32_bits(bits);
+      const bool live = d.m != 0;
+      if (kPass) acc += (d.nonfinite || (live && d.e < ref)) ? 1 : 0;
+      else acc = live ? max(acc, d.e) : acc;
     }
     if (kPass) {
       if (acc) atomicAdd(o.deep + r, acc);
@@ -131,20 +135,18 @@ StatOperand make_op(const void* X, int64_t ld, int op, int64_t rows, int64_t K, 
 }
 
 template <int kBf16>
-cudaError_t prepass_t(const GemmArgs& g, const Scratch& s, int cap, cudaStream_t stream) {
+cudaError_t rowstat_t(const GemmArgs& g, const Scratch& s, bool deep_pass, cudaStream_t stream) {
   StatOperand a = make_op(g.A, g.lda, g.opA, g.M, g.K, s.emaxA, s.deepA);
   StatOperand b = make_op(g.B, g.ldb, g.opB, g.N, g.K, s.emaxB, s.deepB);
   const int64_t blocks = a.blocks + b.blocks;
   if (blocks > 0) {
     rowstat_kernel<kBf16, 0><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, b, g.K);
-    rowstat_kernel<kBf16, 1><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, b, g.K);
-    note_launch(2);
+    note_launch();
+    if (deep_pass) {
+      rowstat_kernel<kBf16, 1><<<static_cast<unsigned>(blocks), kThreads, 0, stream>>>(a, b, g.K);
+      note_launch();
+    }
   }
-  const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
-  const int64_t grid = (tiles + kThreads - 1) / kThreads;
-  classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
-      s.deepA, s.deepB, g.M, g.N, cap, s.route);
-  note_launch();
   return cudaGetLastError();
 }
 
@@ -155,14 +157,32 @@ int deep_list_cap(int64_t K) {
   return static_cast<int>(c > 8 ? c : 8);
 }
 
+cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
+                            cudaStream_t stream) {
+  const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
+  const int64_t grid = (tiles + kThreads - 1) / kThreads;
+  classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
+      deepA, deepB, g.M, g.N, deep_list_cap(g.K), route);
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_emax(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
+  // emax starts at kEmaxEmpty (every byte 0x80)
+  cudaError_t e = cudaMemsetAsync(s.emaxA, 0x80, sizeof(int) * (g.M + g.N), stream);
+  if (e != cudaSuccess) return e;
+  return g.bf16 ? rowstat_t<1>(g, s, false, stream) : rowstat_t<0>(g, s, false, stream);
+}
+
 cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t stream) {
   // emax starts at kEmaxEmpty (every byte 0x80), deep counts at 0
   cudaError_t e = cudaMemsetAsync(s.emaxA, 0x80, sizeof(int) * (g.M + g.N), stream);
   if (e != cudaSuccess) return e;
   e = cudaMemsetAsync(s.deepA, 0, sizeof(int) * (g.M + g.N), stream);
   if (e != cudaSuccess) return e;
-  const int cap = deep_list_cap(g.K);
-  return g.bf16 ? prepass_t<1>(g, s, cap, stream) : prepass_t<0>(g, s, cap, stream);
+  e = g.bf16 ? rowstat_t<1>(g, s, true, stream) : rowstat_t<0>(g, s, true, stream);
+  if (e != cudaSuccess) return e;
+  return launch_classify(g, s.deepA, s.deepB, s.route, stream);
 }
 
 }  // namespace det

@@ -1,18 +1,19 @@
 // Residue (CRT) decomposition of the exact GEMM, the CUDA-core halves:
 //   residue_kernel      operands -> bf16 residue planes + per-row deep lists
 //   reconstruct_kernel  residues of the shallow dot product -> exact value
-//                       (Garner CRT) + deep products -> digits -> round once
+//                       (CRT) + deep products -> round once (or digits)
 //
-// Shallow elements.  For a row r of an operand with largest last-bit exponent
-// emax[r], an element m*2^e with e >= emax[r] - 15 is the integer
-//     X_int = m * 2^(e - emax[r] + 15),   |X_int| < 2^39 (f32), 2^23 (bf16,
-//     whose significand has 8 bits), times 2^(emax[r] - 15).  So for an output (m, n) the shallow products sum to
-//     2^(emaxA[m] + emaxB[n] - 30) * S,   S = sum_k A_int[m,k] * B_int[n,k],
-// an exact integer dot product with |S| < K * 2^78.  S is computed modulo
+// Shallow elements.  For a row r of an operand with largest last-bit
+// exponent emax[r], an element m*2^e with e >= emax[r] - 19 is the integer
+//     X_int = m * 2^(e - emax[r] + 19)
+// times 2^(emax[r] - 19), with |X_int| < 2^43 (f32) or 2^27 (bf16, whose
+// significand has 8 bits).  So for an output (m, n) the shallow products sum
+// to 2^(emaxA[m] + emaxB[n] - 38) * S with S = sum_k A_int[m,k] * B_int[n,k],
+// an exact integer dot product, |S| < K * 2^86.  S is computed modulo
 // kNumModuli small odd pairwise-coprime moduli (residues in bf16 planes,
 // multiplied on tensor cores with exact fp32 accumulation) and rebuilt here
 // by the Chinese remainder theorem: the moduli's product exceeds 2|S|.
-// Deep elements (more than 15 binades below the row max) and non-finite ones
+// Deep elements (more than 19 binades below the row max) and non-finite ones
 // are left out of the planes and listed per row; their products are added
 // exactly, one by one, during reconstruction.  Together this is exactly the
 // det-train page's "exact fp64-product sum rounded once to fp32" (section
@@ -39,46 +40,49 @@ constexpr int kThreads = 256;
 constexpr int kTileRows = 32;
 constexpr int kTileK = 64;
 
-// x mod p for an integer-valued float 0 <= x < 2^24 (every step exact: the
-// quotient estimate is off by at most one and the fma remainder is exact).
+// x mod p for 0 <= x < 2^24 and a compile-time p < 256: with
+// magic = ceil(2^32 / p), umulhi(x, magic) = floor(x/p) + floor(r/p + x*eps)
+// where x*eps < 2^24/2^32 = 2^-8 < 1/p, so the quotient is exact.
 template <int p>
-__device__ __forceinline__ float fmod_exact(float x) {
-  constexpr float fp = static_cast<float>(p);
-  constexpr float inv = 1.0f / static_cast<float>(p);
-  const float q = floorf(x * inv);
-  float r = fmaf(-q, fp, x);
-  r = r < 0.0f ? r + fp : r;
-  r = r >= fp ? r - fp : r;
-  return r;
+__device__ __forceinline__ uint32_t umod(uint32_t x) {
+  constexpr uint32_t magic = static_cast<uint32_t>((0x100000000ull + p - 1) / p);
+  return x - __umulhi(x, magic) * static_cast<uint32_t>(p);
 }
 
-// Balanced residue of the signed integer m * 2^s (|m| < 2^24, 0 <= s <= 15)
-// modulo the compile-time modulus p: a value in [-(p-1)/2, (p-1)/2].
+// bf16 bit pattern of a small integer |v| <= 127: the top half of its exact
+// binary32 pattern (the low 16 bits are zero, so no rounding happens).
+__device__ __forceinline__ uint32_t small_int_bf16_bits(int v) {
+  return __float_as_uint(static_cast<float>(v)) >> 16;
+}
+
+// Balanced residue, modulo the compile-time modulus p, of the integer
+// (+-am) * 2^s with am < 2^24 and pw = 2^s <= 2^19: every intermediate is
+// below 2^24, so each reduction is exact.  Result in [-(p-1)/2, (p-1)/2].
 template <int p>
-__device__ __forceinline__ float balanced_residue(int32_t m, float pow2s) {
-  const float am = static_cast<float>(m < 0 ? -m : m);              // exact
-  const float r = fmod_exact<p>(fmod_exact<p>(am) * fmod_exact<p>(pow2s));   // < 2^16 before mod
-  float v = m < 0 ? -r : r;
-  constexpr float h = static_cast<float>((p - 1) / 2);
-  v = v > h ? v - static_cast<float>(p) : v;
-  v = v < -h ? v + static_cast<float>(p) : v;
-  return v;
+__device__ __forceinline__ int balanced_residue(uint32_t am, uint32_t pw, bool neg) {
+  const uint32_t r = umod<p>(umod<p>(am) * umod<p>(pw));     // < 255 * 255 before the last mod
+  const int c = r > (p - 1) / 2 ? static_cast<int>(r) - p : static_cast<int>(r);
+  return neg ? -c : c;
 }
 
 template <int i>
-__device__ __forceinline__ void write_residues(__nv_bfloat16* planes, int64_t plane_stride,
-                                               int64_t off, int nplanes, int32_t m, float pow2s,
-                                               bool live) {
+__device__ __forceinline__ void write_residue_pairs(uint32_t* dst, int64_t plane_stride2, int nplanes,
+                                                    uint32_t am0, uint32_t pw0, bool ng0,
+                                                    uint32_t am1, uint32_t pw1, bool ng1) {
   if constexpr (i < kNumModuli) {
     if (i < nplanes) {
-      const float v = live ? balanced_residue<modulus(i)>(m, pow2s) : 0.0f;
-      planes[i * plane_stride + off] = __float2bfloat16_rn(v);        // |v| <= 127: exact
-      write_residues<i + 1>(planes, plane_stride, off, nplanes, m, pow2s, live);
+      constexpr int p = modulus(i);
+      *dst = small_int_bf16_bits(balanced_residue<p>(am0, pw0, ng0)) |
+             (small_int_bf16_bits(balanced_residue<p>(am1, pw1, ng1)) << 16);
+      write_residue_pairs<i + 1>(dst + plane_stride2, plane_stride2, nplanes, am0, pw0, ng0, am1,
+                                 pw1, ng1);
     }
   }
 }
 
-// One block: 32 rows x 64 k of one operand.  Planes are [P][rows][Kp].
+// One block: 32 rows x 64 k of one operand; each thread then handles pairs of
+// neighbouring k.  Planes are [P][rows][Kp] (Kp a multiple of 64).  Every
+// deep or non-finite element is counted (and listed while there is room).
 template <int kBf16>
 __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int nplanes) {
   __shared__ uint32_t tile[kTileRows][kTileK + 1];
@@ -96,28 +100,36 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
     tile[r][k] = bits;
   }
   __syncthreads();
-  const int64_t plane_stride = o.rows * o.Kp;
+  const int64_t plane_stride2 = o.rows * o.Kp / 2;          // in bf16 pairs
 #pragma unroll 1
-  for (int u = 0; u < kTileRows * kTileK / kThreads; ++u) {
+  for (int u = 0; u < kTileRows * kTileK / (2 * kThreads); ++u) {
     const int idx = tid + u * kThreads;
-    const int r = idx >> 6, k = idx & 63;
-    const int64_t gr = r0 + r, gk = k0 + k;
-    if (gr >= o.rows || gk >= o.Kp) continue;
-    const Decoded d = decode_f32_bits(tile[r][k]);
+    const int r = idx >> 5, kk = (idx & 31) * 2;
+    const int64_t gr = r0 + r, gk = k0 + kk;
+    if (gr >= o.rows) continue;
     int em = o.emax[gr];
     em = em == kEmaxEmpty ? 0 : em;
-    const int s = d.e - em + kDeepGap;
-    const bool deep = d.nonfinite || (d.m != 0 && s < 0);
-    const bool live = !deep && d.m != 0;
-    // a bf16 significand widened to binary32 carries 16 zero bits: drop them
-    // (exactly) so that |X_int| < 2^23; the reconstruction scales back by 2^32
-    const int32_t m_int = kBf16 ? (d.m >> 16) : d.m;
-    const float pow2s = __int_as_float((127 + (live ? s : 0)) << 23);   // 2^s, exact
-    write_residues<0>(o.planes, plane_stride, gr * o.Kp + gk, nplanes, m_int, pow2s, live);
-    if (deep && gk < o.K) {
-      const int slot = atomicAdd(o.list_count + gr, 1);
-      if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk), tile[r][k]);
+    uint32_t am[2], pw[2];
+    bool ng[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t bits = tile[r][kk + h];
+      const Decoded d = decode_f32_bits(bits);
+      const int s = d.e - em + kDeepGap;
+      const bool deep = d.nonfinite || (d.m != 0 && s < 0);
+      // a bf16 significand widened to binary32 carries 16 zero bits: drop them
+      // (exactly) so that |X_int| < 2^23; the reconstruction scales back by 2^32
+      const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
+      am[h] = deep ? 0u : static_cast<uint32_t>(mi < 0 ? -mi : mi);
+      pw[h] = 1u << (deep || d.m == 0 ? 0 : s);                            // 2^s
+      ng[h] = mi < 0;
+      if (deep && gk + h < o.K) {
+        const int slot = atomicAdd(o.list_count + gr, 1);
+        if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
+      }
     }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(o.planes + gr * o.Kp + gk);   // bf16 pair
+    write_residue_pairs<0>(dst, plane_stride2, nplanes, am[0], pw[0], ng[0], am[1], pw[1], ng[1]);
   }
 }
 
@@ -129,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
 //         S = S' mod M (balanced);
 //   T   = S * 2^64 plus every product involving a deep element, exact, as a
 //         192-bit two's-complement integer whose bit 0 weighs 2^E with
-//         E = emaxA + emaxB - 30 - 64 (+32 for bf16 planes);
+//         E = emaxA + emaxB - 38 - 64 (+32 for bf16 planes);
 //   out = RNE_f32(T * 2^E), or T placed into canonical digits.
 // A deep product whose lowest bit lies below 2^E (more than 64 bits under the
 // shallow grid) or that would leave the window is handled by the full
@@ -319,26 +331,30 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
   }
 }
 
-// S = the balanced CRT value of residues r (one per modulus in use).
-__device__ __forceinline__ __int128 crt_balanced(const uint32_t (&r)[kNumModuli], int P,
-                                                 const CrtTable& crt) {
+// S = the balanced CRT value of residues r (one per modulus in use), as a
+// signed 128-bit integer (hi:lo), |S| < 2^98.
+__device__ __forceinline__ void crt_s128(const uint32_t (&r)[kNumModuli], int P, const CrtTable& crt,
+                                         uint64_t& lo, uint64_t& hi) {
   uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
   float qf = 0.0f;
 #pragma unroll
   for (int i = 0; i < kNumModuli; ++i) {
     if (i < P) {
-      // (a3:a2:a1:a0) += r_i * C_i   (r_i < 256, C_i < M < 2^103; sum < 2^115)
-      uint64_t t = static_cast<uint64_t>(crt.c[i][0]) * r[i] + a0;
-      a0 = static_cast<uint32_t>(t);
-      t = static_cast<uint64_t>(crt.c[i][1]) * r[i] + a1 + (t >> 32);
-      a1 = static_cast<uint32_t>(t);
-      t = static_cast<uint64_t>(crt.c[i][2]) * r[i] + a2 + (t >> 32);
-      a2 = static_cast<uint32_t>(t);
-      a3 = crt.c[i][3] * r[i] + a3 + static_cast<uint32_t>(t >> 32);
+      // (a3:a2:a1:a0) += r_i * C_i: low halves of the four limb products, then
+      // their high halves one limb up (r_i < 256, C_i < M < 2^110; sum < 2^122)
+      asm("mad.lo.cc.u32 %0, %4, %8, %0;\n\t"
+          "madc.lo.cc.u32 %1, %5, %8, %1;\n\t"
+          "madc.lo.cc.u32 %2, %6, %8, %2;\n\t"
+          "madc.lo.u32 %3, %7, %8, %3;\n\t"
+          "mad.hi.cc.u32 %1, %4, %8, %1;\n\t"
+          "madc.hi.cc.u32 %2, %5, %8, %2;\n\t"
+          "madc.hi.u32 %3, %6, %8, %3;"
+          : "+r"(a0), "+r"(a1), "+r"(a2), "+r"(a3)
+          : "r"(crt.c[i][0]), "r"(crt.c[i][1]), "r"(crt.c[i][2]), "r"(crt.c[i][3]), "r"(r[i]));
       qf = fmaf(static_cast<float>(r[i]), crt.frac[i], qf);     // ~ acc / M
     }
   }
-  // quotient estimate within one of floor(acc / M); remainder by one multiply
+  // quotient estimate within one of floor(acc / M); rem = acc - q M
   const uint32_t q = static_cast<uint32_t>(qf);
   uint64_t t = static_cast<uint64_t>(crt.m[0]) * q;
   const uint32_t p0 = static_cast<uint32_t>(t);
@@ -347,42 +363,260 @@ __device__ __forceinline__ __int128 crt_balanced(const uint32_t (&r)[kNumModuli]
   t = static_cast<uint64_t>(crt.m[2]) * q + (t >> 32);
   const uint32_t p2 = static_cast<uint32_t>(t);
   const uint32_t p3 = crt.m[3] * q + static_cast<uint32_t>(t >> 32);
-  const u128 acc = (static_cast<u128>(a3) << 96) | (static_cast<u128>(a2) << 64) |
-                   (static_cast<u128>(a1) << 32) | a0;
-  const u128 qm = (static_cast<u128>(p3) << 96) | (static_cast<u128>(p2) << 64) |
-                  (static_cast<u128>(p1) << 32) | p0;
-  const u128 M = (static_cast<u128>(crt.m[3]) << 96) | (static_cast<u128>(crt.m[2]) << 64) |
-                 (static_cast<u128>(crt.m[1]) << 32) | crt.m[0];
-  __int128 rem = static_cast<__int128>(acc - qm);
-  if (rem < 0) rem += static_cast<__int128>(M);
-  else if (rem >= static_cast<__int128>(M)) rem -= static_cast<__int128>(M);
-  return rem > static_cast<__int128>(M >> 1) ? rem - static_cast<__int128>(M) : rem;
+  const uint64_t alo = (static_cast<uint64_t>(a1) << 32) | a0, ahi = (static_cast<uint64_t>(a3) << 32) | a2;
+  const uint64_t qlo = (static_cast<uint64_t>(p1) << 32) | p0, qhi = (static_cast<uint64_t>(p3) << 32) | p2;
+  const uint64_t mlo = (static_cast<uint64_t>(crt.m[1]) << 32) | crt.m[0];
+  const uint64_t mhi = (static_cast<uint64_t>(crt.m[3]) << 32) | crt.m[2];
+  uint64_t rlo = alo - qlo;
+  uint64_t rhi = ahi - qhi - (alo < qlo ? 1u : 0u);
+  if (static_cast<int64_t>(rhi) < 0) {                       // rem < 0: add M
+    const uint64_t nlo = rlo + mlo;
+    rhi = rhi + mhi + (nlo < rlo ? 1u : 0u);
+    rlo = nlo;
+  } else if (rhi > mhi || (rhi == mhi && rlo >= mlo)) {      // rem >= M: subtract M
+    const uint64_t nlo = rlo - mlo;
+    rhi = rhi - mhi - (rlo < mlo ? 1u : 0u);
+    rlo = nlo;
+  }
+  // balanced: rem > (M-1)/2 means rem - M
+  const uint64_t hlo = (mlo >> 1) | (mhi << 63), hhi = mhi >> 1;
+  if (rhi > hhi || (rhi == hhi && rlo > hlo)) {
+    const uint64_t nlo = rlo - mlo;
+    rhi = rhi - mhi - (rlo < mlo ? 1u : 0u);
+    rlo = nlo;
+  }
+  lo = rlo;
+  hi = rhi;
+}
+
+// RNE_f32(S * 2^E) for a signed 128-bit S = (hi:lo): the binary32 rule.
+__device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) {
+  const bool neg = static_cast<int64_t>(hi) < 0;
+  if (neg) {
+    lo = ~lo + 1;
+    hi = ~hi + (lo == 0 ? 1u : 0u);
+  }
+  const uint32_t sign = neg ? 0x80000000u : 0u;
+  int b;
+  if (hi) b = 64 + 63 - __clzll(static_cast<long long>(hi));
+  else if (lo) b = 63 - __clzll(static_cast<long long>(lo));
+  else return 0u;                                        // exact zero -> +0
+  const int lead = E + b;
+  if (lead >= 128) return sign | 0x7F800000u;
+  int qexp = max(lead - 23, -149);
+  const int s = qexp - E;                                // bit index of one ulp
+  uint64_t q;
+  if (s <= 0) {
+    q = lo << (-s);                                      // exact (fewer than 24 bits)
+  } else {
+    const int p = s - 1;                                 // rounding bit
+    uint64_t win;
+    bool sticky;
+    if (p < 64) {
+      win = p ? ((lo >> p) | (hi << (64 - p))) : lo;
+      sticky = p ? (lo & ((uint64_t(1) << p) - 1)) != 0 : false;
+    } else {
+      const int p2 = p - 64;
+      win = hi >> p2;
+      sticky = lo != 0 || (p2 ? (hi & ((uint64_t(1) << p2) - 1)) != 0 : false);
+    }
+    const uint64_t half = win & 1u;
+    q = (win >> 1) & 0xFFFFFFu;
+    if (half && (sticky || (q & 1u))) ++q;
+    if (q == (uint64_t(1) << 24)) {
+      q >>= 1;
+      ++qexp;
+    }
+  }
+  if (qexp > 104) return sign | 0x7F800000u;
+  const uint32_t bits = q >= (uint64_t(1) << 23)
+                            ? (static_cast<uint32_t>(qexp + 150) << 23) |
+                                  static_cast<uint32_t>(q - (uint64_t(1) << 23))
+                            : static_cast<uint32_t>(q);
+  return sign | bits;
+}
+
+// Deep products of output (m, n) added into t (bit 0 weighs 2^E); returns
+// false if one of them does not fit the window (the caller then takes the
+// digit route).  nf counts products with a non-finite operand.
+template <int kBf16>
+__device__ __noinline__ bool add_deep_products(const GemmArgs& g, const ReconArgs& ra, int64_t m,
+                                               int64_t n, int emA, int E, W192& t, int64_t& nf) {
+  bool fits = true;
+  const int na = min(ra.countA[m], ra.cap);
+  const int nb = min(ra.countB[n], ra.cap);
+  for (int q = 0; q < na; ++q) {                 // row m of A's deep elements x column n of B
+    const uint2 ent = ra.listA[m * ra.cap + q];
+    const int64_t k = ent.x;
+    const Decoded a = decode_f32_bits(ent.y);
+    const Decoded b = decode_f32_bits(load_bits<kBf16>(g.B, g.opB ? k * g.ldb + n : n * g.ldb + k));
+    if (a.nonfinite || b.nonfinite) {
+      ++nf;
+    } else if (a.m != 0 && b.m != 0) {
+      const int sh = a.e + b.e - E;
+      if (sh < 0 || sh > 140) fits = false;
+      else w192_add_shifted(t, static_cast<int64_t>(a.m) * b.m, sh);
+    }
+  }
+  for (int q = 0; q < nb; ++q) {                 // column n of B's deep elements x shallow row m
+    const uint2 ent = ra.listB[n * ra.cap + q];
+    const int64_t k = ent.x;
+    const Decoded b = decode_f32_bits(ent.y);
+    const Decoded a = decode_f32_bits(load_bits<kBf16>(g.A, g.opA ? k * g.lda + m : m * g.lda + k));
+    if (a.nonfinite || (a.m != 0 && a.e - emA + kDeepGap < 0)) continue;   // row m's list had it
+    if (b.nonfinite) {
+      ++nf;
+    } else if (a.m != 0 && b.m != 0) {
+      const int sh = a.e + b.e - E;
+      if (sh < 0 || sh > 140) fits = false;
+      else w192_add_shifted(t, static_cast<int64_t>(a.m) * b.m, sh);
+    }
+  }
+  return fits;
 }
 
 constexpr int kReconCols = 4;                       // outputs per thread (one row)
 
+// Fast path: det_gemm outputs whose row of A and column of B hold no deep
+// element -- CRT, then one rounding.  Nothing else, to keep registers low.
+template <int kBf16>
+__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra,
+                                                                        const __grid_constant__ CrtTable crt) {
+  const int64_t MN = g.M * g.N;
+  const int64_t tiles_n = (g.N + kTile - 1) / kTile;
+  const bool failed = ra.error != nullptr && *ra.error != 0;    // the tensor-core kernel gave up
+  const int64_t n0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) * kReconCols;
+  if (n0 >= g.N) return;
+  const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
+  const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
+                      (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
+  for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
+    if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
+    if (ra.countA[m] != 0) continue;                              // deep row: full kernel
+    int emA = ra.emaxA[m];
+    emA = emA == kEmaxEmpty ? 0 : emA;
+    const int64_t base = m * g.N + n0;
+    uint32_t packed[kNumModuli];
+    const bool vec = vec_ok && ncols == kReconCols;
+#pragma unroll
+    for (int i = 0; i < kNumModuli; ++i) {
+      packed[i] = 0;
+      if (i < ra.nplanes) {
+        const uint8_t* plane = ra.res + i * MN + base;
+        if (vec) {
+          packed[i] = *reinterpret_cast<const uint32_t*>(plane);
+        } else {
+#pragma unroll
+          for (int j = 0; j < kReconCols; ++j)
+            if (j < ncols) packed[i] |= static_cast<uint32_t>(plane[j]) << (8 * j);
+        }
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kReconCols; ++j) {
+      if (j >= ncols) break;
+      const int64_t n = n0 + j;
+      if (ra.countB[n] != 0) continue;                            // deep column: full kernel
+      uint32_t rj[kNumModuli];
+#pragma unroll
+      for (int i = 0; i < kNumModuli; ++i) rj[i] = (packed[i] >> (8 * j)) & 0xFFu;
+      uint64_t slo, shi;
+      crt_s128(rj, ra.nplanes, crt, slo, shi);
+      int emB = ra.emaxB[n];
+      emB = emB == kEmaxEmpty ? 0 : emB;
+      const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+      reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = failed ? kNanBits : round_s128(slo, shi, Es);
+    }
+  }
+}
+
+// Rows of A / columns of C with deep elements, compacted into index lists
+// (order irrelevant: every output is computed independently and exactly).
+__global__ void __launch_bounds__(kThreads) compact_deep_kernel(const int* countA, int64_t M,
+                                                                 const int* countB, int64_t N,
+                                                                 int* rows, int* cols, int* nrc) {
+  for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < M + N;
+       i += int64_t(gridDim.x) * kThreads) {
+    if (i < M) {
+      if (countA[i] != 0) rows[atomicAdd(nrc, 1)] = static_cast<int>(i);
+    } else if (countB[i - M] != 0) {
+      cols[atomicAdd(nrc + 1, 1)] = static_cast<int>(i - M);
+    }
+  }
+}
+
+// det_gemm outputs with deep entries: every output of a deep row, then every
+// output of a deep column outside the deep rows.  Dense work list, so the
+// warps stay full.
+template <int kBf16>
+__global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
+    GemmArgs g, ReconArgs ra, const __grid_constant__ CrtTable crt, const int* rows,
+    const int* cols, const int* nrc) {
+  const int64_t MN = g.M * g.N;
+  const int64_t tiles_n = (g.N + kTile - 1) / kTile;
+  const bool failed = ra.error != nullptr && *ra.error != 0;
+  const int64_t n_rows = nrc[0], n_cols = nrc[1];
+  const int64_t part1 = n_rows * g.N, total = part1 + g.M * n_cols;
+  for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
+       idx += int64_t(gridDim.x) * kThreads) {
+    int64_t m, n;
+    if (idx < part1) {
+      m = rows[idx / g.N];
+      n = idx - (idx / g.N) * g.N;
+    } else {
+      const int64_t j = idx - part1;
+      m = j / n_cols;
+      n = cols[j - m * n_cols];
+      if (ra.countA[m] != 0) continue;                          // done with its deep row
+    }
+    if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's output
+    int emA = ra.emaxA[m], emB = ra.emaxB[n];
+    emA = emA == kEmaxEmpty ? 0 : emA;
+    emB = emB == kEmaxEmpty ? 0 : emB;
+    uint32_t r[kNumModuli];
+#pragma unroll
+    for (int i = 0; i < kNumModuli; ++i) r[i] = i < ra.nplanes ? ra.res[i * MN + m * g.N + n] : 0u;
+    uint64_t slo, shi;
+    crt_s128(r, ra.nplanes, crt, slo, shi);
+    const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
+    W192 t;
+    t.w[0] = 0;
+    t.w[1] = slo;
+    t.w[2] = shi;
+    int64_t nf = 0;
+    const bool fits = add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf);
+    if (failed) nf = 1;
+    if (fits) {
+      reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_w192(t, E);
+    } else {
+      const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
+      output_via_digits<kBf16>(g, ra, m, n, t, E, true, S, emA, nf);
+    }
+  }
+}
+
+// Digit path: every output of det_gemm_partial.
 template <int kBf16>
 __global__ void __launch_bounds__(kThreads, 2) reconstruct_kernel(GemmArgs g, ReconArgs ra,
-                                                                const __grid_constant__ CrtTable crt) {
+                                                                   const __grid_constant__ CrtTable crt) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;
   const int64_t n0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) * kReconCols;
   if (n0 >= g.N) return;
   const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
+  const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
+                      (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
 
   for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
     if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
     int emA = ra.emaxA[m];
     emA = emA == kEmaxEmpty ? 0 : emA;
-    const int na = min(ra.countA[m], ra.cap);
+    const bool row_deep = ra.countA[m] != 0;
     const int64_t base = m * g.N + n0;
     // residues of the (up to) four outputs: one packed word per plane
     uint32_t packed[kNumModuli];
-    // word loads need every plane's address 4-byte aligned: base and M*N both
-    // multiples of 4 (the residue buffer itself is 1024-byte aligned)
-    const bool vec = ncols == kReconCols && ((base | MN) & 3) == 0 &&
-                     (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
+    const bool vec = vec_ok && ncols == kReconCols;
 #pragma unroll
     for (int i = 0; i < kNumModuli; ++i) {
       packed[i] = 0;
@@ -403,58 +637,30 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_kernel(GemmArgs g, Re
       uint32_t rj[kNumModuli];                      // this output's residues
 #pragma unroll
       for (int i = 0; i < kNumModuli; ++i) rj[i] = (packed[i] >> (8 * j)) & 0xFFu;
-      const __int128 S = crt_balanced(rj, ra.nplanes, crt);
+      uint64_t slo, shi;
+      crt_s128(rj, ra.nplanes, crt, slo, shi);
       int emB = ra.emaxB[n];
       emB = emB == kEmaxEmpty ? 0 : emB;
-      const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
+      const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);   // S's bit 0 weighs 2^Es
+      const bool deep = row_deep || ra.countB[n] != 0;
+      // deep elements: S * 2^64 and their products in a 192-bit window
+      const int E = Es - 64;
       W192 t;
       t.w[0] = 0;
-      t.w[1] = static_cast<uint64_t>(S);
-      t.w[2] = static_cast<uint64_t>(S >> 64);
+      t.w[1] = slo;
+      t.w[2] = shi;
       int64_t nf = 0;
-      bool wide = false;
-      const int nb = min(ra.countB[n], ra.cap);
-      // deep elements: row m of A with every element of column n of B, then
-      // column n of B with the shallow (or zero) elements of row m
-      for (int q = 0; q < na; ++q) {
-        const uint2 ent = ra.listA[m * ra.cap + q];
-        const int64_t k = ent.x;
-        const Decoded a = decode_f32_bits(ent.y);
-        const Decoded b =
-            decode_f32_bits(load_bits<kBf16>(g.B, g.opB ? k * g.ldb + n : n * g.ldb + k));
-        if (a.nonfinite || b.nonfinite) {
-          ++nf;
-        } else if (a.m != 0 && b.m != 0) {
-          const int sh = a.e + b.e - E;
-          if (sh < 0 || sh > 140) wide = true;
-          else w192_add_shifted(t, static_cast<int64_t>(a.m) * b.m, sh);
-        }
-      }
-      for (int q = 0; q < nb; ++q) {
-        const uint2 ent = ra.listB[n * ra.cap + q];
-        const int64_t k = ent.x;
-        const Decoded b = decode_f32_bits(ent.y);
-        const Decoded a =
-            decode_f32_bits(load_bits<kBf16>(g.A, g.opA ? k * g.lda + m : m * g.lda + k));
-        if (a.nonfinite || (a.m != 0 && a.e - emA + kDeepGap < 0)) continue;  // row m's list had it
-        if (b.nonfinite) {
-          ++nf;
-        } else if (a.m != 0 && b.m != 0) {
-          const int sh = a.e + b.e - E;
-          if (sh < 0 || sh > 140) wide = true;
-          else w192_add_shifted(t, static_cast<int64_t>(a.m) * b.m, sh);
-        }
-      }
+      const bool fits = deep ? add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf) : true;
       if (failed) nf = 1;
-      if (!wide && g.P == nullptr) {
+      if (fits && g.P == nullptr) {
         reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_w192(t, E);
       } else {
-        output_via_digits<kBf16>(g, ra, m, n, t, E, wide, S, emA, nf);
+        const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
+        output_via_digits<kBf16>(g, ra, m, n, t, E, !fits, S, emA, nf);
       }
     }
   }
 }
-
 
 }  // namespace
 
@@ -504,16 +710,39 @@ CrtTable make_crt_table(int nplanes) {
   return t;
 }
 
-cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream) {
+cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
+                               int* deep_counters, cudaStream_t stream) {
   const int64_t MN = g.M * g.N;
   if (MN == 0) return cudaSuccess;
   const CrtTable crt = make_crt_table(ra.nplanes);
   const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
   dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
             static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
-  if (g.bf16) reconstruct_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra, crt);
-  else reconstruct_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra, crt);
-  note_launch();
+  if (g.P != nullptr) {
+    if (g.bf16) reconstruct_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra, crt);
+    else reconstruct_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra, crt);
+    note_launch();
+    return cudaGetLastError();
+  }
+  if (g.bf16) reconstruct_fast_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra, crt);
+  else reconstruct_fast_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra, crt);
+  // deep rows and columns: index lists [M] and [N], and their two counters
+  int* rows = deep_lists;
+  int* cols = deep_lists + g.M;
+  int* nrc = deep_counters;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int64_t cgrid = (g.M + g.N + kThreads - 1) / kThreads;
+  compact_deep_kernel<<<static_cast<unsigned>(cgrid < sms * 8 ? cgrid : sms * 8), kThreads, 0,
+                        stream>>>(ra.countA, g.M, ra.countB, g.N, rows, cols, nrc);
+  const unsigned dgrid = static_cast<unsigned>(sms) * 4;
+  if (g.bf16)
+    reconstruct_deep_kernel<1><<<dgrid, kThreads, 0, stream>>>(g, ra, crt, rows, cols, nrc);
+  else
+    reconstruct_deep_kernel<0><<<dgrid, kThreads, 0, stream>>>(g, ra, crt, rows, cols, nrc);
+  note_launch(3);
   return cudaGetLastError();
 }
 
