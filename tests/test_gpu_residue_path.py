@@ -1,0 +1,99 @@
+"""Parity of the tensor-core residue path against the oracle, bit for bit.
+
+det_gemm routes tiles whose rows and columns hold few "deep" elements (more
+than 19 binades below their row maximum) to the residue decomposition on the
+tensor cores, and other tiles to the general Kulisch kernel.  These cases aim
+at the residue path's own corners: the longest K (14 moduli, 512 exact fp32
+accumulation windows reduced in TMEM), bf16 planes, deep elements handled
+from the per-row lists (inside and outside the 192-bit window), non-finite
+values next to deep ones, and matrices whose tiles are split between the two
+kernels.  Every expected value comes from the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_sum_gemm_gb300 as dg
+from exact_sum_gemm_gb300 import workloads as wl
+from gpu_util import assert_bits_equal, bits_of, dev_bf16, dev_f32, np_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def test_k_limit_normal_data_takes_the_tensor_core_path(oracle_mod):
+    K = 1 << 19
+    A = wl.normal_f32((256, K), 13, 0)
+    B = wl.normal_f32((256, K), 13, 1)
+    assert dg.library().det_residue_moduli(0, K) == 14
+    got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
+    rows, cols = np.array([0, 131, 255]), np.arange(0, 256, 5)
+    want = np_bits(oracle_mod.gemm(A[rows], B[cols]))
+    assert_bits_equal(got[np.ix_(rows, cols)], want, "K=2^19 N(0,1)")
+
+
+def test_bf16_normal_data_takes_the_tensor_core_path(oracle_mod):
+    g = np.random.default_rng(17)
+    a = (g.standard_normal((300, 4096)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    b = (g.standard_normal((260, 4096)).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    want = np_bits(oracle_mod.gemm(a, b, dtype="bf16"))
+    assert_bits_equal(bits_of(dg.det_gemm(dev_bf16(a), dev_bf16(b))), want, "bf16 N(0,1)")
+    np.testing.assert_array_equal(dg.det_gemm_partial(dev_bf16(a), dev_bf16(b)).cpu().numpy(),
+                                  oracle_mod.gemm_digits(a, b, dtype="bf16"))
+
+
+def test_planted_deep_elements(oracle_mod):
+    g = np.random.default_rng(23)
+    M, N, K = 200, 190, 3000
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((N, K)).astype(np.float32)
+    # deep but inside the 192-bit window: ~2^-25 relative to the row max
+    A[5, 100] = np.float32(3e-8)
+    A[5, 2000] = np.float32(-1e-7)
+    B[7, 100] = np.float32(2e-8)
+    # far below the window: the digit route
+    A[9, 50] = np.float32(1e-35)
+    B[11, 2999] = np.float32(-3e-38)
+    B[12, 17] = np.float32(1e-45)              # subnormal
+    # a deep element and a non-finite one on the same row / column
+    A[20, 30] = np.float32(1e-9)
+    A[20, 31] = np.float32(np.inf)
+    B[40, 30] = np.float32(np.nan)
+    a, b = dev_f32(A), dev_f32(B)
+    want = np_bits(oracle_mod.gemm(A, B))
+    assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, "planted deep elements")
+    np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B))
+
+
+def test_tiles_split_between_tensor_cores_and_general_kernel(oracle_mod):
+    g = np.random.default_rng(29)
+    M, N, K = 300, 280, 1024
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((N, K)).astype(np.float32)
+    # rows 64..127 of A and columns 128..191 of C get wide exponents: those
+    # tiles go to the general kernel, the rest to the residue path
+    A[64:128] = wl.loguniform_f32((64, K), 29, 0, lo=-60, hi=60)
+    B[128:192] = wl.loguniform_f32((64, K), 29, 1, lo=-60, hi=60)
+    want = np_bits(oracle_mod.gemm(A, B))
+    assert_bits_equal(bits_of(dg.det_gemm(dev_f32(A), dev_f32(B))), want, "mixed routing")
+
+
+def test_transposed_operands_on_tensor_core_path(oracle_mod):
+    # the DetLinear dgrad / wgrad layouts with narrow exponents
+    A = wl.normal_f32((192, 700), 31, 0)
+    B = wl.normal_f32((320, 700), 31, 1)
+    want = np_bits(oracle_mod.gemm(A, B))
+    at = dev_f32(np.ascontiguousarray(A.T)).t()
+    bt = dev_f32(np.ascontiguousarray(B.T)).t()
+    assert_bits_equal(bits_of(dg.det_gemm(at, bt)), want, "TT on residue path")
+
+
+def test_all_zero_rows_and_exact_cancellation(oracle_mod):
+    g = np.random.default_rng(37)
+    A = g.standard_normal((130, 512)).astype(np.float32)
+    B = g.standard_normal((140, 512)).astype(np.float32)
+    A[3] = 0.0
+    B[:, 256:] = B[:, :256]
+    A[:, 256:] = -A[:, :256]                   # every output cancels to exactly +0
+    got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
+    assert np.all(got == 0)
+    assert_bits_equal(got, np_bits(oracle_mod.gemm(A, B)), "cancellation")
