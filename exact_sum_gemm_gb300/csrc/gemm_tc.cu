@@ -10,7 +10,8 @@
 // accumulating on top of the reduced value.  The result is the exact integer
 // dot product modulo p_u; the CRT in residue.cu rebuilds the exact sum.
 //
-// Structure (one CTA per 128x256 output tile and pair of moduli, 1 CTA per SM):
+// Structure (persistent, one CTA per SM, looping over units = (pair of moduli,
+// 128x256 output tile), pair-major):
 //   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
 //               rows), 128-byte swizzled, 4-stage mbarrier ring
 //   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
@@ -95,14 +96,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(acc_free + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t m0 = int64_t(blockIdx.y) * kBlockM;
-  const int64_t n0 = int64_t(blockIdx.x) * kBlockN;
-  // this CTA's moduli: the pair (2z, 2z+1), or the last one alone
-  const int u_base = 2 * static_cast<int>(blockIdx.z);
-  const int P = min(2, a.nplanes - u_base);
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
-  const int njobs = P * nch;
+  // work units: (pair of moduli, output tile), pair-major so that the CTAs in
+  // flight share the same two planes of A and B in L2
+  const int64_t tiles_n = (a.N + kBlockN - 1) / kBlockN;
+  const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * tiles_n;
+  const int64_t units = tiles * ((a.nplanes + 1) / 2);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -127,12 +127,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // unit -> this unit's tile origin and moduli (the pair (2z, 2z+1), or the last alone)
+  auto unit_at = [&](int64_t unit, int64_t& m0, int64_t& n0, int& u_base, int& P) {
+    const int64_t z = unit / tiles, t = unit - z * tiles;
+    m0 = (t / tiles_n) * kBlockM;
+    n0 = (t - (t / tiles_n) * tiles_n) * kBlockN;
+    u_base = 2 * static_cast<int>(z);
+    P = min(2, a.nplanes - u_base);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
       bool ok = true;
       uint32_t it = 0;
-      for (int J = 0; J < njobs && ok; ++J) {
+      for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+      int64_t m0, n0;
+      int u_base, P;
+      unit_at(unit, m0, n0, u_base, P);
+      for (int J = 0; J < P * nch && ok; ++J) {
         int u, c;
         job_at(J, P, nch, u, c);
         u += u_base;
@@ -149,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::tma_load_3d(st + kABytes, &tmB, &full[s], kb * kStageK, static_cast<int>(n0), u);
           ++it;
         }
+      }
       }
       // drain before the CTA may exit: the copies still in flight, then (on the
       // normal path) the MMA's release of the last stages, whose commits
@@ -167,7 +180,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it = 0;
       uint32_t uses[2] = {0u, 0u};
-      for (int J = 0; J < njobs && ok; ++J) {
+      for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+      int64_t m0, n0;
+      int u_base, P;
+      unit_at(unit, m0, n0, u_base, P);
+      for (int J = 0; J < P * nch && ok; ++J) {
         int u, c;
         job_at(J, P, nch, u, c);
         u += u_base;
@@ -203,15 +220,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         ptx::mma_commit(&acc_ready[acc]);  // chunk c of modulus u is in TMEM
       }
+      }
       if (!ok) atomicExch(a.error, 1);
     }
   } else {
     const int g = warp & 3;                // TMEM lanes 32g .. 32g+31
-    const int64_t row = m0 + 32 * g + lane;
     const int64_t MN = a.M * a.N;
     bool ok = true;
     uint32_t uses[2] = {0u, 0u};
-    for (int J = 0; J < njobs; ++J) {
+    for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
+    int64_t m0, n0;
+    int u_base, P;
+    unit_at(unit, m0, n0, u_base, P);
+    const int64_t row = m0 + 32 * g + lane;
+    for (int J = 0; J < P * nch; ++J) {
       int u, c;
       job_at(J, P, nch, u, c);
       u += u_base;
@@ -267,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ptx::tc_fence_before();
       __syncwarp();
       if (lane == 0) ptx::mbar_arrive(&acc_free[acc]);
+    }
     }
     if (!ok && lane == 0) atomicExch(a.error, 1);
   }
@@ -325,9 +348,14 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kBlockM) ||
       !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kBlockN))
     return cudaErrorInvalidValue;
-  dim3 grid(static_cast<unsigned>((a.N + kBlockN - 1) / kBlockN),
-            static_cast<unsigned>((a.M + kBlockM - 1) / kBlockM),
-            static_cast<unsigned>((a.nplanes + 1) / 2));
+  // persistent: one CTA per SM (the shared memory and TMEM footprint allow no more)
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
+  const int64_t units = ((a.M + kBlockM - 1) / kBlockM) * ((a.N + kBlockN - 1) / kBlockN) *
+                        ((a.nplanes + 1) / 2);
+  const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   note_launch();
   return cudaGetLastError();
