@@ -73,6 +73,19 @@ def dist_env():
     return world, rank, local
 
 
+def max_over_ranks(value, dist, device):
+    """The largest of every rank's value (the job's time is its slowest rank's)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def rank_seed(rank):
+    """Each rank runs its own independent problem: seed = rank."""
+    return int(rank)
+
+
 def make_inputs(seed, workload):
     from exact_sum_gemm_gb300 import workloads as wl
     if workload == "normal":
@@ -286,7 +299,7 @@ def run_ours(args):
     from exact_sum_gemm_gb300 import _native
     lib = dg.library()
 
-    A, B = make_inputs(rank, args.workload)
+    A, B = make_inputs(rank_seed(rank), args.workload)
     a = torch.from_numpy(A).to(dev)
     b = torch.from_numpy(B).to(dev)
     c = torch.empty((M, N), dtype=torch.float32, device=dev)
@@ -334,9 +347,7 @@ def run_ours(args):
     elapsed_ms = start.elapsed_time(end)
     kern_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     if dist is not None:
-        t = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+        elapsed_ms = max_over_ranks(elapsed_ms, dist, dev)
     ms_per_step = elapsed_ms / args.steps
     flops = 2.0 * M * N * K
     value = flops * world / (ms_per_step * 1e-3) / 1e9
