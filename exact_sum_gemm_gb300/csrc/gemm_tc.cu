@@ -10,8 +10,8 @@
 // accumulating on top of the reduced value.  The result is the exact integer
 // dot product modulo p_u; the CRT in residue.cu rebuilds the exact sum.
 //
-// Structure (persistent, one CTA per SM, looping over units = (pair of moduli,
-// 128x256 output tile), pair-major):
+// Structure (persistent, one CTA per SM, looping over units = (modulus, pair
+// of neighbouring 128x256 output tiles), modulus-major):
 //   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
 //               rows), 128-byte swizzled, 4-stage mbarrier ring
 //   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
@@ -20,8 +20,8 @@
 //               lanes = 32 rows), reduce modulo p_u with exact fp32
 //               arithmetic, tcgen05.st it back (or, after the last chunk,
 //               store the residues to global memory)
-// Two moduli are interleaved chunk by chunk on the two accumulators, so the
-// MMA of one modulus overlaps the in-TMEM reduction of the other.
+// A unit's two tiles are interleaved chunk by chunk on the two accumulators,
+// so the MMA of one tile overlaps the in-TMEM reduction of the other.
 // Every mbarrier wait is bounded (about 2 s): on expiry the kernel records an
 // error flag (the reconstruction then emits NaN), drains its copies in flight,
 // frees TMEM and returns.
@@ -68,19 +68,11 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
   }
 }
 
-// Job J -> (modulus u, K chunk c).  Moduli are taken in pairs (2q, 2q+1);
-// within a pair the chunks alternate between the two moduli.
-__device__ __forceinline__ void job_at(int J, int P, int nch, int& u, int& c) {
-  const int pair_jobs = 2 * nch;
-  const int full = (P / 2) * pair_jobs;
-  if (J < full) {
-    const int q = J / pair_jobs, rem = J - q * pair_jobs;
-    c = rem >> 1;
-    u = 2 * q + (rem & 1);
-  } else {
-    c = J - full;
-    u = P - 1;
-  }
+// Job J of a unit holding T (1 or 2) tiles -> (tile index tt < T, K chunk c):
+// the chunks alternate between the unit's tiles (and their accumulators).
+__device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
+  c = J / T;
+  tt = J - c * T;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -98,11 +90,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
-  // work units: (pair of moduli, output tile), pair-major so that the CTAs in
-  // flight share the same two planes of A and B in L2
+  // work units: (modulus, pair of neighbouring output tiles), modulus-major so
+  // that the CTAs in flight share one plane of A and one of B in L2
   const int64_t tiles_n = (a.N + kBlockN - 1) / kBlockN;
   const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * tiles_n;
-  const int64_t units = tiles * ((a.nplanes + 1) / 2);
+  const int64_t tile_pairs = (tiles + 1) / 2;
+  const int64_t units = tile_pairs * a.nplanes;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -127,13 +120,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  // unit -> this unit's tile origin and moduli (the pair (2z, 2z+1), or the last alone)
-  auto unit_at = [&](int64_t unit, int64_t& m0, int64_t& n0, int& u_base, int& P) {
-    const int64_t z = unit / tiles, t = unit - z * tiles;
+  // unit -> its modulus, first tile and tile count (2, or 1 for an odd last tile)
+  auto unit_at = [&](int64_t unit, int& u, int64_t& t0, int& T) {
+    u = static_cast<int>(unit / tile_pairs);
+    t0 = 2 * (unit - static_cast<int64_t>(u) * tile_pairs);
+    T = t0 + 1 < tiles ? 2 : 1;
+  };
+  auto tile_origin = [&](int64_t t, int64_t& m0, int64_t& n0) {
     m0 = (t / tiles_n) * kBlockM;
     n0 = (t - (t / tiles_n) * tiles_n) * kBlockN;
-    u_base = 2 * static_cast<int>(z);
-    P = min(2, a.nplanes - u_base);
   };
 
   if (warp == 0) {
@@ -141,13 +136,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it = 0;
       for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
-      int64_t m0, n0;
-      int u_base, P;
-      unit_at(unit, m0, n0, u_base, P);
-      for (int J = 0; J < P * nch && ok; ++J) {
-        int u, c;
-        job_at(J, P, nch, u, c);
-        u += u_base;
+      int u, T;
+      int64_t t0;
+      unit_at(unit, u, t0, T);
+      for (int J = 0; J < T * nch && ok; ++J) {
+        int tt, c;
+        job_at(J, T, tt, c);
+        int64_t m0, n0;
+        tile_origin(t0 + tt, m0, n0);
         const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
         for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -181,14 +177,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0;
       uint32_t uses[2] = {0u, 0u};
       for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
-      int64_t m0, n0;
-      int u_base, P;
-      unit_at(unit, m0, n0, u_base, P);
-      for (int J = 0; J < P * nch && ok; ++J) {
-        int u, c;
-        job_at(J, P, nch, u, c);
-        u += u_base;
-        const int acc = u & 1;
+      int u, T;
+      int64_t t0;
+      unit_at(unit, u, t0, T);
+      for (int J = 0; J < T * nch && ok; ++J) {
+        int tt, c;
+        job_at(J, T, tt, c);
+        const int acc = tt;
         if (!wait_bounded(&acc_free[acc], (uses[acc] & 1u) ^ 1u)) {
           ok = false;
           break;
@@ -229,15 +224,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t uses[2] = {0u, 0u};
     for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
-    int64_t m0, n0;
-    int u_base, P;
-    unit_at(unit, m0, n0, u_base, P);
-    const int64_t row = m0 + 32 * g + lane;
-    for (int J = 0; J < P * nch; ++J) {
-      int u, c;
-      job_at(J, P, nch, u, c);
-      u += u_base;
-      const int acc = u & 1;
+    int u, T;
+    int64_t t0;
+    unit_at(unit, u, t0, T);
+    for (int J = 0; J < T * nch; ++J) {
+      int tt, c;
+      job_at(J, T, tt, c);
+      int64_t m0, n0;
+      tile_origin(t0 + tt, m0, n0);
+      const int64_t row = m0 + 32 * g + lane;
+      const int acc = tt;
       if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
         ok = false;
         break;
@@ -353,8 +349,8 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int64_t units = ((a.M + kBlockM - 1) / kBlockM) * ((a.N + kBlockN - 1) / kBlockN) *
-                        ((a.nplanes + 1) / 2);
+  const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * ((a.N + kBlockN - 1) / kBlockN);
+  const int64_t units = (tiles + 1) / 2 * a.nplanes;
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   note_launch();
