@@ -279,6 +279,41 @@ __device__ __forceinline__ void add_product(int64_t (&d)[kDigits], int32_t ma, i
   for (int pl = 0; pl < kDigits; ++pl) d[pl] += pl == j ? lo : pl == j + 1 ? hi : 0;
 }
 
+// Bits [pos, pos+32) of the 192-bit two's-complement t (zero below bit 0,
+// sign bits above bit 191).
+__device__ __forceinline__ uint32_t w192_bits32(const W192& t, int pos) {
+  const uint64_t sx = static_cast<int64_t>(t.w[2]) < 0 ? ~uint64_t(0) : uint64_t(0);
+  if (pos <= -32) return 0u;
+  if (pos < 0) return static_cast<uint32_t>(t.w[0] << (-pos));
+  if (pos >= 192) return static_cast<uint32_t>(sx);
+  const int w = pos >> 6, r = pos & 63;
+  const uint64_t lo = w == 0 ? t.w[0] : (w == 1 ? t.w[1] : t.w[2]);
+  const uint64_t hi = w == 0 ? t.w[1] : (w == 1 ? t.w[2] : sx);
+  return static_cast<uint32_t>(r ? ((lo >> r) | (hi << (64 - r))) : lo);
+}
+
+// The canonical digits of t * 2^E (a multiple of 2^-298 whose magnitude is
+// below 2^(575-298)) written as one output's 20 planes.
+__device__ __forceinline__ void write_canonical_digits(int64_t* out, int64_t MN, W192 t, int E,
+                                                       int64_t K, int64_t nf) {
+  int off = E + kLsbBias;                       // bit offset of t's bit 0 in the digits
+  while (off < 0) {                             // the low bits are zero: shift exactly
+    const int st = -off > 63 ? 63 : -off;
+    t.w[0] = (t.w[0] >> st) | (t.w[1] << (64 - st));
+    t.w[1] = (t.w[1] >> st) | (t.w[2] << (64 - st));
+    t.w[2] = static_cast<uint64_t>(static_cast<int64_t>(t.w[2]) >> st);
+    off += st;
+  }
+#pragma unroll
+  for (int j = 0; j < kDigits - 1; ++j)
+    out[j * MN] = static_cast<int64_t>(w192_bits32(t, 32 * j - off));
+  // digit 17: the signed value of bits 544 and up (fits in 32 bits)
+  const int pos = 32 * (kDigits - 1) - off;
+  out[(kDigits - 1) * MN] = static_cast<int64_t>(static_cast<int32_t>(w192_bits32(t, pos)));
+  out[kDigits * MN] = K;
+  out[(kDigits + 1) * MN] = nf;
+}
+
 // Cold path of one output: the digit route.  Used for det_gemm_partial (the
 // digits are the output) and when a deep product falls outside the 192-bit
 // window; rebuilds the exact value as 18 int64 digits and writes it.
@@ -595,69 +630,43 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
   }
 }
 
-// Digit path: every output of det_gemm_partial.
+// Digit path: every output of det_gemm_partial.  One output per thread, so
+// that each of the 20 plane stores of a warp is one contiguous 256-byte write.
 template <int kBf16>
 __global__ void __launch_bounds__(kThreads, 2) reconstruct_kernel(GemmArgs g, ReconArgs ra,
                                                                    const __grid_constant__ CrtTable crt) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;
-  const int64_t n0 = (int64_t(blockIdx.x) * kThreads + threadIdx.x) * kReconCols;
-  if (n0 >= g.N) return;
-  const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
-  const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
-                      (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
-
+  const int64_t n = int64_t(blockIdx.x) * kThreads + threadIdx.x;
+  if (n >= g.N) return;
+  int emB = ra.emaxB[n];
+  emB = emB == kEmaxEmpty ? 0 : emB;
+  const bool col_deep = ra.countB[n] != 0;
   for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
-    if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
+    if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;    // general kernel's outputs
     int emA = ra.emaxA[m];
     emA = emA == kEmaxEmpty ? 0 : emA;
-    const bool row_deep = ra.countA[m] != 0;
-    const int64_t base = m * g.N + n0;
-    // residues of the (up to) four outputs: one packed word per plane
-    uint32_t packed[kNumModuli];
-    const bool vec = vec_ok && ncols == kReconCols;
+    const int64_t idx = m * g.N + n;
+    uint32_t r[kNumModuli];
 #pragma unroll
-    for (int i = 0; i < kNumModuli; ++i) {
-      packed[i] = 0;
-      if (i < ra.nplanes) {
-        const uint8_t* plane = ra.res + i * MN + base;
-        if (vec) {
-          packed[i] = *reinterpret_cast<const uint32_t*>(plane);
-        } else {
-#pragma unroll
-          for (int j = 0; j < kReconCols; ++j)
-            if (j < ncols) packed[i] |= static_cast<uint32_t>(plane[j]) << (8 * j);
-        }
-      }
-    }
-#pragma unroll 1
-    for (int j = 0; j < ncols; ++j) {
-      const int64_t n = n0 + j;
-      uint32_t rj[kNumModuli];                      // this output's residues
-#pragma unroll
-      for (int i = 0; i < kNumModuli; ++i) rj[i] = (packed[i] >> (8 * j)) & 0xFFu;
-      uint64_t slo, shi;
-      crt_s128(rj, ra.nplanes, crt, slo, shi);
-      int emB = ra.emaxB[n];
-      emB = emB == kEmaxEmpty ? 0 : emB;
-      const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);   // S's bit 0 weighs 2^Es
-      const bool deep = row_deep || ra.countB[n] != 0;
-      // deep elements: S * 2^64 and their products in a 192-bit window
-      const int E = Es - 64;
-      W192 t;
-      t.w[0] = 0;
-      t.w[1] = slo;
-      t.w[2] = shi;
-      int64_t nf = 0;
-      const bool fits = deep ? add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf) : true;
-      if (failed) nf = 1;
-      if (fits && g.P == nullptr) {
-        reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_w192(t, E);
-      } else {
-        const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
-        output_via_digits<kBf16>(g, ra, m, n, t, E, !fits, S, emA, nf);
-      }
+    for (int i = 0; i < kNumModuli; ++i) r[i] = i < ra.nplanes ? ra.res[i * MN + idx] : 0u;
+    uint64_t slo, shi;
+    crt_s128(r, ra.nplanes, crt, slo, shi);
+    const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;   // bit 0 of S * 2^64
+    W192 t;
+    t.w[0] = 0;
+    t.w[1] = slo;
+    t.w[2] = shi;
+    int64_t nf = 0;
+    const bool deep = col_deep || ra.countA[m] != 0;
+    const bool fits = deep ? add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf) : true;
+    if (failed) nf = 1;
+    if (fits) {
+      write_canonical_digits(g.P + idx, MN, t, E, g.K, nf);
+    } else {
+      const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
+      output_via_digits<kBf16>(g, ra, m, n, t, E, true, S, emA, nf);
     }
   }
 }
@@ -719,8 +728,10 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
   dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
             static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
   if (g.P != nullptr) {
-    if (g.bf16) reconstruct_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra, crt);
-    else reconstruct_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra, crt);
+    dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
+               static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
+    if (g.bf16) reconstruct_kernel<1><<<pgrid, kThreads, 0, stream>>>(g, ra, crt);
+    else reconstruct_kernel<0><<<pgrid, kThreads, 0, stream>>>(g, ra, crt);
     note_launch();
     return cudaGetLastError();
   }
