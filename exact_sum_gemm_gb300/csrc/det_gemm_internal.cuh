@@ -19,6 +19,7 @@ struct Scratch {
   int* deepA;          // [M]   (deepB follows contiguously)
   int* deepB;          // [N]
   uint8_t* route;      // [tiles of 64x64]: 1 = general kernel
+  int* general;        // [1 + tiles]: count, then the indices of the tiles routed to the general kernel
   int64_t* fallback;   // [slots][kPlanes][kTile*kTile] band-kernel fallback digits (det_gemm only)
   int64_t slots;       // resident band-kernel CTAs (fallback regions)
 };
@@ -35,9 +36,10 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
 // deep counts produced elsewhere (the residue kernel's list counters).
 cudaError_t launch_emax(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
-                            cudaStream_t stream);
+                            int* general, cudaStream_t stream);
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
-cudaError_t launch_kulisch(const GemmArgs& g, const uint8_t* route, cudaStream_t stream);
+// General kernel over the 64x64 tiles listed in general (count first).
+cudaError_t launch_kulisch(const GemmArgs& g, const int* general, cudaStream_t stream);
 
 // Pre-pass + band + general kernels with caller-provided scratch of at least
 // scratch_bytes(g, slots) bytes (256-byte aligned).

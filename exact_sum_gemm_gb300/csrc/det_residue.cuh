@@ -20,13 +20,52 @@ __host__ __device__ constexpr int modulus(int i) {
        : i == 6 ? 233 : i == 7 ? 229 : i == 8 ? 227 : i == 9 ? 223 : i == 10 ? 217 : i == 11 ? 211
        : i == 12 ? 199 : 197;
 }
-// (p_0 * ... * p_{i-1})^{-1} mod p_i, for Garner's CRT (compile-time use).
-__host__ __device__ constexpr int garner_inverse(int i) {
-  int prod = 1;
-  for (int j = 0; j < i; ++j) prod = (prod * (modulus(j) % modulus(i))) % modulus(i);
-  for (int c = 1; c < modulus(i); ++c)
-    if ((prod * c) % modulus(i) == 1) return c;
-  return 1;
+// Garner's mixed-radix constants (compile time).  With P_i = p_0 * ... *
+// p_{i-1}, the digits of S = sum_i v_i P_i satisfy
+//   v_i = r_i g_i + sum_{j<i} v_j d_ij  (mod p_i),
+//   g_i = P_i^-1 mod p_i,   d_ij = -P_j g_i mod p_i,
+// all taken as balanced representatives (magnitude <= (p_i - 1) / 2).
+__host__ __device__ constexpr int balanced_rep(long long x, int p) {
+  long long r = x % p;
+  if (r < 0) r += p;
+  return static_cast<int>(r > (p - 1) / 2 ? r - p : r);
+}
+__host__ __device__ constexpr int prefix_product_mod(int j, int i) {   // P_j mod p_i
+  int r = 1;
+  for (int l = 0; l < j; ++l) r = (r * (modulus(l) % modulus(i))) % modulus(i);
+  return r;
+}
+__host__ __device__ constexpr int inverse_mod(int a, int p) {
+  for (int c = 1; c < p; ++c)
+    if ((a * c) % p == 1) return c;
+  return 0;
+}
+__host__ __device__ constexpr int garner_g(int i) {
+  return balanced_rep(inverse_mod(prefix_product_mod(i, i), modulus(i)), modulus(i));
+}
+__host__ __device__ constexpr int garner_d(int i, int j) {
+  return balanced_rep(-static_cast<long long>(prefix_product_mod(j, i)) * garner_g(i), modulus(i));
+}
+
+// Exact modular reduction in binary32 (integers below 2^24 are exact there,
+// and the fp32 FMA pipes outrun the integer multiplier).  For an integer-
+// valued a with |a| <= 2^24 and an odd modulus p in [197, 255], with
+// inv_p = fl(1/p) (so |a * inv_p| < 2^17, where adding 1.5*2^23 rounds to an
+// integer):
+//   q = (a * inv_p + 1.5*2^23) - 1.5*2^23      (one rounding to an integer)
+//   r = a - q * p                               (one fma: exact, r is small)
+// inv_p has relative error below 2^-24, so before rounding q is within
+// |a|/p * 2^-23 of the real a/p.  a/p is never a half-integer (p is odd) and
+// a non-integer a/p lies at least 1/(2p) > 2^-9 from one; so whenever
+// |a| < 2^14 * p the rounding gives the nearest integer and r is the balanced
+// residue in [-(p-1)/2, (p-1)/2].  For larger |a| (up to 2^24) q may be one
+// off and |r| <= p/2 + p * 2^-6.6 < 131.  A zero result is +0 unless a is -0.
+constexpr float kRoundMagic = 12582912.0f;           // 1.5 * 2^23
+constexpr int kRoundMagicBits = 0x4B400000;
+
+__device__ __forceinline__ float near_mod_f32(float a, float p, float inv_p) {
+  const float q = __fsub_rn(__fmaf_rn(a, inv_p, kRoundMagic), kRoundMagic);
+  return __fmaf_rn(-q, p, a);
 }
 
 constexpr int kChunkK = 1024;     // K per exact fp32 accumulation window
@@ -47,7 +86,7 @@ struct ResidueOperand {
 };
 
 struct ReconArgs {
-  const uint8_t* res;         // [nplanes][M][N] residues in [0, p_i)
+  const int8_t* res;          // [nplanes][M][N] balanced residues, |r| <= (p_i - 1) / 2
   int nplanes;
   const int* emaxA;
   const int* emaxB;
@@ -71,7 +110,7 @@ struct ResGemmArgs {
   const __nv_bfloat16* B;     // [nplanes][N][Kp]
   int64_t M, N, Kp;
   int nplanes;
-  uint8_t* res;               // [nplanes][M][N]
+  int8_t* res;                // [nplanes][M][N] balanced residues
   int* error;
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);

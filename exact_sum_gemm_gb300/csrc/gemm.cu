@@ -62,6 +62,7 @@ size_t scratch_bytes(const GemmArgs& g, int64_t slots) {
   size_t b = align_up(sizeof(int) * size_t(g.M + g.N), 256);        // emax
   b += align_up(sizeof(int) * size_t(g.M + g.N), 256);              // deep
   b += align_up(size_t(tiles), 256);                                 // route
+  b += align_up(sizeof(int) * size_t(tiles + 1), 256);              // general-tile list
   if (g.P == nullptr) b += sizeof(int64_t) * size_t(slots) * kPlanes * kTile * kTile;
   return b;
 }
@@ -78,6 +79,8 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots) {
   p += align_up(sizeof(int) * size_t(g.M + g.N), 256);
   s.route = reinterpret_cast<uint8_t*>(p);
   p += align_up(size_t(tiles), 256);
+  s.general = reinterpret_cast<int*>(p);
+  p += align_up(sizeof(int) * size_t(tiles + 1), 256);
   s.fallback = g.P == nullptr ? reinterpret_cast<int64_t*>(p) : nullptr;
   s.slots = slots;
   return s;
@@ -98,7 +101,7 @@ cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slot
   }
   if (e != cudaSuccess) return e;
   StageScope t(kStageGeneral, stream);
-  return launch_kulisch(g, s.route, stream);
+  return launch_kulisch(g, s.general, stream);
 }
 
 namespace {
@@ -155,7 +158,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
   __nv_bfloat16* planesA = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesA);
   __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
-  uint8_t* res = reinterpret_cast<uint8_t*>(base + L.off_res);
+  int8_t* res = reinterpret_cast<int8_t*>(base + L.off_res);
 
   cudaError_t e;
   {
@@ -173,7 +176,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
     e = launch_residues(ra, g.bf16, nplanes, stream);
     if (e == cudaSuccess) e = launch_residues(rb, g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s.route, stream);
+    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s.route, s.general, stream);
   }
   if (e != cudaSuccess) return e;
   {
@@ -191,7 +194,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   }
   if (e != cudaSuccess) return e;
   StageScope t(kStageGeneral, stream);
-  return launch_kulisch(g, s.route, stream);
+  return launch_kulisch(g, s.general, stream);
 }
 
 }  // namespace

@@ -71,11 +71,12 @@ __device__ __forceinline__ void normalise_in_place(int64_t* acc_o) {
   acc_o[(kDigits - 1) * kOutputs] += carry;
 }
 
-// Persistent: each CTA loops over 32x32 tiles.  With a route table, a tile is
-// processed here only if its 64x64 parent tile was routed to this kernel.
+// Persistent: each CTA loops over the 32x32 quarters of the 64x64 tiles
+// listed in general (general[0] = their count), so a call with no such tile
+// costs one launch.
 template <int kBf16>
 __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
-                                                                    const uint8_t* route) {
+                                                                    const int* general) {
   extern __shared__ __align__(16) unsigned char smem[];
   int64_t* acc = reinterpret_cast<int64_t*>(smem);
   int2* As = reinterpret_cast<int2*>(smem + kAccBytes);
@@ -83,17 +84,18 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
   uint8_t* nfA = smem + kAccBytes + 2 * kStageBytes;
   uint8_t* nfB = nfA + kFlagBytes;
 
-  const int64_t tiles_n = (p.N + kBN - 1) / kBN;
-  const int64_t tiles = ((p.M + kBM - 1) / kBM) * tiles_n;
   const int64_t parents_n = (p.N + 2 * kBN - 1) / (2 * kBN);
+  const int64_t quarters = int64_t(*general) * 4;
   const int tid = threadIdx.x;
   const int ty = tid >> 4, tx = tid & 15;
 
-  for (int64_t tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-  const int64_t tm = tile / tiles_n;
-  const int64_t tn = tile - tm * tiles_n;
-  if (route != nullptr && !route[(tm >> 1) * parents_n + (tn >> 1)]) continue;
+  for (int64_t w = blockIdx.x; w < quarters; w += gridDim.x) {
+  const int64_t parent = general[1 + (w >> 2)];
+  const int64_t ptm = parent / parents_n;
+  const int64_t tm = 2 * ptm + ((w >> 1) & 1);
+  const int64_t tn = 2 * (parent - ptm * parents_n) + (w & 1);
   const int64_t m0 = tm * kBM, n0 = tn * kBN;
+  if (m0 >= p.M || n0 >= p.N) continue;               // ragged edge: quarter outside
 
   __syncthreads();                                    // previous tile done with smem
   for (int i = tid; i < kDigits * kOutputs; i += kThreads) acc[i] = 0;
@@ -230,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
 }
 
 template <int kBf16>
-cudaError_t launch_kulisch_t(const GemmArgs& a, const uint8_t* route, cudaStream_t stream) {
+cudaError_t launch_kulisch_t(const GemmArgs& a, const int* general, cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kulisch_smem_kernel<kBf16>,
@@ -244,16 +246,16 @@ cudaError_t launch_kulisch_t(const GemmArgs& a, const uint8_t* route, cudaStream
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
   const int64_t grid = tiles < sms ? tiles : (sms > 0 ? sms : 1);
-  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, route);
+  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, general);
   note_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_kulisch(const GemmArgs& a, const uint8_t* route, cudaStream_t stream) {
+cudaError_t launch_kulisch(const GemmArgs& a, const int* general, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
-  return a.bf16 ? launch_kulisch_t<1>(a, route, stream) : launch_kulisch_t<0>(a, route, stream);
+  return a.bf16 ? launch_kulisch_t<1>(a, general, stream) : launch_kulisch_t<0>(a, general, stream);
 }
 
 }  // namespace det

@@ -110,9 +110,11 @@ __global__ void __launch_bounds__(kThreads) rowstat_kernel(StatOperand a, StatOp
 }
 
 // One thread per 64x64 tile: 1 = general kernel, 0 = residue path / band kernel.
+// The general kernel's tiles are also listed (in any order: each tile is
+// computed on its own) after a count, general[0], zero at launch.
 __global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, const int* deepB,
                                                              int64_t M, int64_t N, int cap,
-                                                             uint8_t* route) {
+                                                             uint8_t* route, int* general) {
   const int64_t tiles_n = (N + kTile - 1) / kTile;
   const int64_t tiles = ((M + kTile - 1) / kTile) * tiles_n;
   for (int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x; t < tiles;
@@ -121,7 +123,9 @@ __global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, co
     int da = 0, db = 0;
     for (int64_t m = tm * kTile; m < min(M, tm * kTile + kTile); ++m) da = max(da, deepA[m]);
     for (int64_t n = tn * kTile; n < min(N, tn * kTile + kTile); ++n) db = max(db, deepB[n]);
-    route[t] = static_cast<int64_t>(da) + db > cap ? 1 : 0;
+    const bool gen = static_cast<int64_t>(da) + db > cap;
+    route[t] = gen ? 1 : 0;
+    if (gen) general[1 + atomicAdd(general, 1)] = static_cast<int>(t);
   }
 }
 
@@ -158,11 +162,13 @@ int deep_list_cap(int64_t K) {
 }
 
 cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
-                            cudaStream_t stream) {
+                            int* general, cudaStream_t stream) {
   const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
   const int64_t grid = (tiles + kThreads - 1) / kThreads;
+  cudaError_t e = cudaMemsetAsync(general, 0, sizeof(int), stream);
+  if (e != cudaSuccess) return e;
   classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
-      deepA, deepB, g.M, g.N, deep_list_cap(g.K), route);
+      deepA, deepB, g.M, g.N, deep_list_cap(g.K), route, general);
   note_launch();
   return cudaGetLastError();
 }
@@ -182,7 +188,7 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
   if (e != cudaSuccess) return e;
   e = g.bf16 ? rowstat_t<1>(g, s, true, stream) : rowstat_t<0>(g, s, true, stream);
   if (e != cudaSuccess) return e;
-  return launch_classify(g, s.deepA, s.deepB, s.route, stream);
+  return launch_classify(g, s.deepA, s.deepB, s.route, s.general, stream);
 }
 
 }  // namespace det

@@ -241,8 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ++uses[acc];
       ptx::tc_fence_after();
       const bool last = c == nch - 1;
-      const int pm = modulus(u);
-      const float p = static_cast<float>(pm);
+      const float p = static_cast<float>(modulus(u));
       const float inv_p = 1.0f / p;
 #pragma unroll 1
       for (int cb = 0; cb < kBlockN / 32; ++cb) {
@@ -252,23 +251,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::tmem_ld32(taddr, v);
         ptx::tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          // v is an exact integer below 2^24 in magnitude; reduce it exactly
-          const float f = __uint_as_float(v[j]);
-          const float q = rintf(f * inv_p);
-          v[j] = __float_as_uint(fmaf(-q, p, f));
-        }
+        for (int j = 0; j < 32; ++j)      // exact integers below 2^24: |result| < 131
+          v[j] = __float_as_uint(near_mod_f32(__uint_as_float(v[j]), p, inv_p));
         if (!last) {
           ptx::tmem_st32(taddr, v);
         } else if (row < a.M) {
-          uint8_t* out = a.res + u * MN + row * a.N + n0 + cb * 32;
+          // a second reduction makes the residue balanced (|r| <= 127); its
+          // byte is the low byte of the pattern of r + 1.5*2^23
+          int8_t* out = a.res + u * MN + row * a.N + n0 + cb * 32;
           uint32_t packed[8];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            int r = static_cast<int>(__uint_as_float(v[j])) % pm;
-            if (r < 0) r += pm;
-            if (j % 4 == 0) packed[j / 4] = 0;
-            packed[j / 4] |= static_cast<uint32_t>(r) << (8 * (j % 4));
+          for (int j4 = 0; j4 < 8; ++j4) {
+            uint32_t b[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+              const float r = near_mod_f32(__uint_as_float(v[4 * j4 + h]), p, inv_p);
+              b[h] = __float_as_uint(__fadd_rn(r, kRoundMagic));
+            }
+            packed[j4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
+                                     0x5410);
           }
           const int64_t n_left = a.N - (n0 + cb * 32);
           if (n_left >= 32 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
@@ -277,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
 #pragma unroll
             for (int j = 0; j < 32; ++j)
-              if (j < n_left) out[j] = static_cast<uint8_t>(packed[j / 4] >> (8 * (j % 4)));
+              if (j < n_left) out[j] = static_cast<int8_t>(packed[j / 4] >> (8 * (j % 4)));
           }
         }
       }

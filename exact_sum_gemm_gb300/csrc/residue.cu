@@ -1,6 +1,6 @@
 // Residue (CRT) decomposition of the exact GEMM, the CUDA-core halves:
 //   residue_kernel      operands -> bf16 residue planes + per-row deep lists
-//   reconstruct_kernel  residues of the shallow dot product -> exact value
+//   reconstruct_*       residues of the shallow dot product -> exact value
 //                       (CRT) + deep products -> round once (or digits)
 //
 // Shallow elements.  For a row r of an operand with largest last-bit
@@ -12,12 +12,14 @@
 // an exact integer dot product, |S| < K * 2^86.  S is computed modulo
 // kNumModuli small odd pairwise-coprime moduli (residues in bf16 planes,
 // multiplied on tensor cores with exact fp32 accumulation) and rebuilt here
-// by the Chinese remainder theorem: the moduli's product exceeds 2|S|.
+// by the Chinese remainder theorem in Garner's mixed-radix form: the moduli's
+// product exceeds 2|S|.  All the small modular arithmetic runs in exact
+// binary32 on the FMA pipes.
 // Deep elements (more than 19 binades below the row max) and non-finite ones
 // are left out of the planes and listed per row; their products are added
-// exactly, one by one, during reconstruction.  Together this is exactly the
-// det-train page's "exact fp64-product sum rounded once to fp32" (section
-// "Method"); only the order of the exact integer additions differs.
+// exactly, one by one, during reconstruction.  Together this is the exact sum
+// of the products rounded once to fp32, as the det-train page's "Method"
+// section defines it; only the order of the exact integer additions differs.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -30,52 +32,43 @@
 namespace det {
 namespace {
 
-struct CrtTable {
-  uint32_t c[kNumModuli][4];   // CRT weights C_i, 128-bit, least significant limb first
-  uint32_t m[4];               // M = product of the moduli in use
-  float frac[kNumModuli];      // C_i / M, to estimate the quotient of sum r_i C_i by M
-};
-
 constexpr int kThreads = 256;
 constexpr int kTileRows = 32;
 constexpr int kTileK = 64;
 
-// x mod p for 0 <= x < 2^24 and a compile-time p < 256: with
-// magic = ceil(2^32 / p), umulhi(x, magic) = floor(x/p) + floor(r/p + x*eps)
-// where x*eps < 2^24/2^32 = 2^-8 < 1/p, so the quotient is exact.
+// Reduction modulo a compile-time modulus (near_mod_f32 states the bounds).
 template <int p>
-__device__ __forceinline__ uint32_t umod(uint32_t x) {
-  constexpr uint32_t magic = static_cast<uint32_t>((0x100000000ull + p - 1) / p);
-  return x - __umulhi(x, magic) * static_cast<uint32_t>(p);
+__device__ __forceinline__ float near_mod(float a) {
+  constexpr float inv = 1.0f / static_cast<float>(p);
+  return near_mod_f32(a, static_cast<float>(p), inv);
 }
 
-// bf16 bit pattern of a small integer |v| <= 127: the top half of its exact
-// binary32 pattern (the low 16 bits are zero, so no rounding happens).
-__device__ __forceinline__ uint32_t small_int_bf16_bits(int v) {
-  return __float_as_uint(static_cast<float>(v)) >> 16;
+// Balanced residue, modulo the compile-time modulus p, of the integer x * 2^s
+// given x (|x| < 2^24, exact in binary32) and pw = 2^s (s in [0, 19]):
+//   r1 = x mod p (|r1| < 131),  t = 2^s mod p (balanced: |pw| < 2^14 p),
+//   u = r1 * t (|u| < 2^14.1, exact),  result = u mod p (balanced).
+// The fma with +0 turns a -0 product into +0, so a zero residue is +0.
+template <int p>
+__device__ __forceinline__ float residue_f32(float x, float pw) {
+  const float r1 = near_mod<p>(x);
+  const float t = near_mod<p>(pw);
+  return near_mod<p>(__fmaf_rn(r1, t, 0.0f));
 }
 
-// Balanced residue, modulo the compile-time modulus p, of the integer
-// (+-am) * 2^s with am < 2^24 and pw = 2^s <= 2^19: every intermediate is
-// below 2^24, so each reduction is exact.  Result in [-(p-1)/2, (p-1)/2].
-template <int p>
-__device__ __forceinline__ int balanced_residue(uint32_t am, uint32_t pw, bool neg) {
-  const uint32_t r = umod<p>(umod<p>(am) * umod<p>(pw));     // < 255 * 255 before the last mod
-  const int c = r > (p - 1) / 2 ? static_cast<int>(r) - p : static_cast<int>(r);
-  return neg ? -c : c;
+// bf16 pair of two small integers held exactly in binary32: the top halves of
+// their bit patterns (the low halves are zero).
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+  return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
 template <int i>
 __device__ __forceinline__ void write_residue_pairs(uint32_t* dst, int64_t plane_stride2, int nplanes,
-                                                    uint32_t am0, uint32_t pw0, bool ng0,
-                                                    uint32_t am1, uint32_t pw1, bool ng1) {
+                                                    float x0, float pw0, float x1, float pw1) {
   if constexpr (i < kNumModuli) {
     if (i < nplanes) {
       constexpr int p = modulus(i);
-      *dst = small_int_bf16_bits(balanced_residue<p>(am0, pw0, ng0)) |
-             (small_int_bf16_bits(balanced_residue<p>(am1, pw1, ng1)) << 16);
-      write_residue_pairs<i + 1>(dst + plane_stride2, plane_stride2, nplanes, am0, pw0, ng0, am1,
-                                 pw1, ng1);
+      *dst = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
+      write_residue_pairs<i + 1>(dst + plane_stride2, plane_stride2, nplanes, x0, pw0, x1, pw1);
     }
   }
 }
@@ -109,8 +102,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
     if (gr >= o.rows) continue;
     int em = o.emax[gr];
     em = em == kEmaxEmpty ? 0 : em;
-    uint32_t am[2], pw[2];
-    bool ng[2];
+    float x[2], pw[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const uint32_t bits = tile[r][kk + h];
@@ -118,18 +110,17 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
       const int s = d.e - em + kDeepGap;
       const bool deep = d.nonfinite || (d.m != 0 && s < 0);
       // a bf16 significand widened to binary32 carries 16 zero bits: drop them
-      // (exactly) so that |X_int| < 2^23; the reconstruction scales back by 2^32
+      // (exactly) so that |X_int| < 2^27; the reconstruction scales back by 2^32
       const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
-      am[h] = deep ? 0u : static_cast<uint32_t>(mi < 0 ? -mi : mi);
-      pw[h] = 1u << (deep || d.m == 0 ? 0 : s);                            // 2^s
-      ng[h] = mi < 0;
+      x[h] = static_cast<float>(deep ? 0 : mi);                        // exact: |mi| < 2^24
+      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 19]
       if (deep && gk + h < o.K) {
         const int slot = atomicAdd(o.list_count + gr, 1);
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
       }
     }
     uint32_t* dst = reinterpret_cast<uint32_t*>(o.planes + gr * o.Kp + gk);   // bf16 pair
-    write_residue_pairs<0>(dst, plane_stride2, nplanes, am[0], pw[0], ng[0], am[1], pw[1], ng[1]);
+    write_residue_pairs<0>(dst, plane_stride2, nplanes, x[0], pw[0], x[1], pw[1]);
   }
 }
 
@@ -314,6 +305,42 @@ __device__ __forceinline__ void write_canonical_digits(int64_t* out, int64_t MN,
   out[(kDigits + 1) * MN] = nf;
 }
 
+// The canonical digits of S * 2^E for a signed 128-bit S = (hi:lo) (a
+// multiple of 2^-298 below 2^277 in magnitude), as one output's 20 planes.
+// Digit j holds bits [32j - off, 32j - off + 32) of S, off = E + 298: the
+// five words of S shifted by off mod 32 land on digits off/32 .. off/32 + 4,
+// digits below are 0 and digits above repeat the sign.
+__device__ __forceinline__ void write_digits_s128(int64_t* out, int64_t MN, uint64_t lo, uint64_t hi,
+                                                  int E, int64_t K, int64_t nf) {
+  int off = E + kLsbBias;
+  if (off < 0) {                                // the low -off (< 64) bits are zero
+    const int r = -off;
+    lo = (lo >> r) | (hi << (64 - r));
+    hi = static_cast<uint64_t>(static_cast<int64_t>(hi) >> r);
+    off = 0;
+  }
+  const int j0 = off >> 5, sh = off & 31;
+  const uint32_t w0 = static_cast<uint32_t>(lo), w1 = static_cast<uint32_t>(lo >> 32);
+  const uint32_t w2 = static_cast<uint32_t>(hi), w3 = static_cast<uint32_t>(hi >> 32);
+  const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(w3) >> 31);
+  const uint32_t x0 = w0 << sh, x1 = __funnelshift_l(w0, w1, sh), x2 = __funnelshift_l(w1, w2, sh);
+  const uint32_t x3 = __funnelshift_l(w2, w3, sh), x4 = __funnelshift_l(w3, sx, sh);
+#pragma unroll
+  for (int j = 0; j < kDigits; ++j) {
+    const int k = j - j0;
+    uint32_t d = k < 0 ? 0u : sx;
+    d = k == 0 ? x0 : d;
+    d = k == 1 ? x1 : d;
+    d = k == 2 ? x2 : d;
+    d = k == 3 ? x3 : d;
+    d = k == 4 ? x4 : d;
+    out[j * MN] = j < kDigits - 1 ? static_cast<int64_t>(d)
+                                  : static_cast<int64_t>(static_cast<int32_t>(d));
+  }
+  out[kDigits * MN] = K;
+  out[(kDigits + 1) * MN] = nf;
+}
+
 // Cold path of one output: the digit route.  Used for det_gemm_partial (the
 // digits are the output) and when a deep product falls outside the 192-bit
 // window; rebuilds the exact value as 18 int64 digits and writes it.
@@ -366,66 +393,89 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
   }
 }
 
-// S = the balanced CRT value of residues r (one per modulus in use), as a
-// signed 128-bit integer (hi:lo), |S| < 2^98.
-__device__ __forceinline__ void crt_s128(const uint32_t (&r)[kNumModuli], int P, const CrtTable& crt,
-                                         uint64_t& lo, uint64_t& hi) {
-  uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
-  float qf = 0.0f;
-#pragma unroll
-  for (int i = 0; i < kNumModuli; ++i) {
-    if (i < P) {
-      // (a3:a2:a1:a0) += r_i * C_i: low halves of the four limb products, then
-      // their high halves one limb up (r_i < 256, C_i < M < 2^110; sum < 2^122)
-      asm("mad.lo.cc.u32 %0, %4, %8, %0;\n\t"
-          "madc.lo.cc.u32 %1, %5, %8, %1;\n\t"
-          "madc.lo.cc.u32 %2, %6, %8, %2;\n\t"
-          "madc.lo.u32 %3, %7, %8, %3;\n\t"
-          "mad.hi.cc.u32 %1, %4, %8, %1;\n\t"
-          "madc.hi.cc.u32 %2, %5, %8, %2;\n\t"
-          "madc.hi.u32 %3, %6, %8, %3;"
-          : "+r"(a0), "+r"(a1), "+r"(a2), "+r"(a3)
-          : "r"(crt.c[i][0]), "r"(crt.c[i][1]), "r"(crt.c[i][2]), "r"(crt.c[i][3]), "r"(r[i]));
-      qf = fmaf(static_cast<float>(r[i]), crt.frac[i], qf);     // ~ acc / M
-    }
-  }
-  // quotient estimate within one of floor(acc / M); rem = acc - q M
-  const uint32_t q = static_cast<uint32_t>(qf);
-  uint64_t t = static_cast<uint64_t>(crt.m[0]) * q;
-  const uint32_t p0 = static_cast<uint32_t>(t);
-  t = static_cast<uint64_t>(crt.m[1]) * q + (t >> 32);
-  const uint32_t p1 = static_cast<uint32_t>(t);
-  t = static_cast<uint64_t>(crt.m[2]) * q + (t >> 32);
-  const uint32_t p2 = static_cast<uint32_t>(t);
-  const uint32_t p3 = crt.m[3] * q + static_cast<uint32_t>(t >> 32);
-  const uint64_t alo = (static_cast<uint64_t>(a1) << 32) | a0, ahi = (static_cast<uint64_t>(a3) << 32) | a2;
-  const uint64_t qlo = (static_cast<uint64_t>(p1) << 32) | p0, qhi = (static_cast<uint64_t>(p3) << 32) | p2;
-  const uint64_t mlo = (static_cast<uint64_t>(crt.m[1]) << 32) | crt.m[0];
-  const uint64_t mhi = (static_cast<uint64_t>(crt.m[3]) << 32) | crt.m[2];
-  uint64_t rlo = alo - qlo;
-  uint64_t rhi = ahi - qhi - (alo < qlo ? 1u : 0u);
-  if (static_cast<int64_t>(rhi) < 0) {                       // rem < 0: add M
-    const uint64_t nlo = rlo + mlo;
-    rhi = rhi + mhi + (nlo < rlo ? 1u : 0u);
-    rlo = nlo;
-  } else if (rhi > mhi || (rhi == mhi && rlo >= mlo)) {      // rem >= M: subtract M
-    const uint64_t nlo = rlo - mlo;
-    rhi = rhi - mhi - (rlo < mlo ? 1u : 0u);
-    rlo = nlo;
-  }
-  // balanced: rem > (M-1)/2 means rem - M
-  const uint64_t hlo = (mlo >> 1) | (mhi << 63), hhi = mhi >> 1;
-  if (rhi > hhi || (rhi == hhi && rlo > hlo)) {
-    const uint64_t nlo = rlo - mlo;
-    rhi = rhi - mhi - (rlo < mlo ? 1u : 0u);
-    rlo = nlo;
-  }
-  lo = rlo;
-  hi = rhi;
+// ---------------------------------------------------------------- CRT (Garner)
+//
+// The residue GEMM stores balanced residues r_i (|r_i| <= (p_i - 1)/2) as
+// two's-complement bytes.  S is rebuilt in mixed radix with balanced digits,
+//   S = sum_i v_i P_i,   P_i = p_0 ... p_{i-1},   |v_i| <= (p_i - 1)/2,
+// which spans exactly |S| <= (M - 1)/2 (M = the product of the moduli in use),
+// so it is the unique balanced value.  Garner's recurrence gives the digits,
+//   v_i = r_i g_i + sum_{j<i} v_j d_ij  (mod p_i)   (constants: det_residue.cuh),
+// where every term is below 127^2 in magnitude, so each sum (< 14 * 2^14) is
+// exact in binary32 and near_mod returns the balanced digit.  Digits of
+// moduli not in use stay 0.
+
+// A stored residue byte b as the exact float 2^23 + 128 + r (r = b as int8).
+__device__ __forceinline__ float biased_residue(uint32_t b) {
+  return __uint_as_float(0x4B000000u | ((b ^ 0x80u) & 0xFFu));
+}
+// Byte j of a word of four residue bytes, as above.
+__device__ __forceinline__ float biased_residue_of_word(uint32_t w, int j) {
+  return __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | static_cast<uint32_t>(j)));
 }
 
-// RNE_f32(S * 2^E) for a signed 128-bit S = (hi:lo): the binary32 rule.
-__device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) {
+template <int i, int j>
+__device__ __forceinline__ float garner_sum(float acc, const float (&v)[kNumModuli]) {
+  if constexpr (j < i) {
+    constexpr float d = static_cast<float>(garner_d(i, j));
+    return garner_sum<i, j + 1>(__fmaf_rn(v[j], d, acc), v);
+  } else {
+    return acc;
+  }
+}
+
+template <int i>
+__device__ __forceinline__ void garner_digits(const float (&f)[kNumModuli], int P, float (&v)[kNumModuli]) {
+  if constexpr (i < kNumModuli) {
+    if (i < P) {
+      constexpr float gi = static_cast<float>(garner_g(i));
+      constexpr float bias = -8388736.0f * gi;                  // -(2^23 + 128) g_i, exact
+      const float acc = garner_sum<i, 0>(__fmaf_rn(f[i], gi, bias), v);   // r_i g_i + ...
+      v[i] = near_mod<modulus(i)>(acc);
+      garner_digits<i + 1>(f, P, v);
+    }
+  }
+}
+
+// Integer value of a binary32 holding an integer of magnitude below 2^22.
+__device__ __forceinline__ int64_t small_float_to_int(float x) {
+  return static_cast<int64_t>(__float_as_int(__fadd_rn(x, kRoundMagic)) - kRoundMagicBits);
+}
+
+// S as a signed 128-bit integer (hi:lo), from the biased residue floats f.
+// Horner over digit pairs w_k = v_2k + p_2k v_2k+1 (|w_k| < 2^15, exact in
+// fp32) with radix R_k = p_2k p_2k+1:  the top four pairs (moduli 6..13,
+// |T| < 2^62) and the bottom three (moduli 0..5, |L| < 2^48) in int64, then
+// S = T * P_6 + L.
+__device__ __forceinline__ void garner_s128(const float (&f)[kNumModuli], int P, uint64_t& lo,
+                                            uint64_t& hi) {
+  static_assert(kNumModuli == 14, "digit pairs below assume 14 moduli");
+  float v[kNumModuli];
+#pragma unroll
+  for (int i = 0; i < kNumModuli; ++i) v[i] = 0.0f;
+  garner_digits<0>(f, P, v);
+  int64_t w[kNumModuli / 2];
+#pragma unroll
+  for (int k = 0; k < kNumModuli / 2; ++k)
+    w[k] = small_float_to_int(__fmaf_rn(v[2 * k + 1], static_cast<float>(modulus(2 * k)), v[2 * k]));
+  constexpr int64_t R[kNumModuli / 2] = {
+      int64_t(modulus(0)) * modulus(1), int64_t(modulus(2)) * modulus(3),
+      int64_t(modulus(4)) * modulus(5), int64_t(modulus(6)) * modulus(7),
+      int64_t(modulus(8)) * modulus(9), int64_t(modulus(10)) * modulus(11),
+      int64_t(modulus(12)) * modulus(13)};
+  const int32_t t32 = static_cast<int32_t>(w[6]) * static_cast<int32_t>(R[5]) + static_cast<int32_t>(w[5]);
+  int64_t t = static_cast<int64_t>(t32) * R[4] + w[4];
+  t = t * R[3] + w[3];
+  const int64_t l = (w[2] * R[1] + w[1]) * R[0] + w[0];
+  constexpr int64_t kP6 = R[0] * R[1] * R[2];
+  const __int128 S = static_cast<__int128>(t) * kP6 + l;
+  lo = static_cast<uint64_t>(S);
+  hi = static_cast<uint64_t>(static_cast<unsigned __int128>(S) >> 64);
+}
+
+// RNE_f32(S * 2^E) for a signed 128-bit S = (hi:lo): the binary32 rule,
+// bit by bit.  Used where the result may be subnormal.
+__device__ __noinline__ uint32_t round_s128_exact(uint64_t lo, uint64_t hi, int E) {
   const bool neg = static_cast<int64_t>(hi) < 0;
   if (neg) {
     lo = ~lo + 1;
@@ -469,6 +519,37 @@ __device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) 
                                   static_cast<uint32_t>(q - (uint64_t(1) << 23))
                             : static_cast<uint32_t>(q);
   return sign | bits;
+}
+
+// RNE_f32(S * 2^E), fast form.  The leading 64 bits of |S|, with every bit
+// below them ORed into bit 0 (a sticky bit well below the rounding position),
+// convert to binary32 with the same round-to-nearest-even decision as |S|
+// itself; the exact power-of-two scaling is then an exponent add.  Results
+// that would be subnormal or zero go to the bit-by-bit routine.
+__device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) {
+  const bool neg = static_cast<int64_t>(hi) < 0;
+  uint64_t alo = lo, ahi = hi;
+  if (neg) {
+    alo = ~lo + 1;
+    ahi = ~hi + (alo == 0 ? 1u : 0u);
+  }
+  if ((alo | ahi) == 0) return 0u;                       // exact zero -> +0
+  const int lz = ahi ? __clzll(static_cast<long long>(ahi))
+                     : 64 + __clzll(static_cast<long long>(alo));
+  uint64_t top;
+  if (lz == 0) {
+    top = ahi | (alo != 0 ? 1u : 0u);
+  } else if (lz < 64) {
+    top = (ahi << lz) | (alo >> (64 - lz)) | ((alo << lz) != 0 ? 1u : 0u);
+  } else {
+    top = alo << (lz - 64);
+  }
+  const uint32_t f = __float_as_uint(__ull2float_rn(top));     // |S| * 2^(lz-64), rounded
+  const int shift = E + 64 - lz;
+  const int ef = static_cast<int>(f >> 23) + shift;             // biased exponent of the result
+  if (ef >= 1 && ef <= 254) return (neg ? 0x80000000u : 0u) | (f + (static_cast<uint32_t>(shift) << 23));
+  if (ef >= 255) return (neg ? 0x80000000u : 0u) | 0x7F800000u;
+  return round_s128_exact(lo, hi, E);
 }
 
 // Deep products of output (m, n) added into t (bit 0 weighs 2^E); returns
@@ -515,8 +596,7 @@ constexpr int kReconCols = 4;                       // outputs per thread (one r
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
 template <int kBf16>
-__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra,
-                                                                        const __grid_constant__ CrtTable crt) {
+__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;    // the tensor-core kernel gave up
@@ -537,13 +617,13 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
     for (int i = 0; i < kNumModuli; ++i) {
       packed[i] = 0;
       if (i < ra.nplanes) {
-        const uint8_t* plane = ra.res + i * MN + base;
+        const int8_t* plane = ra.res + i * MN + base;
         if (vec) {
           packed[i] = *reinterpret_cast<const uint32_t*>(plane);
         } else {
 #pragma unroll
           for (int j = 0; j < kReconCols; ++j)
-            if (j < ncols) packed[i] |= static_cast<uint32_t>(plane[j]) << (8 * j);
+            if (j < ncols) packed[i] |= static_cast<uint32_t>(static_cast<uint8_t>(plane[j])) << (8 * j);
         }
       }
     }
@@ -552,11 +632,11 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
       if (j >= ncols) break;
       const int64_t n = n0 + j;
       if (ra.countB[n] != 0) continue;                            // deep column: full kernel
-      uint32_t rj[kNumModuli];
+      float f[kNumModuli];
 #pragma unroll
-      for (int i = 0; i < kNumModuli; ++i) rj[i] = (packed[i] >> (8 * j)) & 0xFFu;
+      for (int i = 0; i < kNumModuli; ++i) f[i] = biased_residue_of_word(packed[i], j);
       uint64_t slo, shi;
-      crt_s128(rj, ra.nplanes, crt, slo, shi);
+      garner_s128(f, ra.nplanes, slo, shi);
       int emB = ra.emaxB[n];
       emB = emB == kEmaxEmpty ? 0 : emB;
       const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
@@ -585,7 +665,7 @@ __global__ void __launch_bounds__(kThreads) compact_deep_kernel(const int* count
 // warps stay full.
 template <int kBf16>
 __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
-    GemmArgs g, ReconArgs ra, const __grid_constant__ CrtTable crt, const int* rows,
+    GemmArgs g, ReconArgs ra, const int* rows,
     const int* cols, const int* nrc) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
@@ -608,11 +688,12 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
     int emA = ra.emaxA[m], emB = ra.emaxB[n];
     emA = emA == kEmaxEmpty ? 0 : emA;
     emB = emB == kEmaxEmpty ? 0 : emB;
-    uint32_t r[kNumModuli];
+    float f[kNumModuli];
 #pragma unroll
-    for (int i = 0; i < kNumModuli; ++i) r[i] = i < ra.nplanes ? ra.res[i * MN + m * g.N + n] : 0u;
+    for (int i = 0; i < kNumModuli; ++i)
+      f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + m * g.N + n]) : 0u);
     uint64_t slo, shi;
-    crt_s128(r, ra.nplanes, crt, slo, shi);
+    garner_s128(f, ra.nplanes, slo, shi);
     const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
     W192 t;
     t.w[0] = 0;
@@ -621,7 +702,9 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
     int64_t nf = 0;
     const bool fits = add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf);
     if (failed) nf = 1;
-    if (fits) {
+    if (fits && g.P != nullptr) {
+      write_canonical_digits(g.P + m * g.N + n, MN, t, E, g.K, nf);
+    } else if (fits) {
       reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_w192(t, E);
     } else {
       const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
@@ -630,44 +713,32 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
   }
 }
 
-// Digit path: every output of det_gemm_partial.  One output per thread, so
-// that each of the 20 plane stores of a warp is one contiguous 256-byte write.
+// det_gemm_partial outputs whose row of A and column of B hold no deep
+// element: CRT, then the digits.  One output per thread, so that each of the
+// 20 plane stores of a warp is one contiguous 256-byte write.
 template <int kBf16>
-__global__ void __launch_bounds__(kThreads, 2) reconstruct_kernel(GemmArgs g, ReconArgs ra,
-                                                                   const __grid_constant__ CrtTable crt) {
+__global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
-  const bool failed = ra.error != nullptr && *ra.error != 0;
+  const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
   const int64_t n = int64_t(blockIdx.x) * kThreads + threadIdx.x;
-  if (n >= g.N) return;
+  if (n >= g.N || ra.countB[n] != 0) return;                  // deep column: deep kernel
   int emB = ra.emaxB[n];
   emB = emB == kEmaxEmpty ? 0 : emB;
-  const bool col_deep = ra.countB[n] != 0;
   for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
-    if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;    // general kernel's outputs
+    if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's outputs
+    if (ra.countA[m] != 0) continue;                            // deep row: deep kernel
     int emA = ra.emaxA[m];
     emA = emA == kEmaxEmpty ? 0 : emA;
     const int64_t idx = m * g.N + n;
-    uint32_t r[kNumModuli];
+    float f[kNumModuli];
 #pragma unroll
-    for (int i = 0; i < kNumModuli; ++i) r[i] = i < ra.nplanes ? ra.res[i * MN + idx] : 0u;
+    for (int i = 0; i < kNumModuli; ++i)
+      f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + idx]) : 0u);
     uint64_t slo, shi;
-    crt_s128(r, ra.nplanes, crt, slo, shi);
-    const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;   // bit 0 of S * 2^64
-    W192 t;
-    t.w[0] = 0;
-    t.w[1] = slo;
-    t.w[2] = shi;
-    int64_t nf = 0;
-    const bool deep = col_deep || ra.countA[m] != 0;
-    const bool fits = deep ? add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf) : true;
-    if (failed) nf = 1;
-    if (fits) {
-      write_canonical_digits(g.P + idx, MN, t, E, g.K, nf);
-    } else {
-      const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
-      output_via_digits<kBf16>(g, ra, m, n, t, E, true, S, emA, nf);
-    }
+    garner_s128(f, ra.nplanes, slo, shi);
+    const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+    write_digits_s128(g.P + idx, MN, slo, shi, Es, g.K, nf);
   }
 }
 
@@ -696,47 +767,23 @@ cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cuda
   return cudaGetLastError();
 }
 
-CrtTable make_crt_table(int nplanes) {
-  // M = prod p_i; C_i = (M/p_i) * ((M/p_i)^-1 mod p_i) mod M  (exact 128-bit host arithmetic)
-  CrtTable t{};
-  unsigned __int128 M = 1;
-  for (int i = 0; i < nplanes; ++i) M *= static_cast<unsigned>(modulus(i));
-  for (int i = 0; i < nplanes; ++i) {
-    const unsigned p = static_cast<unsigned>(modulus(i));
-    const unsigned __int128 Mi = M / p;
-    const unsigned mi = static_cast<unsigned>(Mi % p);
-    unsigned inv = 1;
-    for (unsigned c = 1; c < p; ++c)
-      if ((mi * c) % p == 1) {
-        inv = c;
-        break;
-      }
-    const unsigned __int128 C = (Mi * inv) % M;
-    for (int w = 0; w < 4; ++w) t.c[i][w] = static_cast<uint32_t>(C >> (32 * w));
-    t.frac[i] = static_cast<float>(static_cast<long double>(C) / static_cast<long double>(M));
-  }
-  for (int w = 0; w < 4; ++w) t.m[w] = static_cast<uint32_t>(M >> (32 * w));
-  return t;
-}
-
 cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
                                int* deep_counters, cudaStream_t stream) {
   const int64_t MN = g.M * g.N;
   if (MN == 0) return cudaSuccess;
-  const CrtTable crt = make_crt_table(ra.nplanes);
   const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
   dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
             static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
   if (g.P != nullptr) {
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
                static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
-    if (g.bf16) reconstruct_kernel<1><<<pgrid, kThreads, 0, stream>>>(g, ra, crt);
-    else reconstruct_kernel<0><<<pgrid, kThreads, 0, stream>>>(g, ra, crt);
-    note_launch();
-    return cudaGetLastError();
+    if (g.bf16) partial_fast_kernel<1><<<pgrid, kThreads, 0, stream>>>(g, ra);
+    else partial_fast_kernel<0><<<pgrid, kThreads, 0, stream>>>(g, ra);
+  } else if (g.bf16) {
+    reconstruct_fast_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra);
+  } else {
+    reconstruct_fast_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra);
   }
-  if (g.bf16) reconstruct_fast_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra, crt);
-  else reconstruct_fast_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra, crt);
   // deep rows and columns: index lists [M] and [N], and their two counters
   int* rows = deep_lists;
   int* cols = deep_lists + g.M;
@@ -750,9 +797,9 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
                         stream>>>(ra.countA, g.M, ra.countB, g.N, rows, cols, nrc);
   const unsigned dgrid = static_cast<unsigned>(sms) * 4;
   if (g.bf16)
-    reconstruct_deep_kernel<1><<<dgrid, kThreads, 0, stream>>>(g, ra, crt, rows, cols, nrc);
+    reconstruct_deep_kernel<1><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
   else
-    reconstruct_deep_kernel<0><<<dgrid, kThreads, 0, stream>>>(g, ra, crt, rows, cols, nrc);
+    reconstruct_deep_kernel<0><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
   note_launch(3);
   return cudaGetLastError();
 }
