@@ -9,11 +9,13 @@
 
 namespace det {
 
-// Odd, pairwise coprime moduli <= 255: balanced residues lie in [-127, 127]
-// (exact in bf16), products of two in [-16129, 16129], and 1024 such products
-// plus a reduced carry stay below 2^24, where fp32 accumulation is exact.
-// The product of all 14 exceeds 2^109, enough for |S| < 2^19 * 2^86 * 2
-// (f32 shallow integers are below 2^(24+19)).
+// Odd, pairwise coprime moduli in [197, 255].  The operand planes hold
+// residues r with |r| <= 138 (nearly balanced, exact in bf16, which holds
+// integers up to 256), so a product of two is at most 138^2 = 19044 in
+// magnitude, and 832 such products plus a reduced carry (< 131) stay below
+// 2^24, where fp32 accumulation is exact.  The product of all 14 moduli
+// exceeds 2^109, enough for |S| < 2^19 * 2^86 * 2 (f32 shallow integers are
+// below 2^(24+19)).
 constexpr int kNumModuli = 14;
 __host__ __device__ constexpr int modulus(int i) {
   return i == 0 ? 255 : i == 1 ? 253 : i == 2 ? 251 : i == 3 ? 247 : i == 4 ? 241 : i == 5 ? 239
@@ -49,17 +51,18 @@ __host__ __device__ constexpr int garner_d(int i, int j) {
 
 // Exact modular reduction in binary32 (integers below 2^24 are exact there,
 // and the fp32 FMA pipes outrun the integer multiplier).  For an integer-
-// valued a with |a| <= 2^24 and an odd modulus p in [197, 255], with
-// inv_p = fl(1/p) (so |a * inv_p| < 2^17, where adding 1.5*2^23 rounds to an
-// integer):
+// valued a with |a| <= 2^26 and an odd modulus p in [197, 255], with
+// inv_p = 1/p to within one ulp (so |a * inv_p| < 2^19, where adding
+// 1.5*2^23 rounds to an integer):
 //   q = (a * inv_p + 1.5*2^23) - 1.5*2^23      (one rounding to an integer)
 //   r = a - q * p                               (one fma: exact, r is small)
-// inv_p has relative error below 2^-24, so before rounding q is within
-// |a|/p * 2^-23 of the real a/p.  a/p is never a half-integer (p is odd) and
-// a non-integer a/p lies at least 1/(2p) > 2^-9 from one; so whenever
-// |a| < 2^14 * p the rounding gives the nearest integer and r is the balanced
-// residue in [-(p-1)/2, (p-1)/2].  For larger |a| (up to 2^24) q may be one
-// off and |r| <= p/2 + p * 2^-6.6 < 131.  A zero result is +0 unless a is -0.
+// Before rounding, q is within |a|/p * 2^-23 of the real a/p.  a/p is never
+// a half-integer (p is odd) and a non-integer a/p lies at least 1/(2p) > 2^-9
+// from one; so whenever |a| < 2^14 * p the rounding gives the nearest integer
+// and r is the balanced residue in [-(p-1)/2, (p-1)/2].  Otherwise q may be
+// one off: |r| <= p * (1/2 + |a|/p * 2^-23), which is below 131 for
+// |a| <= 2^24 and below 139 for |a| <= 2^26.  A zero result is +0 unless a
+// is -0.
 constexpr float kRoundMagic = 12582912.0f;           // 1.5 * 2^23
 constexpr int kRoundMagicBits = 0x4B400000;
 
@@ -68,8 +71,10 @@ __device__ __forceinline__ float near_mod_f32(float a, float p, float inv_p) {
   return __fmaf_rn(-q, p, a);
 }
 
-constexpr int kChunkK = 1024;     // K per exact fp32 accumulation window
+constexpr int kChunkK = 832;      // K per exact fp32 accumulation window (13 stages)
 constexpr int kStageK = 64;       // K per TMA/MMA stage (one 128-byte swizzle row of bf16)
+static_assert(kChunkK % kStageK == 0, "accumulation windows are whole stages");
+static_assert(int64_t(kChunkK) * 138 * 138 + 131 < (int64_t(1) << 24), "window stays exact in fp32");
 
 struct ResidueOperand {
   const void* X;
@@ -79,7 +84,9 @@ struct ResidueOperand {
   int64_t K;
   int64_t Kp;                 // K rounded up to kStageK (zero padded)
   const int* emax;            // [rows]
-  __nv_bfloat16* planes;      // [nplanes][rows][Kp]
+  __nv_bfloat16* planes;      // [rows][Kp/64][nplanes][64]: a row's 64-k stages, all planes of a
+                              // stage together (plane u of element (r, k) at
+                              // ((r * Kp/64 + k/64) * nplanes + u) * 64 + k % 64)
   int* list_count;            // [rows], zeroed before the launch
   uint2* list;                // [rows][cap]: (k, raw bits) of deep / non-finite elements
   int cap;
@@ -106,8 +113,8 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
                                int* deep_counters, cudaStream_t stream);
 
 struct ResGemmArgs {
-  const __nv_bfloat16* A;     // [nplanes][M][Kp]
-  const __nv_bfloat16* B;     // [nplanes][N][Kp]
+  const __nv_bfloat16* A;     // [M][Kp/64][nplanes][64] (ResidueOperand::planes)
+  const __nv_bfloat16* B;     // [N][Kp/64][nplanes][64]
   int64_t M, N, Kp;
   int nplanes;
   int8_t* res;                // [nplanes][M][N] balanced residues

@@ -2,18 +2,19 @@
 //
 // For every modulus p_u (u < nplanes) it computes, exactly,
 //     res[u][m][n] = (sum_k A_u[m,k] * B_u[n,k]) mod p_u,
-// where A_u, B_u are bf16 planes of balanced residues (|r| <= 127, see
-// residue.cu).  Each product is an integer of magnitude <= 16129, exact in the
+// where A_u, B_u are bf16 planes of residues with |r| <= 138 (see
+// residue.cu).  Each product is an integer of magnitude <= 19044, exact in the
 // MMA; fp32 accumulation of integers is exact while the running sum stays
 // below 2^24, so the accumulator is reduced modulo p_u in TMEM after every
-// 1024 values of K (1024 * 16129 + a reduced carry < 2^24), and the MMA keeps
+// 832 values of K (832 * 19044 + a reduced carry < 2^24), and the MMA keeps
 // accumulating on top of the reduced value.  The result is the exact integer
 // dot product modulo p_u; the CRT in residue.cu rebuilds the exact sum.
 //
 // Structure (persistent, one CTA per SM, looping over units = (modulus, pair
 // of neighbouring 128x256 output tiles), modulus-major):
 //   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
-//               rows), 128-byte swizzled, 4-stage mbarrier ring
+//               rows), 128-byte swizzled, 4-stage mbarrier ring (the planes
+//               are stored [rows][K/64][P][64], see det_residue.cuh)
 //   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
 //               and the single MMA-issuing thread (UMMA 128x256x16, bf16)
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
@@ -47,7 +48,7 @@ constexpr int kThreads = 192;
 constexpr int kABytes = kBlockM * kStageK * 2;               // 16 KB
 constexpr int kBBytes = kBlockN * kStageK * 2;               // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;               // 48 KB
-constexpr int kKbPerChunk = kChunkK / kStageK;               // 16
+constexpr int kKbPerChunk = kChunkK / kStageK;               // 13
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
 constexpr uint32_t kTmemCols = 512;
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 1024;
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
           unsigned char* st = smem + s * kStageBytes;
-          ptx::tma_load_3d(st, &tmA, &full[s], kb * kStageK, static_cast<int>(m0), u);
-          ptx::tma_load_3d(st + kABytes, &tmB, &full[s], kb * kStageK, static_cast<int>(n0), u);
+          ptx::tma_load_4d(st, &tmA, &full[s], 0, u, kb, static_cast<int>(m0));
+          ptx::tma_load_4d(st + kABytes, &tmB, &full[s], 0, u, kb, static_cast<int>(n0));
           ++it;
         }
       }
@@ -312,18 +313,23 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over planes [P][rows][Kp] of bf16, boxes of 64 (K) x box_rows x 1.
+// 4-D map over the planes [rows][Kp/64][P][64] of bf16 (innermost first:
+// 64 k of one stage, plane, stage, row).  A box of 64 x 1 x 1 x box_rows is
+// one plane's 64-k stage for box_rows rows: box_rows 128-byte rows in shared
+// memory, 128-byte swizzled, as the UMMA descriptors expect.
 bool make_plane_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp, int planes,
                     int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return false;
-  cuuint64_t dims[3] = {static_cast<cuuint64_t>(Kp), static_cast<cuuint64_t>(rows),
-                        static_cast<cuuint64_t>(planes)};
-  cuuint64_t strides[2] = {static_cast<cuuint64_t>(Kp) * 2,
-                           static_cast<cuuint64_t>(rows) * static_cast<cuuint64_t>(Kp) * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(box_rows), 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+  const cuuint64_t nkb = static_cast<cuuint64_t>(Kp / kStageK);
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(planes), nkb,
+                        static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kStageK) * 2,
+                           static_cast<cuuint64_t>(planes) * kStageK * 2,
+                           nkb * static_cast<cuuint64_t>(planes) * kStageK * 2};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(kStageK), 1, 1, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -29,6 +29,8 @@
 #include "det_kernels.h"
 #include "det_residue.cuh"
 
+#include <type_traits>
+
 namespace det {
 namespace {
 
@@ -43,16 +45,14 @@ __device__ __forceinline__ float near_mod(float a) {
   return near_mod_f32(a, static_cast<float>(p), inv);
 }
 
-// Balanced residue, modulo the compile-time modulus p, of the integer x * 2^s
-// given x (|x| < 2^24, exact in binary32) and pw = 2^s (s in [0, 19]):
-//   r1 = x mod p (|r1| < 131),  t = 2^s mod p (balanced: |pw| < 2^14 p),
-//   u = r1 * t (|u| < 2^14.1, exact),  result = u mod p (balanced).
-// The fma with +0 turns a -0 product into +0, so a zero residue is +0.
+// A residue, modulo the compile-time modulus p, of the integer x * 2^s given
+// x (|x| < 2^24, exact in binary32) and pw = 2^s (s in [0, 19]):
+//   r1 = x mod p (|r1| < 131),  u = r1 * 2^s (exact, |u| < 2^26),
+//   result = u mod p, with |result| <= 138.
+// A zero residue is +0 (x = +0 gives r1 = +0, and pw > 0).
 template <int p>
 __device__ __forceinline__ float residue_f32(float x, float pw) {
-  const float r1 = near_mod<p>(x);
-  const float t = near_mod<p>(pw);
-  return near_mod<p>(__fmaf_rn(r1, t, 0.0f));
+  return near_mod<p>(__fmul_rn(near_mod<p>(x), pw));
 }
 
 // bf16 pair of two small integers held exactly in binary32: the top halves of
@@ -61,24 +61,27 @@ __device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
   return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
-template <int i>
-__device__ __forceinline__ void write_residue_pairs(uint32_t* dst, int64_t plane_stride2, int nplanes,
-                                                    float x0, float pw0, float x1, float pw1) {
-  if constexpr (i < kNumModuli) {
-    if (i < nplanes) {
-      constexpr int p = modulus(i);
-      *dst = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
-      write_residue_pairs<i + 1>(dst + plane_stride2, plane_stride2, nplanes, x0, pw0, x1, pw1);
-    }
+// Plane i of an element pair sits 64 bf16 (32 pairs) after plane i - 1.
+template <int i, int P>
+__device__ __forceinline__ void write_residue_pairs(uint32_t* dst, float x0, float pw0, float x1,
+                                                    float pw1) {
+  if constexpr (i < P) {
+    constexpr int p = modulus(i);
+    dst[i * (kStageK / 2)] = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
+    write_residue_pairs<i + 1, P>(dst, x0, pw0, x1, pw1);
   }
 }
 
-// One block: 32 rows x 64 k of one operand; each thread then handles pairs of
-// neighbouring k.  Planes are [P][rows][Kp] (Kp a multiple of 64).  Every
-// deep or non-finite element is counted (and listed while there is room).
-template <int kBf16>
-__global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int nplanes) {
+// One block: 32 rows x one 64-k stage of one operand; each thread then
+// handles pairs of neighbouring k, writing the P residues of a pair as P
+// 4-byte words 128 bytes apart (a warp covers one row's stage: P contiguous
+// 128-byte lines).  Every deep or non-finite element is counted (and listed
+// while there is room).
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
+  static_assert(kTileK == kStageK, "one block covers one plane stage");
   __shared__ uint32_t tile[kTileRows][kTileK + 1];
+  __shared__ int row_emax[kTileRows];
   const int tid = threadIdx.x;
   const int64_t r0 = int64_t(blockIdx.y) * kTileRows;
   const int64_t k0 = int64_t(blockIdx.x) * kTileK;
@@ -92,16 +95,19 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
     if (gr < o.rows && gk < o.K) bits = load_bits<kBf16>(o.X, o.op ? gk * o.ld + gr : gr * o.ld + gk);
     tile[r][k] = bits;
   }
+  if (tid < kTileRows) {
+    const int em = r0 + tid < o.rows ? o.emax[r0 + tid] : 0;
+    row_emax[tid] = em == kEmaxEmpty ? 0 : em;
+  }
   __syncthreads();
-  const int64_t plane_stride2 = o.rows * o.Kp / 2;          // in bf16 pairs
+  const int64_t nkb = o.Kp / kStageK;
 #pragma unroll 1
   for (int u = 0; u < kTileRows * kTileK / (2 * kThreads); ++u) {
     const int idx = tid + u * kThreads;
     const int r = idx >> 5, kk = (idx & 31) * 2;
     const int64_t gr = r0 + r, gk = k0 + kk;
     if (gr >= o.rows) continue;
-    int em = o.emax[gr];
-    em = em == kEmaxEmpty ? 0 : em;
+    const int em = row_emax[r];
     float x[2], pw[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -119,8 +125,9 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o, int
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
       }
     }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(o.planes + gr * o.Kp + gk);   // bf16 pair
-    write_residue_pairs<0>(dst, plane_stride2, nplanes, x[0], pw[0], x[1], pw[1]);
+    uint32_t* dst =
+        reinterpret_cast<uint32_t*>(o.planes + (gr * nkb + int64_t(blockIdx.x)) * P * kStageK + kk);
+    write_residue_pairs<0, P>(dst, x[0], pw[0], x[1], pw[1]);
   }
 }
 
@@ -424,15 +431,17 @@ __device__ __forceinline__ float garner_sum(float acc, const float (&v)[kNumModu
   }
 }
 
-template <int i>
+// Digits v_0 .. v_{P-1} for the P moduli in use (P <= kMaxP; with kMaxP the
+// compiled count, P = kMaxP folds every guard away).
+template <int i, int kMaxP>
 __device__ __forceinline__ void garner_digits(const float (&f)[kNumModuli], int P, float (&v)[kNumModuli]) {
-  if constexpr (i < kNumModuli) {
+  if constexpr (i < kMaxP) {
     if (i < P) {
       constexpr float gi = static_cast<float>(garner_g(i));
       constexpr float bias = -8388736.0f * gi;                  // -(2^23 + 128) g_i, exact
       const float acc = garner_sum<i, 0>(__fmaf_rn(f[i], gi, bias), v);   // r_i g_i + ...
       v[i] = near_mod<modulus(i)>(acc);
-      garner_digits<i + 1>(f, P, v);
+      garner_digits<i + 1, kMaxP>(f, P, v);
     }
   }
 }
@@ -447,13 +456,14 @@ __device__ __forceinline__ int64_t small_float_to_int(float x) {
 // fp32) with radix R_k = p_2k p_2k+1:  the top four pairs (moduli 6..13,
 // |T| < 2^62) and the bottom three (moduli 0..5, |L| < 2^48) in int64, then
 // S = T * P_6 + L.
+template <int kMaxP>
 __device__ __forceinline__ void garner_s128(const float (&f)[kNumModuli], int P, uint64_t& lo,
                                             uint64_t& hi) {
   static_assert(kNumModuli == 14, "digit pairs below assume 14 moduli");
   float v[kNumModuli];
 #pragma unroll
   for (int i = 0; i < kNumModuli; ++i) v[i] = 0.0f;
-  garner_digits<0>(f, P, v);
+  garner_digits<0, kMaxP>(f, P, v);
   int64_t w[kNumModuli / 2];
 #pragma unroll
   for (int k = 0; k < kNumModuli / 2; ++k)
@@ -595,7 +605,7 @@ constexpr int kReconCols = 4;                       // outputs per thread (one r
 
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
-template <int kBf16>
+template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
@@ -616,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
 #pragma unroll
     for (int i = 0; i < kNumModuli; ++i) {
       packed[i] = 0;
-      if (i < ra.nplanes) {
+      if (i < P) {
         const int8_t* plane = ra.res + i * MN + base;
         if (vec) {
           packed[i] = *reinterpret_cast<const uint32_t*>(plane);
@@ -636,7 +646,7 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
 #pragma unroll
       for (int i = 0; i < kNumModuli; ++i) f[i] = biased_residue_of_word(packed[i], j);
       uint64_t slo, shi;
-      garner_s128(f, ra.nplanes, slo, shi);
+      garner_s128<P>(f, P, slo, shi);
       int emB = ra.emaxB[n];
       emB = emB == kEmaxEmpty ? 0 : emB;
       const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
@@ -693,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
     for (int i = 0; i < kNumModuli; ++i)
       f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + m * g.N + n]) : 0u);
     uint64_t slo, shi;
-    garner_s128(f, ra.nplanes, slo, shi);
+    garner_s128<kNumModuli>(f, ra.nplanes, slo, shi);
     const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
     W192 t;
     t.w[0] = 0;
@@ -716,7 +726,7 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
 // det_gemm_partial outputs whose row of A and column of B hold no deep
 // element: CRT, then the digits.  One output per thread, so that each of the
 // 20 plane stores of a warp is one contiguous 256-byte write.
-template <int kBf16>
+template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
@@ -734,25 +744,48 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
     float f[kNumModuli];
 #pragma unroll
     for (int i = 0; i < kNumModuli; ++i)
-      f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + idx]) : 0u);
+      f[i] = biased_residue(i < P ? static_cast<uint8_t>(ra.res[i * MN + idx]) : 0u);
     uint64_t slo, shi;
-    garner_s128(f, ra.nplanes, slo, shi);
+    garner_s128<P>(f, P, slo, shi);
     const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
     write_digits_s128(g.P + idx, MN, slo, shi, Es, g.K, nf);
+  }
+}
+
+// Moduli counts with compiled kernels: f32 operands need 12 to 14 moduli
+// (K from 1 to 2^19), bf16 operands 8 to 10.  A call uses the smallest
+// compiled count that covers its bound (more moduli never change the result).
+template <typename F>
+cudaError_t with_planes(int bf16, int P, F&& launch) {
+  using std::integral_constant;
+  if (bf16) {
+    switch (P) {
+      case 8: return launch(integral_constant<int, 1>{}, integral_constant<int, 8>{});
+      case 9: return launch(integral_constant<int, 1>{}, integral_constant<int, 9>{});
+      case 10: return launch(integral_constant<int, 1>{}, integral_constant<int, 10>{});
+      default: return cudaErrorInvalidValue;
+    }
+  }
+  switch (P) {
+    case 12: return launch(integral_constant<int, 0>{}, integral_constant<int, 12>{});
+    case 13: return launch(integral_constant<int, 0>{}, integral_constant<int, 13>{});
+    case 14: return launch(integral_constant<int, 0>{}, integral_constant<int, 14>{});
+    default: return cudaErrorInvalidValue;
   }
 }
 
 }  // namespace
 
 int residue_planes_needed(const GemmArgs& g) {
-  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^15; need prod > 2|S|
+  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^19; need prod > 2|S|
   const unsigned __int128 sig = g.bf16 ? 0xFFu : 0xFFFFFFu;
   const unsigned __int128 mx = sig << kDeepGap;
   const unsigned __int128 bound = static_cast<unsigned __int128>(g.K > 0 ? g.K : 1) * mx * mx * 2;
   unsigned __int128 prod = 1;
+  const int least = g.bf16 ? 8 : 12;
   for (int i = 0; i < kNumModuli; ++i) {
     prod *= static_cast<unsigned>(modulus(i));
-    if (prod > bound) return i + 1;
+    if (prod > bound) return i + 1 < least ? least : i + 1;
   }
   return -1;
 }
@@ -761,8 +794,11 @@ cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cuda
   if (o.rows == 0 || o.Kp == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((o.Kp + kTileK - 1) / kTileK),
             static_cast<unsigned>((o.rows + kTileRows - 1) / kTileRows));
-  if (bf16) residue_kernel<1><<<grid, kThreads, 0, stream>>>(o, nplanes);
-  else residue_kernel<0><<<grid, kThreads, 0, stream>>>(o, nplanes);
+  const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
+    residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -774,16 +810,21 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
   const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
   dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
             static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
+  cudaError_t e;
   if (g.P != nullptr) {
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
                static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
-    if (g.bf16) partial_fast_kernel<1><<<pgrid, kThreads, 0, stream>>>(g, ra);
-    else partial_fast_kernel<0><<<pgrid, kThreads, 0, stream>>>(g, ra);
-  } else if (g.bf16) {
-    reconstruct_fast_kernel<1><<<grid, kThreads, 0, stream>>>(g, ra);
+    e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
+      partial_fast_kernel<decltype(B)::value, decltype(P)::value><<<pgrid, kThreads, 0, stream>>>(g, ra);
+      return cudaSuccess;
+    });
   } else {
-    reconstruct_fast_kernel<0><<<grid, kThreads, 0, stream>>>(g, ra);
+    e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
+      reconstruct_fast_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(g, ra);
+      return cudaSuccess;
+    });
   }
+  if (e != cudaSuccess) return e;
   // deep rows and columns: index lists [M] and [N], and their two counters
   int* rows = deep_lists;
   int* cols = deep_lists + g.M;

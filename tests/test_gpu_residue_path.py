@@ -3,7 +3,7 @@
 det_gemm routes tiles whose rows and columns hold few "deep" elements (more
 than 19 binades below their row maximum) to the residue decomposition on the
 tensor cores, and other tiles to the general Kulisch kernel.  These cases aim
-at the residue path's own corners: the longest K (14 moduli, 512 exact fp32
+at the residue path's own corners: the longest K (14 moduli, 631 exact fp32
 accumulation windows reduced in TMEM), bf16 planes, deep elements handled
 from the per-row lists (inside and outside the 192-bit window), non-finite
 values next to deep ones, and matrices whose tiles are split between the two
