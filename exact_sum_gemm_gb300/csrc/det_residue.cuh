@@ -76,6 +76,17 @@ constexpr int kStageK = 64;       // K per TMA/MMA stage (one 128-byte swizzle r
 static_assert(kChunkK % kStageK == 0, "accumulation windows are whole stages");
 static_assert(int64_t(kChunkK) * 138 * 138 + 131 < (int64_t(1) << 24), "window stays exact in fp32");
 
+// Plane layout.  Rows are taken in groups of kPlaneRows; for each group and
+// 64-k stage the nplanes planes follow one another, each a 32 x 64 bf16 block
+// (4 KB, 128 bytes per row):
+//   plane u of element (r, k) at
+//   (((r / 32) * Kp/64 + k / 64) * nplanes + u) * 2048 + (r % 32) * 64 + k % 64.
+// The residue kernel writes an element pair's planes at fixed 4 KB steps, and
+// one modulus's stage for 32 rows is one contiguous 4 KB block for the TMA.
+// Padding rows (up to a multiple of 32) hold zero residues.
+constexpr int kPlaneRows = 32;
+inline int64_t plane_rows(int64_t rows) { return (rows + kPlaneRows - 1) / kPlaneRows * kPlaneRows; }
+
 struct ResidueOperand {
   const void* X;
   int64_t ld;
@@ -84,9 +95,8 @@ struct ResidueOperand {
   int64_t K;
   int64_t Kp;                 // K rounded up to kStageK (zero padded)
   const int* emax;            // [rows]
-  __nv_bfloat16* planes;      // [rows][Kp/64][nplanes][64]: a row's 64-k stages, all planes of a
-                              // stage together (plane u of element (r, k) at
-                              // ((r * Kp/64 + k/64) * nplanes + u) * 64 + k % 64)
+  __nv_bfloat16* planes;      // [rows/32][Kp/64][nplanes][32][64] (rows padded to 32, see
+                              // kPlaneRows)
   int* list_count;            // [rows], zeroed before the launch
   uint2* list;                // [rows][cap]: (k, raw bits) of deep / non-finite elements
   int cap;
@@ -113,8 +123,8 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
                                int* deep_counters, cudaStream_t stream);
 
 struct ResGemmArgs {
-  const __nv_bfloat16* A;     // [M][Kp/64][nplanes][64] (ResidueOperand::planes)
-  const __nv_bfloat16* B;     // [N][Kp/64][nplanes][64]
+  const __nv_bfloat16* A;     // [M/32][Kp/64][nplanes][32][64] (ResidueOperand::planes)
+  const __nv_bfloat16* B;     // [N/32][Kp/64][nplanes][32][64]
   int64_t M, N, Kp;
   int nplanes;
   int8_t* res;                // [nplanes][M][N] balanced residues

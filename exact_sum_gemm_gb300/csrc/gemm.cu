@@ -140,9 +140,9 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   r.off_listB = b;
   b = align_up(b + sizeof(uint2) * size_t(g.N) * cap, 1024);
   r.off_planesA = b;
-  b = align_up(b + size_t(2) * nplanes * size_t(g.M) * size_t(Kp), 1024);
+  b = align_up(b + size_t(2) * nplanes * size_t(plane_rows(g.M)) * size_t(Kp), 1024);
   r.off_planesB = b;
-  b = align_up(b + size_t(2) * nplanes * size_t(g.N) * size_t(Kp), 1024);
+  b = align_up(b + size_t(2) * nplanes * size_t(plane_rows(g.N)) * size_t(Kp), 1024);
   r.off_res = b;
   b = align_up(b + size_t(nplanes) * size_t(g.M) * size_t(g.N), 1024);
   r.bytes = b;

@@ -13,8 +13,8 @@
 // Structure (persistent, one CTA per SM, looping over units = (modulus, pair
 // of neighbouring 128x256 output tiles), modulus-major):
 //   warp 0      TMA producer: 64-wide K stages of A_u (128 rows) and B_u (256
-//               rows), 128-byte swizzled, 4-stage mbarrier ring (the planes
-//               are stored [rows][K/64][P][64], see det_residue.cuh)
+//               rows), 128-byte swizzled, 4-stage mbarrier ring (plane
+//               layout: det_residue.cuh)
 //   warp 1      TMEM allocation (512 columns = two 128x256 f32 accumulators)
 //               and the single MMA-issuing thread (UMMA 128x256x16, bf16)
 //   warps 2-5   epilogue: tcgen05.ld the accumulator (each warp owns 32 TMEM
@@ -49,6 +49,7 @@ constexpr int kABytes = kBlockM * kStageK * 2;               // 16 KB
 constexpr int kBBytes = kBlockN * kStageK * 2;               // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;               // 48 KB
 constexpr int kKbPerChunk = kChunkK / kStageK;               // 13
+static_assert(kBlockM % kPlaneRows == 0 && kBlockN % kPlaneRows == 0, "tiles cover whole row groups");
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBlockM, kBlockN);
 constexpr uint32_t kTmemCols = 512;
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 1024;
@@ -154,8 +155,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
           unsigned char* st = smem + s * kStageBytes;
-          ptx::tma_load_4d(st, &tmA, &full[s], 0, u, kb, static_cast<int>(m0));
-          ptx::tma_load_4d(st + kABytes, &tmB, &full[s], 0, u, kb, static_cast<int>(n0));
+          ptx::tma_load_5d(st, &tmA, &full[s], 0, 0, u, kb, static_cast<int>(m0 / kPlaneRows));
+          ptx::tma_load_5d(st + kABytes, &tmB, &full[s], 0, 0, u, kb,
+                           static_cast<int>(n0 / kPlaneRows));
           ++it;
         }
       }
@@ -313,23 +315,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 4-D map over the planes [rows][Kp/64][P][64] of bf16 (innermost first:
-// 64 k of one stage, plane, stage, row).  A box of 64 x 1 x 1 x box_rows is
-// one plane's 64-k stage for box_rows rows: box_rows 128-byte rows in shared
-// memory, 128-byte swizzled, as the UMMA descriptors expect.
+// 5-D map over the planes [rows/32][Kp/64][P][32][64] of bf16 (innermost
+// first: 64 k of one stage, row in group, plane, stage, row group).  A box of
+// 64 x 32 x 1 x 1 x box_rows/32 is one plane's 64-k stage for box_rows rows:
+// box_rows 128-byte rows in shared memory, in row order, 128-byte swizzled,
+// as the UMMA descriptors expect.  Row groups past the end read as zero.
 bool make_plane_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp, int planes,
                     int box_rows) {
   PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
   if (enc == nullptr) return false;
   const cuuint64_t nkb = static_cast<cuuint64_t>(Kp / kStageK);
-  cuuint64_t dims[4] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(planes), nkb,
-                        static_cast<cuuint64_t>(rows)};
-  cuuint64_t strides[3] = {static_cast<cuuint64_t>(kStageK) * 2,
-                           static_cast<cuuint64_t>(planes) * kStageK * 2,
-                           nkb * static_cast<cuuint64_t>(planes) * kStageK * 2};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(kStageK), 1, 1, static_cast<cuuint32_t>(box_rows)};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides,
+  const cuuint64_t block = static_cast<cuuint64_t>(kPlaneRows) * kStageK * 2;     // 4 KB
+  cuuint64_t dims[5] = {static_cast<cuuint64_t>(kStageK), static_cast<cuuint64_t>(kPlaneRows),
+                        static_cast<cuuint64_t>(planes), nkb,
+                        static_cast<cuuint64_t>(plane_rows(rows) / kPlaneRows)};
+  cuuint64_t strides[4] = {static_cast<cuuint64_t>(kStageK) * 2, block,
+                           static_cast<cuuint64_t>(planes) * block,
+                           nkb * static_cast<cuuint64_t>(planes) * block};
+  cuuint32_t box[5] = {static_cast<cuuint32_t>(kStageK), static_cast<cuuint32_t>(kPlaneRows), 1, 1,
+                       static_cast<cuuint32_t>(box_rows / kPlaneRows)};
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(base), dims, strides,
                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

@@ -61,25 +61,26 @@ __device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
   return __byte_perm(__float_as_uint(lo), __float_as_uint(hi), 0x7632);
 }
 
-// Plane i of an element pair sits 64 bf16 (32 pairs) after plane i - 1.
+// Plane i of an element pair sits one 32 x 64 block (4 KB, 1024 bf16 pairs)
+// after plane i - 1.
 template <int i, int P>
 __device__ __forceinline__ void write_residue_pairs(uint32_t* dst, float x0, float pw0, float x1,
                                                     float pw1) {
   if constexpr (i < P) {
     constexpr int p = modulus(i);
-    dst[i * (kStageK / 2)] = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
+    dst[i * (kPlaneRows * kStageK / 2)] = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
     write_residue_pairs<i + 1, P>(dst, x0, pw0, x1, pw1);
   }
 }
 
-// One block: 32 rows x one 64-k stage of one operand; each thread then
-// handles pairs of neighbouring k, writing the P residues of a pair as P
-// 4-byte words 128 bytes apart (a warp covers one row's stage: P contiguous
-// 128-byte lines).  Every deep or non-finite element is counted (and listed
-// while there is room).
+// One block: one group of 32 rows x one 64-k stage of one operand; each
+// thread then handles pairs of neighbouring k, writing the P residues of a
+// pair as P 4-byte words 4 KB apart (a warp covers one row's stage: one
+// 128-byte line per plane).  Padding rows get zero residues.  Every deep or
+// non-finite element is counted (and listed while there is room).
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
-  static_assert(kTileK == kStageK, "one block covers one plane stage");
+  static_assert(kTileK == kStageK && kTileRows == kPlaneRows, "one block covers one plane block");
   __shared__ uint32_t tile[kTileRows][kTileK + 1];
   __shared__ int row_emax[kTileRows];
   const int tid = threadIdx.x;
@@ -106,7 +107,6 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
     const int idx = tid + u * kThreads;
     const int r = idx >> 5, kk = (idx & 31) * 2;
     const int64_t gr = r0 + r, gk = k0 + kk;
-    if (gr >= o.rows) continue;
     const int em = row_emax[r];
     float x[2], pw[2];
 #pragma unroll
@@ -120,13 +120,14 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
       const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
       x[h] = static_cast<float>(deep ? 0 : mi);                        // exact: |mi| < 2^24
       pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 19]
-      if (deep && gk + h < o.K) {
+      if (deep && gk + h < o.K && gr < o.rows) {
         const int slot = atomicAdd(o.list_count + gr, 1);
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
       }
     }
-    uint32_t* dst =
-        reinterpret_cast<uint32_t*>(o.planes + (gr * nkb + int64_t(blockIdx.x)) * P * kStageK + kk);
+    uint32_t* dst = reinterpret_cast<uint32_t*>(
+        o.planes + (int64_t(blockIdx.y) * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
+        r * kStageK + kk);
     write_residue_pairs<0, P>(dst, x[0], pw[0], x[1], pw[1]);
   }
 }
