@@ -20,6 +20,7 @@ struct Scratch {
   int* deepB;          // [N]
   uint8_t* route;      // [tiles of 64x64]: 1 = general kernel
   int* general;        // [1 + tiles]: count, then the indices of the tiles routed to the general kernel
+  int* bmax;           // [tiles_m + tiles_n]: largest deep count per 64-row / 64-column block
   int64_t* fallback;   // [slots][kPlanes][kTile*kTile] band-kernel fallback digits (det_gemm only)
   int64_t slots;       // resident band-kernel CTAs (fallback regions)
 };
@@ -35,8 +36,12 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
 // The residue path's pieces of the pre-pass: row maxima only, and routing from
 // deep counts produced elsewhere (the residue kernel's list counters).
 cudaError_t launch_emax(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
-cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
-                            int* general, cudaStream_t stream);
+// Routing from deep counts; with deep_rows / deep_cols / deep_counters (two
+// ints, zero at launch) it also lists the rows and columns holding deep
+// elements (residue path), else pass null.
+cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, const Scratch& s,
+                            int* deep_rows, int* deep_cols, int* deep_counters,
+                            cudaStream_t stream);
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 // General kernel over the 64x64 tiles listed in general (count first).
 cudaError_t launch_kulisch(const GemmArgs& g, const int* general, cudaStream_t stream);

@@ -118,7 +118,9 @@ struct ReconArgs {
 
 int residue_planes_needed(const GemmArgs& g);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
-// deep_lists: scratch of M + N ints; deep_counters: 2 ints, zero at launch.
+// deep_lists: the rows of A then the columns of C that hold deep elements
+// (M + N ints), with their two counts in deep_counters, as the routing step
+// lists them.
 cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
                                int* deep_counters, cudaStream_t stream);
 

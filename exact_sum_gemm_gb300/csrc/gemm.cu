@@ -54,6 +54,7 @@ cudaError_t device_pool(cudaMemPool_t* out) {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+int64_t tiles_mn(const GemmArgs& g) { return (g.M + kTile - 1) / kTile + (g.N + kTile - 1) / kTile; }
 
 }  // namespace
 
@@ -63,6 +64,7 @@ size_t scratch_bytes(const GemmArgs& g, int64_t slots) {
   b += align_up(sizeof(int) * size_t(g.M + g.N), 256);              // deep
   b += align_up(size_t(tiles), 256);                                 // route
   b += align_up(sizeof(int) * size_t(tiles + 1), 256);              // general-tile list
+  b += align_up(sizeof(int) * size_t(tiles_mn(g)), 256);            // block maxima
   if (g.P == nullptr) b += sizeof(int64_t) * size_t(slots) * kPlanes * kTile * kTile;
   return b;
 }
@@ -81,6 +83,8 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots) {
   p += align_up(size_t(tiles), 256);
   s.general = reinterpret_cast<int*>(p);
   p += align_up(sizeof(int) * size_t(tiles + 1), 256);
+  s.bmax = reinterpret_cast<int*>(p);
+  p += align_up(sizeof(int) * size_t(tiles_mn(g)), 256);
   s.fallback = g.P == nullptr ? reinterpret_cast<int64_t*>(p) : nullptr;
   s.slots = slots;
   return s;
@@ -159,6 +163,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   __nv_bfloat16* planesA = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesA);
   __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
   int8_t* res = reinterpret_cast<int8_t*>(base + L.off_res);
+  int* deep_rows = reinterpret_cast<int*>(base + L.off_deep_idx);   // [M] rows, then [N] columns
 
   cudaError_t e;
   {
@@ -176,7 +181,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
     e = launch_residues(ra, g.bf16, nplanes, stream);
     if (e == cudaSuccess) e = launch_residues(rb, g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s.route, s.general, stream);
+    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M,
+                                               error + 1, stream);
   }
   if (e != cudaSuccess) return e;
   {
@@ -190,7 +196,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
                  error};
     // deep-row/column lists, and their two counters right after the error flag
-    e = launch_reconstruct(g, rc, reinterpret_cast<int*>(base + L.off_deep_idx), error + 1, stream);
+    e = launch_reconstruct(g, rc, deep_rows, error + 1, stream);
   }
   if (e != cudaSuccess) return e;
   StageScope t(kStageGeneral, stream);

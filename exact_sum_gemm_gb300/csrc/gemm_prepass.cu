@@ -41,10 +41,66 @@ __device__ __forceinline__ int row_emax(const int* emax, int64_t r) {
   return v == kEmaxEmpty ? 0 : v;
 }
 
+// Exponent key of a binary32 pattern (a bf16 widened to binary32): the
+// biased exponent, with subnormals counted as 1 (their last-bit exponent,
+// -149, is that of biased exponent 1), and 0 for zero and non-finite values.
+// For a live element, key - 150 is the exponent e of its last significand bit.
+__device__ __forceinline__ int exp_key(uint32_t bits) {
+  const uint32_t a = bits & 0x7FFFFFFFu;
+  const int key = max(static_cast<int>(a >> 23), 1);
+  return (a == 0u || a >= 0x7F800000u) ? 0 : key;
+}
+
+// emax of one full kRowChunk of a K-contiguous row whose chunk start is
+// 16-byte aligned: 16-byte loads, exponent keys only.
+template <int kBf16>
+__device__ void emax_chunk_vec(const StatOperand& o, int64_t r, int64_t k0) {
+  constexpr int kPer = kBf16 ? 8 : 4;                     // elements per 16-byte load
+  constexpr int kLoads = kRowChunk / kPer / kThreads;
+  const uint4* src = reinterpret_cast<const uint4*>(static_cast<const char*>(o.X) +
+                                                    (r * o.ld + k0) * (kBf16 ? 2 : 4));
+  const int tid = threadIdx.x;
+  uint4 v[kLoads];
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) v[u] = __ldg(src + u * kThreads + tid);
+  int key = 0;
+#pragma unroll
+  for (int u = 0; u < kLoads; ++u) {
+    const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      if (kBf16) {
+        key = max(key, max(exp_key(w[q] << 16), exp_key(w[q] & 0xFFFF0000u)));
+      } else {
+        key = max(key, exp_key(w[q]));
+      }
+    }
+  }
+  __shared__ int red[kThreads / 32];
+  key = __reduce_max_sync(0xFFFFFFFFu, key);
+  if ((tid & 31) == 0) red[tid >> 5] = key;
+  __syncthreads();
+  if (tid == 0) {
+    int k = red[0];
+    for (int w = 1; w < kThreads / 32; ++w) k = max(k, red[w]);
+    if (k != 0) atomicMax(o.emax + r, k - 150);
+  }
+}
+
 // pass 0: emax; pass 1: deep counts (needs emax complete)
 template <int kBf16, int kPass>
 __device__ void stat_block(const StatOperand& o, int64_t K, int64_t b) {
   const int tid = threadIdx.x;
+  if (o.op == 0 && kPass == 0) {
+    const int64_t nkc = (K + kRowChunk - 1) / kRowChunk;
+    const int64_t r = b / nkc;
+    const int64_t k0 = (b - r * nkc) * kRowChunk;
+    const uintptr_t addr = reinterpret_cast<uintptr_t>(o.X) + (r * o.ld + k0) * (kBf16 ? 2 : 4);
+    if (k0 + kRowChunk <= K && (addr & 15u) == 0) {
+      emax_chunk_vec<kBf16>(o, r, k0);
+      return;
+    }
+  }
   if (o.op == 0) {
     const int64_t nkc = (K + kRowChunk - 1) / kRowChunk;
     const int64_t r = b / nkc;
@@ -109,21 +165,52 @@ __global__ void __launch_bounds__(kThreads) rowstat_kernel(StatOperand a, StatOp
   else stat_block<kBf16, kPass>(b, K, blk - a.blocks);
 }
 
-// One thread per 64x64 tile: 1 = general kernel, 0 = residue path / band kernel.
-// The general kernel's tiles are also listed (in any order: each tile is
-// computed on its own) after a count, general[0], zero at launch.
-__global__ void __launch_bounds__(kThreads) classify_kernel(const int* deepA, const int* deepB,
-                                                             int64_t M, int64_t N, int cap,
-                                                             uint8_t* route, int* general) {
-  const int64_t tiles_n = (N + kTile - 1) / kTile;
-  const int64_t tiles = ((M + kTile - 1) / kTile) * tiles_n;
+// Routing, step 1: the largest deep count of every 64-row block of A and of
+// every 64-column block of C (one warp each), into bmax[tiles_m + tiles_n].
+// With lists (residue path) it also lists the rows of A and columns of C that
+// hold deep elements (in any order: every output is computed on its own).
+// It resets the general-tile count read by step 2.
+__global__ void __launch_bounds__(kThreads) block_max_kernel(const int* deepA, int64_t M,
+                                                              const int* deepB, int64_t N, int* bmax,
+                                                              int* rows, int* cols, int* nrc,
+                                                              int* general) {
+  if (blockIdx.x == 0 && threadIdx.x == 0) general[0] = 0;
+  const int64_t tiles_m = (M + kTile - 1) / kTile, tiles_n = (N + kTile - 1) / kTile;
+  const int64_t w = (int64_t(blockIdx.x) * kThreads + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (w >= tiles_m + tiles_n) return;                       // whole warps
+  const bool is_a = w < tiles_m;
+  const int* cnt = is_a ? deepA : deepB;
+  const int64_t len = is_a ? M : N;
+  const int64_t base = (is_a ? w : w - tiles_m) * kTile;
+  int mx = 0;
+#pragma unroll
+  for (int h = 0; h < kTile / 32; ++h) {
+    const int64_t i = base + lane + 32 * h;
+    if (i < len) {
+      const int c = cnt[i];
+      mx = max(mx, c);
+      if (c != 0 && rows != nullptr) {
+        if (is_a) rows[atomicAdd(nrc, 1)] = static_cast<int>(i);
+        else cols[atomicAdd(nrc + 1, 1)] = static_cast<int>(i);
+      }
+    }
+  }
+  mx = __reduce_max_sync(0xFFFFFFFFu, mx);
+  if (lane == 0) bmax[w] = mx;
+}
+
+// Routing, step 2, one thread per 64x64 tile: 1 = general kernel, 0 = residue
+// path / band kernel.  The general kernel's tiles are also listed after a
+// count, general[0].
+__global__ void __launch_bounds__(kThreads) route_kernel(const int* bmax, int64_t tiles_m,
+                                                          int64_t tiles_n, int cap, uint8_t* route,
+                                                          int* general) {
+  const int64_t tiles = tiles_m * tiles_n;
   for (int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x; t < tiles;
        t += int64_t(gridDim.x) * kThreads) {
     const int64_t tm = t / tiles_n, tn = t - (t / tiles_n) * tiles_n;
-    int da = 0, db = 0;
-    for (int64_t m = tm * kTile; m < min(M, tm * kTile + kTile); ++m) da = max(da, deepA[m]);
-    for (int64_t n = tn * kTile; n < min(N, tn * kTile + kTile); ++n) db = max(db, deepB[n]);
-    const bool gen = static_cast<int64_t>(da) + db > cap;
+    const bool gen = static_cast<int64_t>(bmax[tm]) + bmax[tiles_m + tn] > cap;
     route[t] = gen ? 1 : 0;
     if (gen) general[1 + atomicAdd(general, 1)] = static_cast<int>(t);
   }
@@ -161,15 +248,19 @@ int deep_list_cap(int64_t K) {
   return static_cast<int>(c > 8 ? c : 8);
 }
 
-cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, uint8_t* route,
-                            int* general, cudaStream_t stream) {
-  const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
-  const int64_t grid = (tiles + kThreads - 1) / kThreads;
-  cudaError_t e = cudaMemsetAsync(general, 0, sizeof(int), stream);
-  if (e != cudaSuccess) return e;
-  classify_kernel<<<static_cast<unsigned>(grid < 1024 ? grid : 1024), kThreads, 0, stream>>>(
-      deepA, deepB, g.M, g.N, deep_list_cap(g.K), route, general);
-  note_launch();
+cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, const Scratch& s,
+                            int* deep_rows, int* deep_cols, int* deep_counters,
+                            cudaStream_t stream) {
+  const int64_t tiles_m = (g.M + kTile - 1) / kTile, tiles_n = (g.N + kTile - 1) / kTile;
+  const int64_t warps = tiles_m + tiles_n;
+  const int64_t grid1 = (warps * 32 + kThreads - 1) / kThreads;
+  block_max_kernel<<<static_cast<unsigned>(grid1 > 0 ? grid1 : 1), kThreads, 0, stream>>>(
+      deepA, g.M, deepB, g.N, s.bmax, deep_rows, deep_cols, deep_counters, s.general);
+  const int64_t tiles = tiles_m * tiles_n;
+  const int64_t grid2 = (tiles + kThreads - 1) / kThreads;
+  route_kernel<<<static_cast<unsigned>(grid2 < 1024 ? (grid2 > 0 ? grid2 : 1) : 1024), kThreads, 0,
+                 stream>>>(s.bmax, tiles_m, tiles_n, deep_list_cap(g.K), s.route, s.general);
+  note_launch(2);
   return cudaGetLastError();
 }
 
@@ -188,7 +279,7 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
   if (e != cudaSuccess) return e;
   e = g.bf16 ? rowstat_t<1>(g, s, true, stream) : rowstat_t<0>(g, s, true, stream);
   if (e != cudaSuccess) return e;
-  return launch_classify(g, s.deepA, s.deepB, s.route, s.general, stream);
+  return launch_classify(g, s.deepA, s.deepB, s, nullptr, nullptr, nullptr, stream);
 }
 
 }  // namespace det

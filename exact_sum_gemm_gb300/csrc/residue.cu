@@ -656,21 +656,6 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
   }
 }
 
-// Rows of A / columns of C with deep elements, compacted into index lists
-// (order irrelevant: every output is computed independently and exactly).
-__global__ void __launch_bounds__(kThreads) compact_deep_kernel(const int* countA, int64_t M,
-                                                                 const int* countB, int64_t N,
-                                                                 int* rows, int* cols, int* nrc) {
-  for (int64_t i = int64_t(blockIdx.x) * kThreads + threadIdx.x; i < M + N;
-       i += int64_t(gridDim.x) * kThreads) {
-    if (i < M) {
-      if (countA[i] != 0) rows[atomicAdd(nrc, 1)] = static_cast<int>(i);
-    } else if (countB[i - M] != 0) {
-      cols[atomicAdd(nrc + 1, 1)] = static_cast<int>(i - M);
-    }
-  }
-}
-
 // det_gemm outputs with deep entries: every output of a deep row, then every
 // output of a deep column outside the deep rows.  Dense work list, so the
 // warps stay full.
@@ -826,7 +811,8 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
     });
   }
   if (e != cudaSuccess) return e;
-  // deep rows and columns: index lists [M] and [N], and their two counters
+  // deep rows and columns: index lists [M] and [N] and their two counters,
+  // filled by the routing step
   int* rows = deep_lists;
   int* cols = deep_lists + g.M;
   int* nrc = deep_counters;
@@ -834,15 +820,12 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int64_t cgrid = (g.M + g.N + kThreads - 1) / kThreads;
-  compact_deep_kernel<<<static_cast<unsigned>(cgrid < sms * 8 ? cgrid : sms * 8), kThreads, 0,
-                        stream>>>(ra.countA, g.M, ra.countB, g.N, rows, cols, nrc);
   const unsigned dgrid = static_cast<unsigned>(sms) * 4;
   if (g.bf16)
     reconstruct_deep_kernel<1><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
   else
     reconstruct_deep_kernel<0><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
-  note_launch(3);
+  note_launch(2);
   return cudaGetLastError();
 }
 
