@@ -114,7 +114,17 @@ struct ReconArgs {
   const uint2* listB;
   int cap;
   const int* error;           // nonzero: the tensor-core kernel gave up (outputs NaN)
+  const int* colslot;         // [N]: a deep column's slot in the deep-column list, else -1
+  ulonglong2* sbuf;           // [M][slots]: shallow sums S of deep-column outputs (lo, hi)
+  int slots;                  // slots kept in sbuf; columns in later slots re-read residues
 };
+
+// Deep columns whose shallow sums are passed from the fast reconstruction to
+// the deep one through a compact buffer (the rest re-read their residues).
+inline int deep_col_slots(int64_t N) {
+  const int64_t s = N / 16;
+  return static_cast<int>(N < 64 ? N : (s < 64 ? 64 : s));
+}
 
 int residue_planes_needed(const GemmArgs& g);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);

@@ -129,7 +129,7 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
 
 struct ResidueScratch {
   size_t bytes;
-  size_t off_counts, off_deep_idx, off_listA, off_listB, off_planesA, off_planesB, off_res;
+  size_t off_counts, off_deep_idx, off_sbuf, off_listA, off_listB, off_planesA, off_planesB, off_res;
 };
 
 ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int cap) {
@@ -137,8 +137,10 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   size_t b = align_up(scratch_bytes(g, 0), 1024);
   r.off_counts = b;                     // countA [M], countB [N], error, deep-row/col counters [2]
   b = align_up(b + sizeof(int) * size_t(g.M + g.N + 3), 1024);
-  r.off_deep_idx = b;                    // deep rows [M], deep columns [N] (+ the 2 counters above)
-  b = align_up(b + sizeof(int) * size_t(g.M + g.N), 1024);
+  r.off_deep_idx = b;                    // deep rows [M], deep columns [N], column slots [N]
+  b = align_up(b + sizeof(int) * size_t(g.M + 2 * g.N), 1024);
+  r.off_sbuf = b;                        // shallow sums of deep-column outputs [M][slots]
+  b = align_up(b + 16 * size_t(g.M) * size_t(deep_col_slots(g.N)), 1024);
   r.off_listA = b;
   b = align_up(b + sizeof(uint2) * size_t(g.M) * cap, 1024);
   r.off_listB = b;
@@ -194,7 +196,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   {
     StageScope t(kStageReconstruct, stream);
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
-                 error};
+                 error, deep_rows + g.M + g.N, reinterpret_cast<ulonglong2*>(base + L.off_sbuf),
+                 deep_col_slots(g.N)};
     // deep-row/column lists, and their two counters right after the error flag
     e = launch_reconstruct(g, rc, deep_rows, error + 1, stream);
   }

@@ -317,7 +317,9 @@ __device__ __forceinline__ void write_canonical_digits(int64_t* out, int64_t MN,
 // multiple of 2^-298 below 2^277 in magnitude), as one output's 20 planes.
 // Digit j holds bits [32j - off, 32j - off + 32) of S, off = E + 298: the
 // five words of S shifted by off mod 32 land on digits off/32 .. off/32 + 4,
-// digits below are 0 and digits above repeat the sign.
+// digits below are 0 and digits above repeat the sign.  Every digit plane
+// gets its fill value first, then the five words overwrite theirs (the same
+// thread's stores to one address stay in order).
 __device__ __forceinline__ void write_digits_s128(int64_t* out, int64_t MN, uint64_t lo, uint64_t hi,
                                                   int E, int64_t K, int64_t nf) {
   int off = E + kLsbBias;
@@ -331,19 +333,18 @@ __device__ __forceinline__ void write_digits_s128(int64_t* out, int64_t MN, uint
   const uint32_t w0 = static_cast<uint32_t>(lo), w1 = static_cast<uint32_t>(lo >> 32);
   const uint32_t w2 = static_cast<uint32_t>(hi), w3 = static_cast<uint32_t>(hi >> 32);
   const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(w3) >> 31);
-  const uint32_t x0 = w0 << sh, x1 = __funnelshift_l(w0, w1, sh), x2 = __funnelshift_l(w1, w2, sh);
-  const uint32_t x3 = __funnelshift_l(w2, w3, sh), x4 = __funnelshift_l(w3, sx, sh);
+  const int64_t fill = static_cast<int64_t>(sx);                      // digit value above
 #pragma unroll
-  for (int j = 0; j < kDigits; ++j) {
-    const int k = j - j0;
-    uint32_t d = k < 0 ? 0u : sx;
-    d = k == 0 ? x0 : d;
-    d = k == 1 ? x1 : d;
-    d = k == 2 ? x2 : d;
-    d = k == 3 ? x3 : d;
-    d = k == 4 ? x4 : d;
-    out[j * MN] = j < kDigits - 1 ? static_cast<int64_t>(d)
-                                  : static_cast<int64_t>(static_cast<int32_t>(d));
+  for (int j = 0; j < kDigits - 1; ++j) out[j * MN] = j < j0 ? 0 : fill;
+  out[(kDigits - 1) * MN] = static_cast<int64_t>(static_cast<int32_t>(sx));
+  const uint32_t x[5] = {w0 << sh, __funnelshift_l(w0, w1, sh), __funnelshift_l(w1, w2, sh),
+                         __funnelshift_l(w2, w3, sh), __funnelshift_l(w3, sx, sh)};
+  int64_t* dst = out + j0 * MN;
+#pragma unroll
+  for (int i = 0; i < 5; ++i) {
+    const int j = j0 + i;
+    if (j < kDigits - 1) dst[i * MN] = static_cast<int64_t>(x[i]);
+    else if (j == kDigits - 1) dst[i * MN] = static_cast<int64_t>(static_cast<int32_t>(x[i]));
   }
   out[kDigits * MN] = K;
   out[(kDigits + 1) * MN] = nf;
@@ -642,12 +643,18 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
     for (int j = 0; j < kReconCols; ++j) {
       if (j >= ncols) break;
       const int64_t n = n0 + j;
-      if (ra.countB[n] != 0) continue;                            // deep column: full kernel
+      const bool col_deep = ra.countB[n] != 0;
+      const int slot = col_deep ? ra.colslot[n] : -1;
+      if (col_deep && (slot < 0 || slot >= ra.slots)) continue;  // deep kernel re-reads it
       float f[kNumModuli];
 #pragma unroll
       for (int i = 0; i < kNumModuli; ++i) f[i] = biased_residue_of_word(packed[i], j);
       uint64_t slo, shi;
       garner_s128<P>(f, P, slo, shi);
+      if (col_deep) {                                             // the deep kernel finishes it
+        ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
+        continue;
+      }
       int emB = ra.emaxB[n];
       emB = emB == kEmaxEmpty ? 0 : emB;
       const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
@@ -670,26 +677,33 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
   const int64_t part1 = n_rows * g.N, total = part1 + g.M * n_cols;
   for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * kThreads) {
-    int64_t m, n;
+    int64_t m, n, slot = -1;
     if (idx < part1) {
       m = rows[idx / g.N];
       n = idx - (idx / g.N) * g.N;
     } else {
       const int64_t j = idx - part1;
       m = j / n_cols;
-      n = cols[j - m * n_cols];
+      slot = j - m * n_cols;
+      n = cols[slot];
       if (ra.countA[m] != 0) continue;                          // done with its deep row
     }
     if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's output
     int emA = ra.emaxA[m], emB = ra.emaxB[n];
     emA = emA == kEmaxEmpty ? 0 : emA;
     emB = emB == kEmaxEmpty ? 0 : emB;
-    float f[kNumModuli];
-#pragma unroll
-    for (int i = 0; i < kNumModuli; ++i)
-      f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + m * g.N + n]) : 0u);
     uint64_t slo, shi;
-    garner_s128<kNumModuli>(f, ra.nplanes, slo, shi);
+    if (slot >= 0 && slot < ra.slots) {          // shallow sum left by the fast kernel
+      const ulonglong2 v = ra.sbuf[m * ra.slots + slot];
+      slo = v.x;
+      shi = v.y;
+    } else {
+      float f[kNumModuli];
+#pragma unroll
+      for (int i = 0; i < kNumModuli; ++i)
+        f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + m * g.N + n]) : 0u);
+      garner_s128<kNumModuli>(f, ra.nplanes, slo, shi);
+    }
     const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
     W192 t;
     t.w[0] = 0;
@@ -718,7 +732,10 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
   const int64_t n = int64_t(blockIdx.x) * kThreads + threadIdx.x;
-  if (n >= g.N || ra.countB[n] != 0) return;                  // deep column: deep kernel
+  if (n >= g.N) return;
+  const bool col_deep = ra.countB[n] != 0;                    // the deep kernel finishes these
+  const int slot = col_deep ? ra.colslot[n] : -1;
+  if (col_deep && (slot < 0 || slot >= ra.slots)) return;     // ... re-reading the residues
   int emB = ra.emaxB[n];
   emB = emB == kEmaxEmpty ? 0 : emB;
   for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
@@ -733,6 +750,10 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
       f[i] = biased_residue(i < P ? static_cast<uint8_t>(ra.res[i * MN + idx]) : 0u);
     uint64_t slo, shi;
     garner_s128<P>(f, P, slo, shi);
+    if (col_deep) {
+      ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
+      continue;
+    }
     const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
     write_digits_s128(g.P + idx, MN, slo, shi, Es, g.K, nf);
   }

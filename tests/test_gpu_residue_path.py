@@ -97,3 +97,22 @@ def test_all_zero_rows_and_exact_cancellation(oracle_mod):
     got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
     assert np.all(got == 0)
     assert_bits_equal(got, np_bits(oracle_mod.gemm(A, B)), "cancellation")
+
+
+def test_many_deep_columns_and_rows(oracle_mod):
+    # 100 columns of C and 40 rows of A with one deep element each: more deep
+    # columns than the reconstruction buffers (64 here), so some deep-column
+    # outputs take the buffered shallow sum and the rest re-read residues
+    g = np.random.default_rng(41)
+    M, N, K = 130, 300, 1000
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((N, K)).astype(np.float32)
+    for i, n in enumerate(range(0, N, 3)):
+        B[n, (7 * i) % K] = np.float32(3e-9) * (1 if i % 2 else -1)
+    for i, m in enumerate(range(0, M, 3)[:40]):
+        A[m, (11 * i + 5) % K] = np.float32(-2e-9)
+    A[4, 9] = np.float32(1e-40)                  # far below the window: digit route
+    want = np_bits(oracle_mod.gemm(A, B))
+    a, b = dev_f32(A), dev_f32(B)
+    assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, "many deep rows and columns")
+    np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B))
