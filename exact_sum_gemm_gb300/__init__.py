@@ -1,11 +1,12 @@
 """Exact-sum (Kulisch long-accumulator) GEMM for GB300, as a thin torch binding.
 
-The calls follow the det-train page's usage section:
+The call names follow the det-train page's usage section:
 
-    y  = det_gemm(x, w)                      # x [M,K], w [N,K] -> fp32 [M,N]
-    a1 = det_gemm_partial(x[:, :k], w[:, :k])  # int64 digit array [20,M,N]
-    y2 = det_finalize(det_combine([a1, a2]))   # == det_gemm(x, w), bit for bit
-    layer = DetLinear(4096, 4096, device="cuda")
+    y = det_gemm(a, b)                         # a [M,K], b [N,K] -> fp32 [M,N]
+    lo = det_gemm_partial(a[:, :k], b[:, :k])  # int64 digit array [20,M,N]
+    hi = det_gemm_partial(a[:, k:], b[:, k:])
+    y2 = det_finalize(det_combine([lo, hi]))   # equal to y, bit for bit
+    lin = DetLinear(1024, 512, device="cuda")
 
 Every step runs in the sm_103a kernels of ``libdetgemm.so`` behind the C ABI of
 ``include/det_gemm.h``; this module only checks arguments, allocates outputs

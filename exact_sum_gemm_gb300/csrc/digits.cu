@@ -1,9 +1,9 @@
 // Digit-array kernels: combine (elementwise int64 addition of partials) and
 // finalize (carry-normalise, round once to fp32).
 //
-// det-train page, section "Method": "Sharded partials compose by adding digit
-// arrays", and the final digits are rounded once to fp32 (round to nearest
-// even).  Both kernels are HBM-bound streams over planar [20][M][N] int64
+// det-train page, section "Method": digit arrays of K-shards combine by plain
+// addition, and the final digits get a single rounding to fp32 (to nearest,
+// ties to even).  Both kernels are HBM-bound streams over planar [20][M][N] int64
 // arrays: consecutive threads touch consecutive outputs of one plane, so every
 // load and store is coalesced; where alignment allows, each thread handles two
 // neighbouring outputs with 16-byte accesses.  Grids are a multiple of the SM

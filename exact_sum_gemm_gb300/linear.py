@@ -1,9 +1,8 @@
 """DetLinear: a bias-free linear layer whose forward and backward GEMMs are exact.
 
-det-train page, usage section: ``layer = dt.DetLinear(4096, 4096, device="cuda")``;
-``y = layer(x); y.square().mean().backward()`` is deterministic in forward and
-backward.  Forward is y = x W^T, dgrad dx = dy W, wgrad dW = dy^T x; each is one
-exact GEMM (rounded once to fp32).  With ``k_shards = s > 1`` every GEMM is
+det-train page, usage section: a DetLinear layer is deterministic in both the
+forward and the backward pass.  Forward is y = x W^T, dgrad dx = dy W, wgrad
+dW = dy^T x; each is one exact GEMM with a single rounding to fp32.  With ``k_shards = s > 1`` every GEMM is
 instead computed as s K-shard partials, one combine and one finalize, which the
 page's "Method" section says gives identical bytes.
 """

@@ -1,14 +1,13 @@
 /*
  * det_gemm.h -- C ABI of the exact-sum (Kulisch long-accumulator) GEMM.
  *
- * What the library computes (det-train page, section "Method"): each output
- * of C = A * B^T owns a fixed array of signed int64 digits of radix 2^32 that
- * spans the whole range of an fp32 x fp32 product.  Every bf16/f32 product is
- * formed exactly, its base-2^32 limbs are added into those digits with exact
- * integer additions, and the final digits are carry-normalised and rounded
- * ONCE to fp32 with round-to-nearest-even.  Integer addition is associative,
- * so the result does not depend on tiling, K-sharding, fold order or
- * repetition ("Sharded partials compose by adding digit arrays").
+ * What the library computes (det-train page, section "Method"): every output
+ * of C = A * B^T is the exact sum of its bf16/f32 products, kept as signed
+ * int64 digits of radix 2^32 wide enough for any fp32 x fp32 product, then
+ * carry-normalised and rounded to fp32 exactly once, to nearest with ties to
+ * even.  Integer addition is associative, so the result does not depend on
+ * tiling, K-sharding, fold order or repetition, and digit arrays of K-shards
+ * combine by plain addition.
  * The call names follow the page's usage section: det_gemm, det_gemm_partial,
  * det_combine, det_finalize, and the forward/dgrad/wgrad of DetLinear.
  *
@@ -99,7 +98,7 @@ int det_stage_report(const char** names, double* total_ms, int* counts, int max)
 
 /*
  * det_gemm -- C = RNE_f32( sum_k A(m,k) * B(n,k) ), computed exactly.
- * det-train page, usage section ("det_gemm(x, w)") and section "Method".
+ * det-train page, usage section (the det_gemm call) and section "Method".
  * Enqueues the exponent pre-pass and the accumulate kernel on `stream`; the
  * digits are never written to memory (finalize is fused).  A and B must be
  * aligned to their element size, C to 4 bytes.
@@ -112,8 +111,8 @@ det_status det_gemm(det_dtype dtype, int64_t M, int64_t N, int64_t K,
 /*
  * det_gemm_partial -- the same exact accumulation, written out unrounded as a
  * canonical digit array P [DET_PLANES][M][N] (8-byte aligned, contiguous,
- * M*N*160 bytes).  det-train page, usage section ("det_gemm_partial") and
- * section "Method" ("Sharded partials compose by adding digit arrays").
+ * M*N*160 bytes).  det-train page, usage section (the det_gemm_partial
+ * call) and section "Method" (partials of K-shards add up to the full sum).
  * Plane 18 is set to K.
  */
 det_status det_gemm_partial(det_dtype dtype, int64_t M, int64_t N, int64_t K,
@@ -124,7 +123,7 @@ det_status det_gemm_partial(det_dtype dtype, int64_t M, int64_t N, int64_t K,
 /*
  * det_combine -- out = sum_i parts[i], elementwise over all DET_PLANES planes,
  * then carry-normalised to canonical form.  det-train page, usage section
- * ("det_combine([a1, a2])") and section "Method".  `parts` is a HOST array of
+ * (the det_combine call) and section "Method".  `parts` is a HOST array of
  * n >= 1 device pointers, each to a [DET_PLANES][M][N] int64 array; `out` may
  * alias any of them.  Inputs need not be canonical, but the per-digit sums
  * must stay below 2^62 in magnitude (always true for up to DET_MAX_COMBINE
@@ -135,7 +134,7 @@ det_status det_combine(int64_t M, int64_t N, const int64_t* const* parts, int n,
 
 /*
  * det_finalize -- round a digit array once to fp32.  det-train page, usage
- * section ("det_finalize(acc)") and section "Method" (carry-normalise, round
+ * section (the det_finalize call) and section "Method" (carry-normalise, round
  * once, round-to-nearest-even).  P is [DET_PLANES][M][N] int64 with digits of
  * magnitude below 2^62; C is fp32 [M, N] with leading dimension ldc >= N.
  */
@@ -172,8 +171,8 @@ det_status det_gemm_partial_noalloc(det_dtype dtype, int64_t M, int64_t N, int64
                                     int64_t* P, void* stream);
 
 /*
- * DetLinear (det-train page, usage section: "DetLinear(4096, 4096)",
- * "y = layer(x); y.square().mean().backward()  # deterministic fwd and bwd").
+ * DetLinear (det-train page, usage section: a 4096 -> 4096 layer whose
+ * forward and backward passes are both deterministic).
  * Bias-free; every GEMM is an exact det_gemm:
  *   forward: y[b,o]  = sum_i x[b,i]  W[o,i]   x [batch,in], W [out,in], y [batch,out]
  *   dgrad:   dx[b,i] = sum_o dy[b,o] W[o,i]   dy [batch,out], dx [batch,in]

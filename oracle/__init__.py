@@ -7,8 +7,8 @@ never imports it and shares no code with it.
 The arithmetic lives in ``exact_oracle.cpp`` (plain C++, compiled with
 ``-ffp-contract=off``); this module only compiles it with g++ and marshals
 numpy arrays.  What it computes follows the det-train page, section "Method":
-each output is the exact sum of the exact fp64 products, rounded once to fp32
-with round-to-nearest-even.  Its pins (tests that tie it to something other
+each output is the exact sum of the exact products, given a single rounding
+to fp32 with round-to-nearest-even.  Its pins (tests that tie it to something other
 than itself) are in ``tests/test_oracle_pins.py``; no function here is
 "parity unpinned".
 """

@@ -4,9 +4,9 @@
 //
 // What it computes (det-train page, section "Method"): every output of a
 // bf16/f32 GEMM is the exact real sum of the exact fp64 products of its
-// inputs, rounded once to binary32 with round-to-nearest, ties-to-even.
-// The section "Correctness" restates it: "results carry the exact
-// fp64-product sum rounded once to fp32".
+// inputs, rounded a single time to binary32 with round-to-nearest,
+// ties-to-even.  The section "Correctness" states the same property of the
+// results.
 //
 // This is the plain definition written out, deliberately on a different
 // route from the GPU kernels:
@@ -31,8 +31,8 @@
 //     and any output with a nonzero count is the canonical NaN 0x7FC00000;
 //   * the canonical digit form of a sum is 18 digits of radix 2^32, digit j
 //     weighing 2^(32j-298); digits 0..16 lie in [0, 2^32) and digit 17 carries
-//     the sign.  (The pages say only "signed int64 digits in radix 2^32
-//     spanning the full fp32 product exponent range".)
+//     the sign.  (The pages fix only signed int64 digits of radix 2^32
+//     covering the whole range of fp32 product exponents.)
 //
 // Build: g++ -O2 -std=c++17 -ffp-contract=off -shared -fPIC -pthread.
 // Rows of the output are spread over std::threads; nothing else is clever.

@@ -3,8 +3,8 @@
 Every input comes from the seeded generators; every expected value from the
 oracle.  The det-train page's "Correctness" section sets the bar: full-K
 det_gemm equals the combine/finalize composition of 2/4/8/16-way K-shards in
-any fold grouping, bitwise, for bf16 and f32, and results carry the exact
-fp64-product sum rounded once to fp32.
+any fold grouping, bitwise, for bf16 and f32, and every output is the exact
+sum of the exact products with a single rounding to fp32.
 """
 import numpy as np
 import pytest

@@ -1,8 +1,8 @@
-"""The det-train page's training comparison: the same 160-step run computed
-unsharded and with every GEMM 4-way K-sharded (partials + combine + finalize).
-With exact GEMMs the per-step losses and the final weights are identical
-bytes; the page reports exactly zero difference at every step (usage text,
-"The same 160-step training run computed unsharded and 4-way K-sharded").
+"""The det-train page's training comparison: one 160-step run computed
+unsharded and again with every GEMM 4-way K-sharded (partials + combine +
+finalize).  With exact GEMMs the per-step losses and the final weights are
+identical bytes; the page reports a difference of exactly zero at every step
+(its usage section).
 
 Workload: a bias-free student MLP 1024 -> 4096 (ReLU) -> 1024 in f32, batch
 256, MSE against a fixed random teacher of the same shape (targets through

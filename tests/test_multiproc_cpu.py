@@ -1,9 +1,10 @@
 """World-size-2 tests on CPU (gloo): the multi-process logic of the benchmark
 and the det-train page's multi-rank claim, without any GPU.
 
-The page ("Correctness", "Real multi-GPU") reduces K-sharded partials across
-ranks with one int64 sum all-reduce of the long-accumulator digits, and every
-rank at world size 1 and 4 emits the identical result digest.  Here each rank
+The page (sections "Correctness" and "Real multi-GPU") sums K-sharded
+partials across ranks with a single int64 all-reduce of the accumulator
+digits, and reports the same result digest on every rank at world sizes 1
+and 4.  Here each rank
 computes the oracle's digits of its own K-shard, the digits are summed with a
 gloo all-reduce, and the canonical digits, the rounded result and its digest
 must equal the single-process ones on every rank.

@@ -1,9 +1,9 @@
 """Pins for the CPU oracle: tie it to things other than itself.
 
 Each test checks the oracle against something the det-train page or plain
-mathematics fixes (page section "Method": the exact fp64-product sum rounded
-once to fp32; section "Correctness": K-shard/fold invariance and the fp32
-rounding floor against an fp64 matmul):
+mathematics fixes (page section "Method": the exact sum of the exact products,
+rounded to fp32 a single time; section "Correctness": K-shard/fold invariance
+and the fp32 rounding floor against an fp64 matmul):
   * exact-rational brute force on tiny inputs (fractions.Fraction);
   * the small-integer special case (exact int64 GEMM + one RNE cast);
   * K = 1, which is one RNE of an exact double (numpy's cast);
