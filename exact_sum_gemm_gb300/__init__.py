@@ -23,7 +23,8 @@ from ._native import (DET_BF16, DET_DIGITS, DET_F32, DET_K_MAX, DET_MAX_COMBINE,
 
 __all__ = [
     "det_gemm", "det_gemm_partial", "det_combine", "det_finalize", "det_gemm_sharded",
-    "det_linear_forward", "det_linear_dgrad", "det_linear_wgrad", "DetLinear",
+    "det_gemm_batched", "det_linear_forward", "det_linear_forward_bias", "det_linear_dgrad",
+    "det_linear_wgrad", "det_linear_bias_grad", "DetLinear",
     "DetError", "DET_DIGITS", "DET_PLANES", "DET_K_MAX", "DET_MAX_COMBINE", "library",
 ]
 
@@ -223,6 +224,81 @@ def det_linear_wgrad(dy, x):
                                             dW.data_ptr(), _stream(dy))
     _native.check("det_linear_wgrad", st)
     return dW
+
+
+def det_linear_forward_bias(x, W, bias):
+    """y = x W^T + bias, the bias summed exactly with the products and rounded once."""
+    torch = _torch()
+    B, d_in = x.shape
+    d_out = W.shape[0]
+    _linear_check(W, "W", (d_out, d_in), x.dtype)
+    _linear_check(x, "x", (B, d_in))
+    _linear_check(bias, "bias", (d_out,), x.dtype)
+    y = torch.empty((B, d_out), dtype=torch.float32, device=x.device)
+    with torch.cuda.device(x.device):
+        st = _native.lib().det_linear_forward_bias(_dtype_code(x), B, d_in, d_out, x.data_ptr(),
+                                                   W.data_ptr(), bias.data_ptr(), y.data_ptr(),
+                                                   _stream(x))
+    _native.check("det_linear_forward_bias", st)
+    return y
+
+
+def det_linear_bias_grad(dy):
+    """db = column sums of dy [B, out], exact (fp32)."""
+    torch = _torch()
+    B, d_out = dy.shape
+    _linear_check(dy, "dy", (B, d_out), torch.float32)
+    db = torch.empty((d_out,), dtype=torch.float32, device=dy.device)
+    with torch.cuda.device(dy.device):
+        st = _native.lib().det_linear_bias_grad(B, d_out, dy.data_ptr(), db.data_ptr(), _stream(dy))
+    _native.check("det_linear_bias_grad", st)
+    return db
+
+
+def _batch_operand(t, name, batch, K):
+    """(tensor, ld, op, batch stride) for [batch, rows, K] (or a shared [rows, K])."""
+    if t.dim() == 2:
+        a, ld, op = _operand(t, name)
+        return a, ld, op, 0
+    if t.dim() != 3 or t.shape[0] != batch or t.shape[2] != K:
+        raise ValueError(f"{name} must be [{batch}, rows, {K}] or [rows, {K}], got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if batch > 0:
+        a, ld, op = _operand(t[0], name)
+        if a.data_ptr() != t[0].data_ptr():            # unsupported inner strides: copy once
+            t = t.contiguous()
+            a, ld, op = _operand(t[0], name)
+    else:
+        ld, op = max(K, 1), 0
+    return t, ld, op, t.stride(0)
+
+
+def det_gemm_batched(x, w, out=None):
+    """y[b] = RNE_f32(x[b] @ w[b].T) for each b; x [B,M,K], w [B,N,K] or a shared [N,K]."""
+    torch = _torch()
+    if x.dim() != 3:
+        raise ValueError(f"x must be [batch, M, K], got {tuple(x.shape)}")
+    batch, M, K = x.shape
+    if w.dtype != x.dtype or w.device != x.device:
+        raise ValueError("x and w must share dtype and device")
+    dt = _dtype_code(x)
+    a, lda, opa, sa = _batch_operand(x, "x", batch, K)
+    b, ldb, opb, sb = _batch_operand(w, "w", batch, K)
+    N = w.shape[-2]
+    if out is None:
+        out = torch.empty((batch, M, N), dtype=torch.float32, device=x.device)
+    elif (out.shape != (batch, M, N) or out.dtype != torch.float32 or out.stride(2) != 1
+          or (M > 1 and out.stride(1) < N)):
+        raise ValueError("out must be a float32 [batch,M,N] tensor with unit column stride")
+    if batch == 0 or M == 0 or N == 0:
+        return out
+    with torch.cuda.device(x.device):
+        st = _native.lib().det_gemm_strided_batched(
+            dt, batch, M, N, K, a.data_ptr(), lda, opa, sa, b.data_ptr(), ldb, opb, sb,
+            out.data_ptr(), max(out.stride(1), N), out.stride(0), _stream(x))
+    _native.check("det_gemm_strided_batched", st)
+    return out
 
 
 def __getattr__(name):

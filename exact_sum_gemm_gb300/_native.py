@@ -44,6 +44,10 @@ SIGNATURES = {
     "det_linear_forward": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "det_linear_dgrad": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "det_linear_wgrad": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
+    "det_linear_forward_bias": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
+    "det_linear_bias_grad": (_i32, [_i64, _i64, _vp, _vp, _vp]),
+    "det_gemm_strided_batched": (_i32, [_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp,
+                                        _i64, _i32, _i64, _vp, _i64, _i64, _vp]),
 }
 
 _lock = threading.Lock()

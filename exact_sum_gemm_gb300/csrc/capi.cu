@@ -190,4 +190,64 @@ det_status det_linear_wgrad(int64_t batch, int64_t in_features, int64_t out_feat
                   1, dW, in_features, stream);
 }
 
+det_status det_gemm_strided_batched(det_dtype dtype, int64_t batch, int64_t M, int64_t N,
+                                    int64_t K, const void* A, int64_t lda, int opA,
+                                    int64_t strideA, const void* B, int64_t ldb, int opB,
+                                    int64_t strideB, float* C, int64_t ldc, int64_t strideC,
+                                    void* stream) {
+  det_status s = validate_gemm(dtype, M, N, K, A, lda, opA, B, ldb, opB);
+  if (s != DET_OK) return s;
+  if (batch < 0 || strideA < 0 || strideB < 0 || strideC < 0) return DET_ERR_SHAPE;
+  if (batch == 0 || M == 0 || N == 0) return DET_OK;
+  if (C == nullptr || ldc < N) return DET_ERR_INVALID_ARG;
+  if (!aligned(C, 4)) return DET_ERR_ALIGNMENT;
+  const int64_t last = batch - 1;
+  if ((strideA > 0 && last > INT64_MAX / 8 / strideA) || (strideB > 0 && last > INT64_MAX / 8 / strideB) ||
+      (strideC > 0 && last > INT64_MAX / 8 / strideC))
+    return DET_ERR_SHAPE;
+  const int64_t es = dtype == DET_F32 ? 4 : 2;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int64_t b = 0; b < batch; ++b) {
+    const void* Ab = static_cast<const char*>(A) + b * strideA * es;
+    const void* Bb = static_cast<const char*>(B) + b * strideB * es;
+    det::GemmArgs a = make_args(dtype, M, N, K, Ab, lda, opA, Bb, ldb, opB);
+    a.C = C + b * strideC;
+    a.ldc = ldc;
+    const det_status r = from_cuda(det::launch_gemm(a, st));
+    if (r != DET_OK) return r;
+  }
+  return DET_OK;
+}
+
+det_status det_linear_forward_bias(det_dtype dtype, int64_t batch, int64_t in_features,
+                                   int64_t out_features, const void* x, const void* W,
+                                   const void* bias, float* y, void* stream) {
+  if (bias == nullptr)
+    return det_linear_forward(dtype, batch, in_features, out_features, x, W, y, stream);
+  if (in_features < 0 || in_features + 1 > DET_K_MAX) return in_features < 0 ? DET_ERR_SHAPE
+                                                                             : DET_ERR_K_LIMIT;
+  det_status s = validate_gemm(dtype, batch, out_features, in_features + 1, x, in_features + 1 > 1
+                               ? in_features + 1 : 1, 0, W, in_features + 1, 0);
+  if (s != DET_OK) return s;
+  if (batch == 0 || out_features == 0) return DET_OK;
+  if (x == nullptr || W == nullptr || y == nullptr) return DET_ERR_INVALID_ARG;
+  const uintptr_t es = dtype == DET_F32 ? 4 : 2;
+  if (!aligned(bias, es) || !aligned(y, 4)) return DET_ERR_ALIGNMENT;
+  return from_cuda(det::launch_linear_bias(dtype == DET_BF16 ? 1 : 0, batch, in_features,
+                                           out_features, x, W, bias, y,
+                                           static_cast<cudaStream_t>(stream)));
+}
+
+det_status det_linear_bias_grad(int64_t batch, int64_t out_features, const float* dy, float* db,
+                                void* stream) {
+  if (batch < 0 || out_features < 0) return DET_ERR_SHAPE;
+  if (batch > DET_K_MAX) return DET_ERR_K_LIMIT;
+  if (out_features > (int64_t(1) << 31)) return DET_ERR_SHAPE;
+  if (out_features == 0) return DET_OK;
+  if (db == nullptr || (batch > 0 && dy == nullptr)) return DET_ERR_INVALID_ARG;
+  if (!aligned(db, 4) || !aligned(dy, 4)) return DET_ERR_ALIGNMENT;
+  return from_cuda(det::launch_bias_grad(batch, out_features, dy, db,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

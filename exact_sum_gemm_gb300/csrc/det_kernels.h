@@ -45,6 +45,20 @@ struct GemmArgs {
 // Exact GEMM; writes C (if args.C) or the digit planes P (if args.P).
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 
+// Stream-ordered scratch from the library's memory pool (one per device, kept
+// reserved between calls); release with cudaFreeAsync on the same stream.
+cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream);
+
+// y = RNE_f32(x W^T + bias): the bias enters as one more exact product,
+// 1 * bias[o], through [x | 1] and [W | bias] built in pool scratch.
+// x [rows, in], W [out, in], bias [out] contiguous, all of one dtype.
+cudaError_t launch_linear_bias(int bf16, int64_t rows, int64_t in, int64_t out, const void* x,
+                               const void* W, const void* bias, float* y, cudaStream_t stream);
+
+// db[o] = RNE_f32(sum_r dy[r, o]) exactly (dy fp32 [rows, out]).
+cudaError_t launch_bias_grad(int64_t rows, int64_t out, const float* dy, float* db,
+                             cudaStream_t stream);
+
 constexpr int kMaxPartsPerLaunch = 16;
 
 // out = canonical(sum of parts), over count = M*N outputs of 20 planes each.

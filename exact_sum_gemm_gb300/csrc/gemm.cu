@@ -108,14 +108,14 @@ cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slot
   return launch_kulisch(g, s.general, stream);
 }
 
-namespace {
-
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream) {
   cudaMemPool_t pool;
   cudaError_t e = device_pool(&pool);
   if (e != cudaSuccess) return e;
   return cudaMallocFromPoolAsync(p, bytes, pool, stream);
 }
+
+namespace {
 
 cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
   const int64_t slots = band_slots(g);

@@ -187,6 +187,47 @@ det_status det_linear_dgrad(int64_t batch, int64_t in_features, int64_t out_feat
 det_status det_linear_wgrad(int64_t batch, int64_t in_features, int64_t out_features,
                             const float* dy, const float* x, float* dW, void* stream);
 
+/*
+ * det_linear_forward_bias -- y[b,o] = RNE_f32( sum_i x[b,i] W[o,i] + bias[o] ),
+ * the bias being one more exact term of the same sum, rounded with it once.
+ * The det-train page shows a bias-free layer; this is its bias-carrying form:
+ * the product 1 * bias[o] joins the exact accumulation, so the result keeps
+ * every invariance of det_gemm.  bias [out] is contiguous and has the dtype
+ * of x and W (a null bias is det_linear_forward).  Needs in + 1 <= DET_K_MAX.
+ * Scratch: (batch + out) * (in + 1) elements from the library's memory pool
+ * for the widened operands [x | 1] and [W | bias], released on `stream`.
+ */
+det_status det_linear_forward_bias(det_dtype dtype, int64_t batch, int64_t in_features,
+                                   int64_t out_features, const void* x, const void* W,
+                                   const void* bias, float* y, void* stream);
+
+/*
+ * det_linear_bias_grad -- db[o] = RNE_f32( sum_b dy[b,o] ), exact (the
+ * gradient of the bias term above).  dy fp32 [batch, out] contiguous, db fp32
+ * [out]; batch <= DET_K_MAX.  Scratch: batch floats from the memory pool.
+ */
+det_status det_linear_bias_grad(int64_t batch, int64_t out_features, const float* dy, float* db,
+                                void* stream);
+
+/*
+ * det_gemm_strided_batched -- `batch` independent exact GEMMs,
+ *   C_b = RNE_f32( A_b * B_b^T ),  b = 0 .. batch-1,
+ * with A_b = A + b * strideA, B_b = B + b * strideB (in elements of the
+ * operand dtype) and C_b = C + b * strideC (floats); every matrix uses the
+ * layout rules of det_gemm (lda/opA, ldb/opB, ldc).  A stride of 0 shares
+ * one operand across the batch.  The det-train page has no batched call; it
+ * names reproducible training under sequence parallelism among its
+ * references (section "References"), whose per-head attention products are
+ * batches of small independent GEMMs.  Each C_b is bitwise the det_gemm of
+ * its operands.  The C_b must not overlap.  Negative strides return
+ * DET_ERR_SHAPE.  Entries are enqueued one after another on `stream`.
+ */
+det_status det_gemm_strided_batched(det_dtype dtype, int64_t batch, int64_t M, int64_t N,
+                                    int64_t K, const void* A, int64_t lda, int opA,
+                                    int64_t strideA, const void* B, int64_t ldb, int opB,
+                                    int64_t strideB, float* C, int64_t ldc, int64_t strideC,
+                                    void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -68,6 +68,18 @@ def test_host_side_validation_without_gpu():
     assert lib.det_finalize(2, 2, 8, 4, 1, S) == 1                           # ldc < N
     assert lib.det_finalize(2, 2, 12, 4, 2, S) == 6
     assert lib.det_linear_wgrad((1 << 19) + 1, 4, 4, 4, 4, 4, S) == 4        # K = batch
+    # batched: negative batch or stride, bad shared argument; batch 0 is a no-op
+    assert lib.det_gemm_strided_batched(0, -1, 2, 2, 4, 4, 4, 0, 8, 4, 4, 0, 8, 4, 2, 4, S) == 3
+    assert lib.det_gemm_strided_batched(0, 2, 2, 2, 4, 4, 4, 0, -8, 4, 4, 0, 8, 4, 2, 4, S) == 3
+    assert lib.det_gemm_strided_batched(0, 2, 2, 2, 4, 4, 3, 0, 8, 4, 4, 0, 8, 4, 2, 4, S) == 1
+    assert lib.det_gemm_strided_batched(0, 0, 2, 2, 4, 4, 4, 0, 8, 4, 4, 0, 8, 4, 2, 4, S) == 0
+    assert lib.det_gemm_strided_batched(0, 3, 2, 2, 4, 4, 4, 0, 8, 4, 4, 0, 8, 6, 2, 4, S) == 6
+    # bias: the widened K (in + 1) must stay within the per-call limit
+    assert lib.det_linear_forward_bias(0, 2, 1 << 19, 2, 4, 4, 4, 4, S) == 4
+    assert lib.det_linear_forward_bias(0, 2, 4, 2, 4, 4, 6, 4, S) == 6       # misaligned bias
+    assert lib.det_linear_bias_grad((1 << 19) + 1, 4, 4, 4, S) == 4          # K = batch
+    assert lib.det_linear_bias_grad(4, -1, 4, 4, S) == 3
+    assert lib.det_linear_bias_grad(4, 4, 4, 6, S) == 6                      # misaligned db
 
 
 def test_python_layer_rejects_host_tensors():

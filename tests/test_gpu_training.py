@@ -87,3 +87,68 @@ def test_plain_fp32_training_is_not_shard_invariant():
     exact_split = dg.det_gemm_sharded(x, w, wl.equal_cuts(4096, 4))
     assert torch.equal(exact_full.view(torch.int32), exact_split.view(torch.int32))
     assert not torch.equal(full, split)
+
+
+def _train_variant(steps, cuts, bias):
+    """The student MLP with optional biases; cuts=None computes every GEMM unsharded."""
+    dev = torch.device("cuda")
+    w1, w2 = wl.mlp_init(stream=0)
+    t1, t2 = wl.mlp_init(stream=1)
+    g = np.random.default_rng(99)
+    b1 = torch.from_numpy((g.standard_normal(4096) * 2.0 ** -5).astype(np.float32)) if bias else None
+    b2 = torch.from_numpy((g.standard_normal(1024) * 2.0 ** -5).astype(np.float32)) if bias else None
+    kw = dict(device=dev, cuts=cuts, k_shards=2 if cuts else 1)
+    l1 = dg.DetLinear(1024, 4096, weight=torch.from_numpy(w1), bias=b1 if bias else False, **kw)
+    l2 = dg.DetLinear(4096, 1024, weight=torch.from_numpy(w2), bias=b2 if bias else False, **kw)
+    t1d, t2d = torch.from_numpy(t1).to(dev), torch.from_numpy(t2).to(dev)
+    lr = torch.tensor(LR, dtype=torch.float32, device=dev)
+    params = [p for p in l1.parameters()] + [p for p in l2.parameters()]
+    losses = []
+    for step in range(steps):
+        x = torch.from_numpy(wl.mlp_batch(step)).to(dev)
+        with torch.no_grad():
+            target = dg.det_gemm(_relu(dg.det_gemm(x, t1d)), t2d)
+        loss = (l2(_relu(l1(x))) - target).square().mean()
+        for p in params:
+            p.grad = None
+        loss.backward()
+        with torch.no_grad():
+            for p in params:
+                p.sub_(p.grad * lr)
+        losses.append(loss.detach().clone())
+    return torch.stack(losses), [p.detach().clone() for p in params]
+
+
+@pytest.mark.parametrize("shards", [2, 8, 16])
+def test_training_with_bias_and_random_cuts_is_bitwise_identical(shards):
+    # every GEMM of the run (forward, dgrad, wgrad, bias gradient) split at
+    # random cut points, empty shards allowed; the biases enter as one more
+    # exact term of each forward sum
+    steps = 10
+    cuts = lambda K: wl.kshard_cuts(K, shards, seed=K + shards)
+    loss_a, par_a = _train_variant(steps, None, True)
+    loss_b, par_b = _train_variant(steps, cuts, True)
+    assert torch.equal(loss_a.view(torch.int32), loss_b.view(torch.int32))
+    for pa, pb in zip(par_a, par_b):
+        assert torch.equal(pa.view(torch.int32), pb.view(torch.int32))
+    assert torch.isfinite(loss_a).all() and float(loss_a[-1]) < float(loss_a[0])
+
+
+def test_partials_saved_mid_step_and_resumed(tmp_path):
+    # half of a GEMM's K-shard partials are computed, written to disk and the
+    # device copies dropped; after reloading, the rest are computed and the
+    # combine gives the same bytes as the uninterrupted computation
+    x = torch.from_numpy(wl.mlp_batch(0)).cuda()
+    w1, _ = wl.mlp_init(stream=0)
+    w = torch.from_numpy(w1).cuda()
+    cuts = wl.kshard_cuts(1024, 6, seed=5)
+    full = dg.det_gemm(x, w)
+    first = [dg.det_gemm_partial(x[:, k0:k1], w[:, k0:k1]) for k0, k1 in cuts[:3]]
+    path = tmp_path / "partials.pt"
+    torch.save([p.cpu() for p in first], path)
+    del first
+    torch.cuda.synchronize()
+    resumed = [p.cuda() for p in torch.load(path)]
+    resumed += [dg.det_gemm_partial(x[:, k0:k1], w[:, k0:k1]) for k0, k1 in cuts[3:]]
+    y = dg.det_finalize(dg.det_combine(resumed))
+    assert torch.equal(y.view(torch.int32), full.view(torch.int32))
