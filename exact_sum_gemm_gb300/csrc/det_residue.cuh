@@ -117,6 +117,7 @@ struct ReconArgs {
   const int* colslot;         // [N]: a deep column's slot in the deep-column list, else -1
   ulonglong2* sbuf;           // [M][slots]: shallow sums S of deep-column outputs (lo, hi)
   int slots;                  // slots kept in sbuf; columns in later slots re-read residues
+  int64_t m_begin, m_end;     // rows of C handled by this launch (a band)
 };
 
 // Deep columns whose shallow sums are passed from the fast reconstruction to
@@ -139,7 +140,8 @@ struct ResGemmArgs {
   const __nv_bfloat16* B;     // [N/32][Kp/64][nplanes][32][64]
   int64_t M, N, Kp;
   int nplanes;
-  int8_t* res;                // [nplanes][M][N] balanced residues
+  int8_t* res;                // [nplanes][.][N] balanced residues: plane u of row m at
+  int64_t res_plane;          //   res + u * res_plane + m * N
   int* error;
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);

@@ -155,8 +155,59 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   return r;
 }
 
+// Banded schedule.  C is cut into row bands; band b's tensor-core GEMM runs on
+// a high-priority library stream while the caller's stream computes the next
+// band's A residue planes and the previous band's reconstruction, so the
+// CUDA-core stages overlap the tensor-core kernel.  Only stream order and
+// events connect the two streams (no kernel waits on another).
+constexpr int kMaxBands = 4;
+
+struct BandSync {
+  cudaStream_t hi = nullptr;                       // tensor-core launches
+  cudaEvent_t planes_done[kMaxBands] = {};         // caller's stream -> hi
+  cudaEvent_t gemm_done[kMaxBands] = {};           // hi -> caller's stream
+};
+std::mutex g_band_mu[kMaxDevices];
+BandSync g_band[kMaxDevices];
+
+cudaError_t band_sync(int dev, BandSync** out) {
+  BandSync& b = g_band[dev];
+  if (b.hi == nullptr) {
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&b.hi, cudaStreamNonBlocking, greatest);
+    for (int i = 0; i < kMaxBands && e == cudaSuccess; ++i) {
+      e = cudaEventCreateWithFlags(&b.planes_done[i], cudaEventDisableTiming);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b.gemm_done[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) {
+      b.hi = nullptr;
+      return e;
+    }
+  }
+  *out = &b;
+  return cudaSuccess;
+}
+
+// Rows per band: whole 128-row tiles; two bands once each half still fills
+// the GPU with tensor-core work.
+int64_t band_rows(const GemmArgs& g) {
+  if (g.M < 2048) return g.M;
+  return (g.M / 2 + 127) / 128 * 128;
+}
+
 cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch& L, int nplanes,
                              int64_t Kp, int cap, cudaStream_t stream) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_band_mu[dev]);     // the streams and events are shared
+  BandSync* bs = nullptr;
+  e = band_sync(dev, &bs);
+  if (e != cudaSuccess) return e;
+  const cudaStream_t hi = bs->hi;
+
   const Scratch s = carve_scratch(base, g, 0);
   int* counts = reinterpret_cast<int*>(base + L.off_counts);
   int* error = counts + g.M + g.N;
@@ -166,8 +217,11 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
   int8_t* res = reinterpret_cast<int8_t*>(base + L.off_res);
   int* deep_rows = reinterpret_cast<int*>(base + L.off_deep_idx);   // [M] rows, then [N] columns
+  const int64_t H = band_rows(g);
+  const int nb = static_cast<int>((g.M + H - 1) / H);
+  const int64_t nkb = Kp / kStageK;
+  const size_t es = g.bf16 ? 2 : 4;
 
-  cudaError_t e;
   {
     StageScope t(kStagePrepass, stream);
     e = launch_emax(g, s, stream);
@@ -175,33 +229,64 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
       e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 3), stream);
   }
   if (e != cudaSuccess) return e;
+  // the residue kernels' deep-list counters double as the rows' deep counts,
+  // from which the tiles are routed
+  auto planes_of_band = [&](int b) {
+    const int64_t m0 = b * H, rows = (g.M - m0) < H ? g.M - m0 : H;
+    const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
+    ResidueOperand ra{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
+                      planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
+                      counts + m0, listA + m0 * cap, cap};
+    return launch_residues(ra, g.bf16, nplanes, stream);
+  };
+  auto gemm_of_band = [&](int b) {
+    const int64_t m0 = b * H, rows = (g.M - m0) < H ? g.M - m0 : H;
+    StageScope t(kStageResidueGemm, hi);
+    ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
+                   rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error};
+    return launch_residue_gemm(rg, hi);
+  };
   {
-    // residue planes; the deep-list counters double as the rows' deep counts,
-    // from which the tiles are routed
     StageScope t(kStageResiduePlanes, stream);
-    ResidueOperand ra{g.A, g.lda, g.opA, g.M, g.K, Kp, s.emaxA, planesA, counts, listA, cap};
     ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
-    e = launch_residues(ra, g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = launch_residues(rb, g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M,
-                                               error + 1, stream);
+    e = launch_residues(rb, g.bf16, nplanes, stream);
+    if (e == cudaSuccess) e = planes_of_band(0);
   }
-  if (e != cudaSuccess) return e;
-  {
-    StageScope t(kStageResidueGemm, stream);
-    ResGemmArgs rg{planesA, planesB, g.M, g.N, Kp, nplanes, res, error};
-    e = launch_residue_gemm(rg, stream);
+  if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[0], stream);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, bs->planes_done[0], 0);
+  if (e == cudaSuccess) e = gemm_of_band(0);
+  if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[0], hi);
+  for (int b = 1; b < nb && e == cudaSuccess; ++b) {
+    {
+      StageScope t(kStageResiduePlanes, stream);
+      e = planes_of_band(b);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[b], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, bs->planes_done[b], 0);
+    if (e == cudaSuccess) e = gemm_of_band(b);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[b], hi);
   }
-  if (e != cudaSuccess) return e;
-  {
+  if (e == cudaSuccess) {
+    StageScope t(kStageResiduePlanes, stream);
+    e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M, error + 1, stream);
+  }
+  for (int b = 0; b < nb && e == cudaSuccess; ++b) {
+    e = cudaStreamWaitEvent(stream, bs->gemm_done[b], 0);
+    if (e != cudaSuccess) break;
     StageScope t(kStageReconstruct, stream);
+    const int64_t m0 = b * H, m1 = (g.M - m0) < H ? g.M : m0 + H;
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
                  error, deep_rows + g.M + g.N, reinterpret_cast<ulonglong2*>(base + L.off_sbuf),
-                 deep_col_slots(g.N)};
+                 deep_col_slots(g.N), m0, m1};
     // deep-row/column lists, and their two counters right after the error flag
     e = launch_reconstruct(g, rc, deep_rows, error + 1, stream);
   }
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess) {
+    // keep the caller's stream ordered after everything enqueued on hi
+    cudaEvent_t join = bs->gemm_done[0];
+    if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
+    return e;
+  }
   StageScope t(kStageGeneral, stream);
   return launch_kulisch(g, s.general, stream);
 }

@@ -223,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     const int g = warp & 3;                // TMEM lanes 32g .. 32g+31
-    const int64_t MN = a.M * a.N;
     bool ok = true;
     uint32_t uses[2] = {0u, 0u};
     for (int64_t unit = blockIdx.x; unit < units && ok; unit += gridDim.x) {
@@ -261,7 +260,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (row < a.M) {
           // a second reduction makes the residue balanced (|r| <= 127); its
           // byte is the low byte of the pattern of r + 1.5*2^23
-          int8_t* out = a.res + u * MN + row * a.N + n0 + cb * 32;
+          int8_t* out = a.res + u * a.res_plane + row * a.N + n0 + cb * 32;
           uint32_t packed[8];
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {

@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
   const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
   const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
                       (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
-  for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
+  for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
     if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
     if (ra.countA[m] != 0) continue;                              // deep row: full kernel
     int emA = ra.emaxA[m];
@@ -674,17 +674,20 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;
   const int64_t n_rows = nrc[0], n_cols = nrc[1];
-  const int64_t part1 = n_rows * g.N, total = part1 + g.M * n_cols;
+  const int64_t band = ra.m_end - ra.m_begin;
+  const int64_t part1 = n_rows * g.N, total = part1 + band * n_cols;
   for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * kThreads) {
     int64_t m, n, slot = -1;
     if (idx < part1) {
       m = rows[idx / g.N];
+      if (m < ra.m_begin || m >= ra.m_end) continue;              // another band's row
       n = idx - (idx / g.N) * g.N;
     } else {
       const int64_t j = idx - part1;
-      m = j / n_cols;
-      slot = j - m * n_cols;
+      const int64_t mb = j / n_cols;
+      slot = j - mb * n_cols;
+      m = ra.m_begin + mb;
       n = cols[slot];
       if (ra.countA[m] != 0) continue;                          // done with its deep row
     }
@@ -738,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
   if (col_deep && (slot < 0 || slot >= ra.slots)) return;     // ... re-reading the residues
   int emB = ra.emaxB[n];
   emB = emB == kEmaxEmpty ? 0 : emB;
-  for (int64_t m = blockIdx.y; m < g.M; m += gridDim.y) {
+  for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
     if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's outputs
     if (ra.countA[m] != 0) continue;                            // deep row: deep kernel
     int emA = ra.emaxA[m];
@@ -815,12 +818,14 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
   const int64_t MN = g.M * g.N;
   if (MN == 0) return cudaSuccess;
   const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
+  const int64_t band = ra.m_end - ra.m_begin;
+  if (band <= 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
-            static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
+            static_cast<unsigned>(band < 65535 ? band : 65535));
   cudaError_t e;
   if (g.P != nullptr) {
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
-               static_cast<unsigned>(g.M < 65535 ? g.M : 65535));
+               static_cast<unsigned>(band < 65535 ? band : 65535));
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
       partial_fast_kernel<decltype(B)::value, decltype(P)::value><<<pgrid, kThreads, 0, stream>>>(g, ra);
       return cudaSuccess;
