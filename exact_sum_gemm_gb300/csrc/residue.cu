@@ -132,6 +132,84 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
   }
 }
 
+// Four neighbouring elements' residues: plane i gets one 8-byte word of four
+// bf16 values, one 32 x 64 block (4 KB, 512 8-byte words) after plane i - 1.
+template <int i, int P>
+__device__ __forceinline__ void write_residue_quads(uint2* dst, const float (&x)[4],
+                                                    const float (&pw)[4]) {
+  if constexpr (i < P) {
+    constexpr int p = modulus(i);
+    dst[i * (kPlaneRows * kStageK / 4)] =
+        make_uint2(bf16_pair(residue_f32<p>(x[0], pw[0]), residue_f32<p>(x[1], pw[1])),
+                   bf16_pair(residue_f32<p>(x[2], pw[2]), residue_f32<p>(x[3], pw[3])));
+    write_residue_quads<i + 1, P>(dst, x, pw);
+  }
+}
+
+// The residue kernel for K-contiguous operands (op 0) whose rows start on a
+// vector boundary: no shared-memory staging.  A block covers one group of 32
+// rows x one 64-k stage; each thread takes two runs of 4 neighbouring k
+// (one 16-byte f32 or 8-byte bf16 load each) and writes each plane as one
+// 8-byte word, so a half-warp stores one 128-byte plane row.
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o) {
+  const int tid = threadIdx.x;
+  const int64_t r0 = int64_t(blockIdx.y) * kTileRows;
+  const int64_t k0 = int64_t(blockIdx.x) * kTileK;
+  const int64_t nkb = o.Kp / kStageK;
+#pragma unroll 1
+  for (int u = 0; u < kTileRows * kTileK / (4 * kThreads); ++u) {
+    const int idx = tid + u * kThreads;
+    const int r = idx >> 4, kq = (idx & 15) * 4;
+    const int64_t gr = r0 + r, gk = k0 + kq;
+    uint32_t bits[4] = {0u, 0u, 0u, 0u};
+    int em = 0;
+    if (gr < o.rows) {
+      em = o.emax[gr];
+      em = em == kEmaxEmpty ? 0 : em;
+      if (gk + 4 <= o.K) {
+        if (kBf16) {
+          const uint2 v = __ldg(reinterpret_cast<const uint2*>(
+              static_cast<const uint16_t*>(o.X) + gr * o.ld + gk));
+          bits[0] = v.x << 16;
+          bits[1] = v.x & 0xFFFF0000u;
+          bits[2] = v.y << 16;
+          bits[3] = v.y & 0xFFFF0000u;
+        } else {
+          const uint4 v = __ldg(reinterpret_cast<const uint4*>(
+              static_cast<const uint32_t*>(o.X) + gr * o.ld + gk));
+          bits[0] = v.x;
+          bits[1] = v.y;
+          bits[2] = v.z;
+          bits[3] = v.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          if (gk + h < o.K) bits[h] = load_bits<kBf16>(o.X, gr * o.ld + gk + h);
+      }
+    }
+    float x[4], pw[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const Decoded d = decode_f32_bits(bits[h]);
+      const int s = d.e - em + kDeepGap;
+      const bool deep = d.nonfinite || (d.m != 0 && s < 0);
+      const int32_t mi = kBf16 ? (d.m >> 16) : d.m;   // bf16: drop the 16 zero bits
+      x[h] = static_cast<float>(deep ? 0 : mi);
+      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);
+      if (deep && gk + h < o.K && gr < o.rows) {
+        const int slot = atomicAdd(o.list_count + gr, 1);
+        if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits[h]);
+      }
+    }
+    uint2* dst = reinterpret_cast<uint2*>(
+        o.planes + (int64_t(blockIdx.y) * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
+        r * kStageK + kq);
+    write_residue_quads<0, P>(dst, x, pw);
+  }
+}
+
 // ---------------------------------------------------------------- reconstruction
 //
 // Per output (m, n) on a residue-path tile:
@@ -804,8 +882,16 @@ cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cuda
   if (o.rows == 0 || o.Kp == 0) return cudaSuccess;
   dim3 grid(static_cast<unsigned>((o.Kp + kTileK - 1) / kTileK),
             static_cast<unsigned>((o.rows + kTileRows - 1) / kTileRows));
+  // vector loads: K-contiguous rows whose every row start is 16-byte (f32) or
+  // 8-byte (bf16) aligned
+  const uintptr_t vec = bf16 ? 8 : 16;
+  const bool rows_ok = o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
+                       (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
   const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
-    residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
+    if (rows_ok)
+      residue_rows_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
+    else
+      residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;

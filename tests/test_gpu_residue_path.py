@@ -116,3 +116,27 @@ def test_many_deep_columns_and_rows(oracle_mod):
     a, b = dev_f32(A), dev_f32(B)
     assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, "many deep rows and columns")
     np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B))
+
+
+def test_vector_rows_with_ragged_k_tail(oracle_mod):
+    # rows padded to a 16-byte multiple (the vector-load residue kernel) with
+    # K = 1001, so the last run of four k crosses the end of the row
+    M, N, K, ld = 70, 90, 1001, 1004
+    A = wl.normal_f32((M, K), 43, 0)
+    B = wl.normal_f32((N, K), 43, 1)
+    A[2, 1000] = np.float32(3e-9)                # deep element in the tail
+    pa = np.zeros((M, ld), np.float32)
+    pb = np.zeros((N, ld), np.float32)
+    pa[:, :K] = A
+    pb[:, :K] = B
+    pa[:, K:] = np.float32(np.nan)               # padding must never be read
+    pb[:, K:] = np.float32(np.nan)
+    a = dev_f32(pa)[:, :K]
+    b = dev_f32(pb)[:, :K]
+    want = np_bits(oracle_mod.gemm(A, B))
+    assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, "vector rows, ragged K")
+    abf = (pa.view(np.uint32) >> 16).astype(np.uint16)     # bf16 rows: 2008-byte stride
+    bbf = (pb.view(np.uint32) >> 16).astype(np.uint16)
+    want16 = np_bits(oracle_mod.gemm(abf[:, :K], bbf[:, :K], dtype="bf16"))
+    got16 = dg.det_gemm(dev_bf16(abf)[:, :K], dev_bf16(bbf)[:, :K])
+    assert_bits_equal(bits_of(got16), want16, "bf16 vector rows, ragged K")
