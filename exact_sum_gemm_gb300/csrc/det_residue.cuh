@@ -145,5 +145,8 @@ struct ResGemmArgs {
   int* error;
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
+// The same GEMM with 256 x 256 tiles over CTA pairs (cta_group::2); returns
+// cudaErrorNotSupported (nothing enqueued) where clusters of two cannot run.
+cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream);
 
 }  // namespace det

@@ -244,6 +244,12 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageResidueGemm, hi);
     ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
                    rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error};
+    // 256 x 256 tiles on CTA pairs, unless a single 128-row tile covers M or
+    // the device cannot run clusters of two
+    if (rows > 128) {
+      const cudaError_t ep = launch_residue_gemm_pair(rg, hi);
+      if (ep != cudaErrorNotSupported) return ep;
+    }
     return launch_residue_gemm(rg, hi);
   };
   {

@@ -299,6 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) ptx::tmem_dealloc(tmem_base, kTmemCols);
 }
 
+}  // namespace
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static std::mutex mu;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -339,8 +341,6 @@ bool make_plane_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
-
-}  // namespace
 
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
