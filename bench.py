@@ -186,12 +186,12 @@ def cpu_baseline(workload, rows, seed=0):
 CAPTURED_TRAFFIC = {
     # det_gemm at 4096^3 runs the tensor-core kernel once per row band (two
     # bands); bytes are per launch, the mean of the call's two launches
-    "residue_gemm": {"fingerprint": "d8db9e979fa9bb7e", "mnk": (4096, 4096, 4096),
+    "residue_gemm": {"fingerprint": "073a5ec5cc837e96", "mnk": (4096, 4096, 4096),
                      "workload": "normal", "launches_per_call": 2,
-                     "bytes": (940786432 + 100576000 + 939516672 + 97751552) // 2},
+                     "bytes": (932100608 + 101554176 + 932126208 + 98440448) // 2},
 }
 KERNEL_SOURCES = {
-    "residue_gemm": ["gemm_tc.cu", "tc_ptx.cuh", "det_residue.cuh"],
+    "residue_gemm": ["gemm_tc2.cu", "gemm_tc.cu", "tc_ptx.cuh", "det_residue.cuh"],
 }
 
 
@@ -229,7 +229,7 @@ def roofline_for(stage_ms, stages, props, peaks, lib, workload="normal"):
         achieved = exact_flops / t / 1e12
         traffic, launches = captured_traffic(dom, workload)
         launches = launches or 1
-        return {"kernel": "residue_gemm_kernel (tcgen05 bf16, 128x256 tiles)", "bound": "tensor",
+        return {"kernel": "residue_gemm_pair_kernel (tcgen05 cta_group::2 bf16, 256x256 tiles)", "bound": "tensor",
                 "achieved": round(achieved, 3), "peak": peak, "unit": "TFLOP/s",
                 "frac": round(achieved / peak, 5), "traffic": traffic,
                 "launches_per_call": launches,
