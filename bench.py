@@ -252,6 +252,20 @@ def roofline_for(stage_ms, stages, props, peaks, lib, workload="normal"):
             "kernel_ms": round(stage_ms[dom], 4)}
 
 
+def pipe_fractions(gflops, props, peaks):
+    """The metric's reference pipes: exact work per second against the INT32 issue
+    peak (one exact multiply-add per lane per clock, counted as 2 ops like 2MNK)
+    and against GB300's nominal FP64 rate.  Above 1.0 means the tensor-core
+    residue path outruns any CUDA-core Kulisch kernel's ceiling."""
+    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    int_peak = alu_peak_gops(props.multi_processor_count, clock_mhz)
+    fp64_peak = 1250.0
+    return {"int32_issue": round(gflops / int_peak, 4), "int32_issue_peak_gops": round(int_peak, 1),
+            "fp64": round(gflops / fp64_peak, 2), "fp64_peak_gflops": fp64_peak,
+            "basis": f"{props.multi_processor_count} SMs x 128 INT32 lanes x {clock_mhz:.0f} MHz x "
+                     "2 ops per exact MAC; FP64 nominal 1.25 TFLOP/s"}
+
+
 def alu_peak_gops(sm_count, clock_mhz):
     """Integer-ALU issue peak: SMs x 128 lanes x clock, one instruction per exact
     multiply-add counted as 2 ops (the same convention as 2MNK)."""
@@ -400,6 +414,7 @@ def run_ours(args):
         "det_gemm_ms": round(kern_avg, 4),
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "roofline": roofline,
+        "pipe_fractions": pipe_fractions(value / world, props, peaks),
         "clocks": clocks,
     }
     line.update(extras)
