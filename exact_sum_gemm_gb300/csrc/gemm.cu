@@ -189,11 +189,19 @@ cudaError_t band_sync(int dev, BandSync** out) {
   return cudaSuccess;
 }
 
-// Rows per band: whole 128-row tiles; two bands once each half still fills
-// the GPU with tensor-core work.
-int64_t band_rows(const GemmArgs& g) {
-  if (g.M < 2048) return g.M;
-  return (g.M / 2 + 127) / 128 * 128;
+// Row bands: two bands of whole 256-row tiles once each still fills the GPU
+// with tensor-core work.  (Measured at 4096^3: one band, or three or four,
+// including a short last band, were slower: each extra band re-reads B's
+// planes and adds a tensor-core launch with its tail.)
+int band_bounds(const GemmArgs& g, int64_t (&edge)[kMaxBands + 1]) {
+  edge[0] = 0;
+  if (g.M < 2048) {
+    edge[1] = g.M;
+    return 1;
+  }
+  edge[1] = (g.M + 1) / 2 / 256 * 256;
+  edge[2] = g.M;
+  return 2;
 }
 
 cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch& L, int nplanes,
@@ -217,8 +225,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   __nv_bfloat16* planesB = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesB);
   int8_t* res = reinterpret_cast<int8_t*>(base + L.off_res);
   int* deep_rows = reinterpret_cast<int*>(base + L.off_deep_idx);   // [M] rows, then [N] columns
-  const int64_t H = band_rows(g);
-  const int nb = static_cast<int>((g.M + H - 1) / H);
+  int64_t edge[kMaxBands + 1];
+  const int nb = band_bounds(g, edge);
   const int64_t nkb = Kp / kStageK;
   const size_t es = g.bf16 ? 2 : 4;
 
@@ -232,7 +240,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // the residue kernels' deep-list counters double as the rows' deep counts,
   // from which the tiles are routed
   auto planes_of_band = [&](int b) {
-    const int64_t m0 = b * H, rows = (g.M - m0) < H ? g.M - m0 : H;
+    const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
     const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
     ResidueOperand ra{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
                       planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
@@ -240,7 +248,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     return launch_residues(ra, g.bf16, nplanes, stream);
   };
   auto gemm_of_band = [&](int b) {
-    const int64_t m0 = b * H, rows = (g.M - m0) < H ? g.M - m0 : H;
+    const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
     StageScope t(kStageResidueGemm, hi);
     ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
                    rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error};
@@ -280,7 +288,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     e = cudaStreamWaitEvent(stream, bs->gemm_done[b], 0);
     if (e != cudaSuccess) break;
     StageScope t(kStageReconstruct, stream);
-    const int64_t m0 = b * H, m1 = (g.M - m0) < H ? g.M : m0 + H;
+    const int64_t m0 = edge[b], m1 = edge[b + 1];
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
                  error, deep_rows + g.M + g.N, reinterpret_cast<ulonglong2*>(base + L.off_sbuf),
                  deep_col_slots(g.N), m0, m1};
