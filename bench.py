@@ -478,6 +478,38 @@ def measure_extras(args, dg, a, b, c, A, B, dev, stream):
                   "d2h_bytes_per_step": int(hC[0].nbytes), "ms_per_step": round(t, 4),
                   "pipelining": "double-buffered; copies on separate streams overlap the GEMM"}
     del dA[1], dB[1], dC[1]
+    # ---- the same det_gemm captured once in a CUDA graph and replayed: the
+    # launches of a call go to the GPU as one graph (flush outside the events)
+    out_g = torch.empty_like(c)
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        dg.det_gemm(a, b, out=out_g)
+    stream.wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        dg.det_gemm(a, b, out=out_g)
+    flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    for _ in range(3):
+        flush.zero_()
+        graph.replay()
+    torch.cuda.synchronize(dev)
+    g_ms = []
+    for _ in range(steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        g_ms.append(e0.elapsed_time(e1))
+    tg = statistics.mean(g_ms)
+    out["graph_replay"] = {
+        "value": round(2.0 * M * N * K / (tg * 1e-3) / 1e9, 3), "unit": UNIT,
+        "ms_per_step": round(tg, 4),
+        "equal_to_eager": bool(torch.equal(out_g.view(torch.int32), c.view(torch.int32)))}
+    del graph, out_g, flush
     # ---- sharded: 2-way K split through partial / combine / finalize
     full_bits = c.clone()
     cuts = [(0, K // 2), (K // 2, K)]
