@@ -78,38 +78,35 @@ __device__ __forceinline__ void normalise_digits(const int64_t (&d)[kDigits], ui
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t round_to_f32_bits(const uint32_t (&w)[kDigits - 1], int64_t top) {
   const bool neg = top < 0;
-  uint32_t mag[kDigits - 1];
-  uint64_t mag_top;
-  if (neg) {                          // magnitude = ~x + 1
-    uint32_t carry = 1;
-#pragma unroll
-    for (int j = 0; j < kDigits - 1; ++j) {
-      uint32_t v = ~w[j] + carry;
-      carry = (carry != 0u && v == 0u) ? 1u : 0u;
-      mag[j] = v;
-    }
-    mag_top = static_cast<uint64_t>(~top) + carry;
-  } else {
-#pragma unroll
-    for (int j = 0; j < kDigits - 1; ++j) mag[j] = w[j];
-    mag_top = static_cast<uint64_t>(top);
-  }
-  const uint32_t sign = neg ? 0x80000000u : 0u;
-  if (mag_top != 0) return sign | 0x7F800000u;     // >= 2^(544-298): overflow
-
+  // One pass over the words of the magnitude (negated on the fly when the
+  // value is negative: magnitude = ~x + 1), keeping only registers: the
+  // leading nonzero word, the two words below it, and the OR of all lower ones.
+  uint32_t carry = neg ? 1u : 0u;
+  uint32_t p1 = 0, p2 = 0, older = 0;              // the two previous words, OR of the rest
+  uint32_t whi = 0, wmid = 0, wlo = 0, rest = 0;    // 96-bit window below the leading bit
   int hi = -1;                                      // index of the leading nonzero word
 #pragma unroll
-  for (int j = 0; j < kDigits - 1; ++j) hi = mag[j] != 0u ? j : hi;
-  if (hi < 0) return 0u;                            // exact zero -> +0
-
-  uint32_t whi = 0, wmid = 0, wlo = 0, rest = 0;    // 96-bit window below the leading bit
-#pragma unroll
   for (int j = 0; j < kDigits - 1; ++j) {
-    whi = j == hi ? mag[j] : whi;
-    wmid = j == hi - 1 ? mag[j] : wmid;
-    wlo = j == hi - 2 ? mag[j] : wlo;
-    rest |= j < hi - 2 ? mag[j] : 0u;
+    uint32_t v = w[j];
+    if (neg) {
+      v = ~v + carry;
+      carry = (carry != 0u && v == 0u) ? 1u : 0u;
+    }
+    if (v != 0u) {
+      whi = v;
+      wmid = p1;
+      wlo = p2;
+      rest = older;
+      hi = j;
+    }
+    older |= p2;
+    p2 = p1;
+    p1 = v;
   }
+  const uint64_t mag_top = neg ? static_cast<uint64_t>(~top) + carry : static_cast<uint64_t>(top);
+  const uint32_t sign = neg ? 0x80000000u : 0u;
+  if (mag_top != 0) return sign | 0x7F800000u;     // >= 2^(544-298): overflow
+  if (hi < 0) return 0u;                            // exact zero -> +0
   const int msb = 32 * hi + 31 - __clz(whi);        // bit index of the leading 1
   if (msb >= 128 + kLsbBias) return sign | 0x7F800000u;   // |x| >= 2^128
 
