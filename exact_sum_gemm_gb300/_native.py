@@ -35,6 +35,8 @@ SIGNATURES = {
     "det_residue_moduli": (_i32, [_i32, _i64]),
     "det_stage_report": (_i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(_i32), _i32]),
+    "det_stage_timeline": (_i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
+                                  ctypes.POINTER(ctypes.c_double), _i32]),
     "det_gemm": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _i64, _vp]),
     "det_gemm_partial": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32, _vp, _vp]),
     "det_gemm_partial_noalloc": (_i32, [_i32, _i64, _i64, _i64, _vp, _i64, _i32, _vp, _i64, _i32,
@@ -91,6 +93,16 @@ def stage_report():
     counts = (ctypes.c_int * n_max)()
     n = lib().det_stage_report(names, ms, counts, n_max)
     return {names[i].decode(): (ms[i], counts[i]) for i in range(n)}
+
+
+def stage_timeline(n_max: int = 4096):
+    """[(stage name, start ms, stop ms)] recorded since det_stage_timing(1), in
+    the order the stages were enqueued, from the first record's start."""
+    names = (ctypes.c_char_p * n_max)()
+    t0 = (ctypes.c_double * n_max)()
+    t1 = (ctypes.c_double * n_max)()
+    n = lib().det_stage_timeline(names, t0, t1, n_max)
+    return [(names[i].decode(), t0[i], t1[i]) for i in range(n)]
 
 
 def check(fn_name: str, status: int) -> None:

@@ -84,4 +84,27 @@ int det_stage_report(const char** names, double* total_ms, int* counts, int max)
   return n;
 }
 
+int det_stage_timeline(const char** names, double* start_ms, double* stop_ms, int max) {
+  std::lock_guard<std::mutex> lock(det::g_mu);
+  int n = 0;
+  const det::Record* first = det::g_records.empty() ? nullptr : &det::g_records.front();
+  for (const det::Record& r : det::g_records) {
+    float t0 = 0.f, t1 = 0.f;
+    if (n < max && cudaEventSynchronize(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&t0, first->start, r.start) == cudaSuccess &&
+        cudaEventElapsedTime(&t1, first->start, r.stop) == cudaSuccess) {
+      if (names) names[n] = det::kStageNames[r.stage];
+      if (start_ms) start_ms[n] = t0;
+      if (stop_ms) stop_ms[n] = t1;
+      ++n;
+    }
+  }
+  for (const det::Record& r : det::g_records) {
+    cudaEventDestroy(r.start);
+    cudaEventDestroy(r.stop);
+  }
+  det::g_records.clear();
+  return n;
+}
+
 }  // extern "C"

@@ -96,6 +96,15 @@ int det_stage_timing(int enable);
 int det_residue_moduli(det_dtype dtype, int64_t K);
 int det_stage_report(const char** names, double* total_ms, int* counts, int max);
 
+/* The same records as a timeline, in the order the stages were enqueued:
+ * stage name, start and stop in milliseconds from the first record's start.
+ * Tensor-core launches ("residue_gemm") sit on a library stream and overlap
+ * the stages on the call's stream; a record starts when its stream reaches
+ * it, which may precede its first kernel's start.  Writes up to `max`
+ * entries, clears the record and returns the number written.  Any output
+ * pointer may be NULL. */
+int det_stage_timeline(const char** names, double* start_ms, double* stop_ms, int max);
+
 /*
  * det_gemm -- C = RNE_f32( sum_k A(m,k) * B(n,k) ), computed exactly.
  * det-train page, usage section (the det_gemm call) and section "Method".

@@ -140,3 +140,19 @@ def test_vector_rows_with_ragged_k_tail(oracle_mod):
     want16 = np_bits(oracle_mod.gemm(abf[:, :K], bbf[:, :K], dtype="bf16"))
     got16 = dg.det_gemm(dev_bf16(abf)[:, :K], dev_bf16(bbf)[:, :K])
     assert_bits_equal(bits_of(got16), want16, "bf16 vector rows, ragged K")
+
+
+def test_banded_schedule_matches_single_band_calls(oracle_mod):
+    # At 4096^3 f32 the rows run in two bands, each band's CUDA-core stages
+    # beside the other's tensor-core GEMM.  Four 1024-row calls run the
+    # one-band schedule: the two must agree on every output, and rows on both
+    # sides of the band edge on the oracle.
+    A = wl.normal_f32((4096, 4096), 0, 0)
+    B = wl.normal_f32((4096, 4096), 0, 1)
+    a, b = dev_f32(A), dev_f32(B)
+    whole = bits_of(dg.det_gemm(a, b))
+    parts = np.concatenate([bits_of(dg.det_gemm(a[i:i + 1024], b)) for i in range(0, 4096, 1024)])
+    assert np.array_equal(whole, parts), "4096^3: banded schedule differs from single-band calls"
+    rows = np.array([5, 1500, 2047, 2048, 4095])
+    want = np_bits(oracle_mod.gemm(A[rows], B))
+    assert_bits_equal(whole[rows], want, "4096^3 rows on both sides of the band edge")
