@@ -480,10 +480,15 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
   }
 }
 
-// ---------------------------------------------------------------- CRT (Garner)
+// ---------------------------------------------------------------- CRT
 //
 // The residue GEMM stores balanced residues r_i (|r_i| <= (p_i - 1)/2) as
-// two's-complement bytes.  S is rebuilt in mixed radix with balanced digits,
+// two's-complement bytes.  The fast reconstruction kernels rebuild S as one
+// sum of products (crt_s128, det_residue.cuh): about 60 integer multiply-
+// adds per output.  The deep-element kernel, which runs once per deep row or
+// column, uses Garner's mixed-radix form below; both give the unique S.
+//
+// Garner: S is rebuilt in mixed radix with balanced digits,
 //   S = sum_i v_i P_i,   P_i = p_0 ... p_{i-1},   |v_i| <= (p_i - 1)/2,
 // which spans exactly |S| <= (M - 1)/2 (M = the product of the moduli in use),
 // so it is the unique balanced value.  Garner's recurrence gives the digits,
@@ -496,9 +501,9 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
 __device__ __forceinline__ float biased_residue(uint32_t b) {
   return __uint_as_float(0x4B000000u | ((b ^ 0x80u) & 0xFFu));
 }
-// Byte j of a word of four residue bytes, as above.
-__device__ __forceinline__ float biased_residue_of_word(uint32_t w, int j) {
-  return __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | static_cast<uint32_t>(j)));
+// Byte j of a word of four residue bytes, sign-extended.
+__host__ __device__ __forceinline__ int32_t residue_of_word(uint32_t w, int j) {
+  return static_cast<int32_t>(w << (24 - 8 * j)) >> 24;
 }
 
 template <int i, int j>
@@ -724,11 +729,11 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
       const bool col_deep = ra.countB[n] != 0;
       const int slot = col_deep ? ra.colslot[n] : -1;
       if (col_deep && (slot < 0 || slot >= ra.slots)) continue;  // deep kernel re-reads it
-      float f[kNumModuli];
+      int32_t r[kNumModuli];
 #pragma unroll
-      for (int i = 0; i < kNumModuli; ++i) f[i] = biased_residue_of_word(packed[i], j);
+      for (int i = 0; i < kNumModuli; ++i) r[i] = residue_of_word(packed[i], j);
       uint64_t slo, shi;
-      garner_s128<P>(f, P, slo, shi);
+      crt_s128<P>(r, slo, shi);
       if (col_deep) {                                             // the deep kernel finishes it
         ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
         continue;
@@ -825,12 +830,11 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
     int emA = ra.emaxA[m];
     emA = emA == kEmaxEmpty ? 0 : emA;
     const int64_t idx = m * g.N + n;
-    float f[kNumModuli];
+    int32_t r[kNumModuli];
 #pragma unroll
-    for (int i = 0; i < kNumModuli; ++i)
-      f[i] = biased_residue(i < P ? static_cast<uint8_t>(ra.res[i * MN + idx]) : 0u);
+    for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(ra.res[i * MN + idx]) : 0;
     uint64_t slo, shi;
-    garner_s128<P>(f, P, slo, shi);
+    crt_s128<P>(r, slo, shi);
     if (col_deep) {
       ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
       continue;
@@ -865,10 +869,13 @@ cudaError_t with_planes(int bf16, int P, F&& launch) {
 }  // namespace
 
 int residue_planes_needed(const GemmArgs& g) {
-  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^19; need prod > 2|S|
+  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^19.  The CRT sum needs
+  // prod > 2|S| (1 + 2^-7): the margin lets its fixed-point quotient round
+  // to the right integer (crt_s128).
   const unsigned __int128 sig = g.bf16 ? 0xFFu : 0xFFFFFFu;
   const unsigned __int128 mx = sig << kDeepGap;
-  const unsigned __int128 bound = static_cast<unsigned __int128>(g.K > 0 ? g.K : 1) * mx * mx * 2;
+  const unsigned __int128 twice = static_cast<unsigned __int128>(g.K > 0 ? g.K : 1) * mx * mx * 2;
+  const unsigned __int128 bound = twice + (twice >> 7);
   unsigned __int128 prod = 1;
   const int least = g.bf16 ? 8 : 12;
   for (int i = 0; i < kNumModuli; ++i) {
