@@ -36,10 +36,9 @@ cudaError_t launch_prepass(const GemmArgs& g, const Scratch& s, cudaStream_t str
 // The residue path's pieces of the pre-pass: row maxima only, and routing from
 // deep counts produced elsewhere (the residue kernel's list counters).
 cudaError_t launch_emax(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
-// Routing from deep counts; with deep_rows [M] / deep_cols [2N] /
+// Routing from deep counts; with deep_rows [M] / deep_cols [N] /
 // deep_counters (two ints, zero at launch) it also lists the rows and columns
-// holding deep elements and maps columns to their list slots (residue path),
-// else pass null.
+// holding deep elements (residue path), else pass null.
 cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, const Scratch& s,
                             int* deep_rows, int* deep_cols, int* deep_counters,
                             cudaStream_t stream);

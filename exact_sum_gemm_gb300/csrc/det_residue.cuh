@@ -22,33 +22,18 @@ __host__ __device__ constexpr int modulus(int i) {
        : i == 6 ? 233 : i == 7 ? 229 : i == 8 ? 227 : i == 9 ? 223 : i == 10 ? 217 : i == 11 ? 211
        : i == 12 ? 199 : 197;
 }
-// Garner's mixed-radix constants (compile time).  With P_i = p_0 * ... *
-// p_{i-1}, the digits of S = sum_i v_i P_i satisfy
-//   v_i = r_i g_i + sum_{j<i} v_j d_ij  (mod p_i),
-//   g_i = P_i^-1 mod p_i,   d_ij = -P_j g_i mod p_i,
-// all taken as balanced representatives (magnitude <= (p_i - 1) / 2).
+// Balanced representatives, inverses and products modulo the moduli (compile
+// time).
 __host__ __device__ constexpr int balanced_rep(long long x, int p) {
   long long r = x % p;
   if (r < 0) r += p;
   return static_cast<int>(r > (p - 1) / 2 ? r - p : r);
-}
-__host__ __device__ constexpr int prefix_product_mod(int j, int i) {   // P_j mod p_i
-  int r = 1;
-  for (int l = 0; l < j; ++l) r = (r * (modulus(l) % modulus(i))) % modulus(i);
-  return r;
 }
 __host__ __device__ constexpr int inverse_mod(int a, int p) {
   for (int c = 1; c < p; ++c)
     if ((a * c) % p == 1) return c;
   return 0;
 }
-__host__ __device__ constexpr int garner_g(int i) {
-  return balanced_rep(inverse_mod(prefix_product_mod(i, i), modulus(i)), modulus(i));
-}
-__host__ __device__ constexpr int garner_d(int i, int j) {
-  return balanced_rep(-static_cast<long long>(prefix_product_mod(j, i)) * garner_g(i), modulus(i));
-}
-
 // The CRT as one sum.  For the first P moduli, with M = p_0 ... p_{P-1}, the
 // balanced residues r_i of an integer S with |S| < M/2 give
 //   S = sum_i r_i C_i - q M,   C_i = (M / p_i) c_i,  c_i = (M / p_i)^-1 mod p_i,
@@ -176,7 +161,6 @@ __host__ __device__ __forceinline__ void crt_s128(const int32_t (&r)[kNumModuli]
 // |a| <= 2^24 and below 139 for |a| <= 2^26.  A zero result is +0 unless a
 // is -0.
 constexpr float kRoundMagic = 12582912.0f;           // 1.5 * 2^23
-constexpr int kRoundMagicBits = 0x4B400000;
 
 __device__ __forceinline__ float near_mod_f32(float a, float p, float inv_p) {
   const float q = __fsub_rn(__fmaf_rn(a, inv_p, kRoundMagic), kRoundMagic);
@@ -226,26 +210,19 @@ struct ReconArgs {
   const uint2* listB;
   int cap;
   const int* error;           // nonzero: the tensor-core kernel gave up (outputs NaN)
-  const int* colslot;         // [N]: a deep column's slot in the deep-column list, else -1
-  ulonglong2* sbuf;           // [M][slots]: shallow sums S of deep-column outputs (lo, hi)
-  int slots;                  // slots kept in sbuf; columns in later slots re-read residues
   int64_t m_begin, m_end;     // rows of C handled by this launch (a band)
 };
 
-// Deep columns whose shallow sums are passed from the fast reconstruction to
-// the deep one through a compact buffer (the rest re-read their residues).
-inline int deep_col_slots(int64_t N) {
-  const int64_t s = N / 16;
-  return static_cast<int>(N < 64 ? N : (s < 64 ? 64 : s));
-}
-
 int residue_planes_needed(const GemmArgs& g);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
-// deep_lists: the rows of A then the columns of C that hold deep elements
-// (M + N ints), with their two counts in deep_counters, as the routing step
-// lists them.
-cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
-                               int* deep_counters, cudaStream_t stream);
+// The outputs of a band whose row of A and column of B hold no deep element.
+cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream);
+// The band's other outputs (independent of the fast kernel: both may run at
+// once).  deep_lists: the rows of A then the columns of C that hold deep
+// elements (M + N ints), with their two counts in deep_counters, as the
+// routing step lists them.
+cudaError_t launch_reconstruct_deep(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
+                                    int* deep_counters, cudaStream_t stream);
 
 struct ResGemmArgs {
   const __nv_bfloat16* A;     // [M/32][Kp/64][nplanes][32][64] (ResidueOperand::planes)

@@ -129,7 +129,7 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
 
 struct ResidueScratch {
   size_t bytes;
-  size_t off_counts, off_deep_idx, off_sbuf, off_listA, off_listB, off_planesA, off_planesB, off_res;
+  size_t off_counts, off_deep_idx, off_listA, off_listB, off_planesA, off_planesB, off_res;
 };
 
 ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int cap) {
@@ -137,10 +137,8 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   size_t b = align_up(scratch_bytes(g, 0), 1024);
   r.off_counts = b;                     // countA [M], countB [N], error, deep-row/col counters [2]
   b = align_up(b + sizeof(int) * size_t(g.M + g.N + 3), 1024);
-  r.off_deep_idx = b;                    // deep rows [M], deep columns [N], column slots [N]
-  b = align_up(b + sizeof(int) * size_t(g.M + 2 * g.N), 1024);
-  r.off_sbuf = b;                        // shallow sums of deep-column outputs [M][slots]
-  b = align_up(b + 16 * size_t(g.M) * size_t(deep_col_slots(g.N)), 1024);
+  r.off_deep_idx = b;                    // deep rows [M], deep columns [N]
+  b = align_up(b + sizeof(int) * size_t(g.M + g.N), 1024);
   r.off_listA = b;
   b = align_up(b + sizeof(uint2) * size_t(g.M) * cap, 1024);
   r.off_listB = b;
@@ -158,14 +156,19 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
 // Banded schedule.  C is cut into row bands; band b's tensor-core GEMM runs on
 // a high-priority library stream while the caller's stream computes the next
 // band's A residue planes and the previous band's reconstruction, so the
-// CUDA-core stages overlap the tensor-core kernel.  Only stream order and
-// events connect the two streams (no kernel waits on another).
+// CUDA-core stages overlap the tensor-core kernel.  A band's outputs with
+// deep elements are reconstructed on a second library stream beside its
+// other outputs (that kernel mostly waits on memory).  Only stream order and
+// events connect the streams (no kernel waits on another).
 constexpr int kMaxBands = 4;
 
 struct BandSync {
   cudaStream_t hi = nullptr;                       // tensor-core launches
+  cudaStream_t side = nullptr;                     // deep-output reconstruction
   cudaEvent_t planes_done[kMaxBands] = {};         // caller's stream -> hi
   cudaEvent_t gemm_done[kMaxBands] = {};           // hi -> caller's stream
+  cudaEvent_t fork[kMaxBands] = {};                // caller's stream -> side
+  cudaEvent_t deep_done[kMaxBands] = {};           // side -> caller's stream
 };
 std::mutex g_band_mu[kMaxDevices];
 BandSync g_band[kMaxDevices];
@@ -175,15 +178,23 @@ cudaError_t band_sync(int dev, BandSync** out) {
   if (b.hi == nullptr) {
     int least = 0, greatest = 0;
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&b.hi, cudaStreamNonBlocking, greatest);
+    cudaStream_t hi = nullptr;
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
+    // the deep kernel's few blocks go ahead of the caller's kernels, behind
+    // the tensor-core launches
+    const int side_prio = greatest < least ? greatest + 1 : greatest;
+    if (e == cudaSuccess && b.side == nullptr)
+      e = cudaStreamCreateWithPriority(&b.side, cudaStreamNonBlocking, side_prio);
     for (int i = 0; i < kMaxBands && e == cudaSuccess; ++i) {
-      e = cudaEventCreateWithFlags(&b.planes_done[i], cudaEventDisableTiming);
-      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&b.gemm_done[i], cudaEventDisableTiming);
+      cudaEvent_t* ev[4] = {&b.planes_done[i], &b.gemm_done[i], &b.fork[i], &b.deep_done[i]};
+      for (int k = 0; k < 4 && e == cudaSuccess; ++k)
+        if (*ev[k] == nullptr) e = cudaEventCreateWithFlags(ev[k], cudaEventDisableTiming);
     }
     if (e != cudaSuccess) {
-      b.hi = nullptr;
+      if (hi != nullptr) cudaStreamDestroy(hi);
       return e;
     }
+    b.hi = hi;
   }
   *out = &b;
   return cudaSuccess;
@@ -284,21 +295,34 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageResiduePlanes, stream);
     e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M, error + 1, stream);
   }
+  int forked = 0;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
     e = cudaStreamWaitEvent(stream, bs->gemm_done[b], 0);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->fork[b], stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->side, bs->fork[b], 0);
     if (e != cudaSuccess) break;
-    StageScope t(kStageReconstruct, stream);
+    forked = b + 1;
     const int64_t m0 = edge[b], m1 = edge[b + 1];
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
-                 error, deep_rows + g.M + g.N, reinterpret_cast<ulonglong2*>(base + L.off_sbuf),
-                 deep_col_slots(g.N), m0, m1};
-    // deep-row/column lists, and their two counters right after the error flag
-    e = launch_reconstruct(g, rc, deep_rows, error + 1, stream);
+                 error, m0, m1};
+    {
+      // deep-row/column lists, and their two counters right after the error flag
+      StageScope t(kStageReconstruct, bs->side);
+      e = launch_reconstruct_deep(g, rc, deep_rows, error + 1, bs->side);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(bs->deep_done[b], bs->side);
+    if (e == cudaSuccess) {
+      StageScope t(kStageReconstruct, stream);
+      e = launch_reconstruct_fast(g, rc, stream);
+    }
   }
+  for (int b = 0; b < forked && e == cudaSuccess; ++b) e = cudaStreamWaitEvent(stream, bs->deep_done[b], 0);
   if (e != cudaSuccess) {
-    // keep the caller's stream ordered after everything enqueued on hi
+    // keep the caller's stream ordered after everything enqueued on hi and side
     cudaEvent_t join = bs->gemm_done[0];
     if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
+    join = bs->deep_done[0];
+    if (cudaEventRecord(join, bs->side) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     return e;
   }
   StageScope t(kStageGeneral, stream);

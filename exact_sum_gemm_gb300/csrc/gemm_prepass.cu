@@ -168,8 +168,7 @@ __global__ void __launch_bounds__(kThreads) rowstat_kernel(StatOperand a, StatOp
 // Routing, step 1: the largest deep count of every 64-row block of A and of
 // every 64-column block of C (one warp each), into bmax[tiles_m + tiles_n].
 // With lists (residue path) it also lists the rows of A and columns of C that
-// hold deep elements (in any order: every output is computed on its own), and
-// maps each column to its slot in the column list (cols[N + n], -1 if none).
+// hold deep elements (in any order: every output is computed on its own).
 // It resets the general-tile count read by step 2.
 __global__ void __launch_bounds__(kThreads) block_max_kernel(const int* deepA, int64_t M,
                                                               const int* deepB, int64_t N, int* bmax,
@@ -192,12 +191,9 @@ __global__ void __launch_bounds__(kThreads) block_max_kernel(const int* deepA, i
       const int c = cnt[i];
       mx = max(mx, c);
       if (rows != nullptr) {
-        if (is_a) {
-          if (c != 0) rows[atomicAdd(nrc, 1)] = static_cast<int>(i);
-        } else {
-          const int slot = c != 0 ? atomicAdd(nrc + 1, 1) : -1;
-          if (c != 0) cols[slot] = static_cast<int>(i);
-          cols[len + i] = slot;                 // column -> its slot in the list, or -1
+        if (c != 0) {
+          if (is_a) rows[atomicAdd(nrc, 1)] = static_cast<int>(i);
+          else cols[atomicAdd(nrc + 1, 1)] = static_cast<int>(i);
         }
       }
     }

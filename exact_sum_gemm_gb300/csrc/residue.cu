@@ -483,89 +483,13 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
 // ---------------------------------------------------------------- CRT
 //
 // The residue GEMM stores balanced residues r_i (|r_i| <= (p_i - 1)/2) as
-// two's-complement bytes.  The fast reconstruction kernels rebuild S as one
-// sum of products (crt_s128, det_residue.cuh): about 60 integer multiply-
-// adds per output.  The deep-element kernel, which runs once per deep row or
-// column, uses Garner's mixed-radix form below; both give the unique S.
-//
-// Garner: S is rebuilt in mixed radix with balanced digits,
-//   S = sum_i v_i P_i,   P_i = p_0 ... p_{i-1},   |v_i| <= (p_i - 1)/2,
-// which spans exactly |S| <= (M - 1)/2 (M = the product of the moduli in use),
-// so it is the unique balanced value.  Garner's recurrence gives the digits,
-//   v_i = r_i g_i + sum_{j<i} v_j d_ij  (mod p_i)   (constants: det_residue.cuh),
-// where every term is below 127^2 in magnitude, so each sum (< 14 * 2^14) is
-// exact in binary32 and near_mod returns the balanced digit.  Digits of
-// moduli not in use stay 0.
+// two's-complement bytes.  The reconstruction rebuilds S as one sum of
+// products, crt_s128 (det_residue.cuh): about 60 integer multiply-adds per
+// output, with compile-time constants for each count of moduli.
 
-// A stored residue byte b as the exact float 2^23 + 128 + r (r = b as int8).
-__device__ __forceinline__ float biased_residue(uint32_t b) {
-  return __uint_as_float(0x4B000000u | ((b ^ 0x80u) & 0xFFu));
-}
 // Byte j of a word of four residue bytes, sign-extended.
 __host__ __device__ __forceinline__ int32_t residue_of_word(uint32_t w, int j) {
   return static_cast<int32_t>(w << (24 - 8 * j)) >> 24;
-}
-
-template <int i, int j>
-__device__ __forceinline__ float garner_sum(float acc, const float (&v)[kNumModuli]) {
-  if constexpr (j < i) {
-    constexpr float d = static_cast<float>(garner_d(i, j));
-    return garner_sum<i, j + 1>(__fmaf_rn(v[j], d, acc), v);
-  } else {
-    return acc;
-  }
-}
-
-// Digits v_0 .. v_{P-1} for the P moduli in use (P <= kMaxP; with kMaxP the
-// compiled count, P = kMaxP folds every guard away).
-template <int i, int kMaxP>
-__device__ __forceinline__ void garner_digits(const float (&f)[kNumModuli], int P, float (&v)[kNumModuli]) {
-  if constexpr (i < kMaxP) {
-    if (i < P) {
-      constexpr float gi = static_cast<float>(garner_g(i));
-      constexpr float bias = -8388736.0f * gi;                  // -(2^23 + 128) g_i, exact
-      const float acc = garner_sum<i, 0>(__fmaf_rn(f[i], gi, bias), v);   // r_i g_i + ...
-      v[i] = near_mod<modulus(i)>(acc);
-      garner_digits<i + 1, kMaxP>(f, P, v);
-    }
-  }
-}
-
-// Integer value of a binary32 holding an integer of magnitude below 2^22.
-__device__ __forceinline__ int64_t small_float_to_int(float x) {
-  return static_cast<int64_t>(__float_as_int(__fadd_rn(x, kRoundMagic)) - kRoundMagicBits);
-}
-
-// S as a signed 128-bit integer (hi:lo), from the biased residue floats f.
-// Horner over digit pairs w_k = v_2k + p_2k v_2k+1 (|w_k| < 2^15, exact in
-// fp32) with radix R_k = p_2k p_2k+1:  the top four pairs (moduli 6..13,
-// |T| < 2^62) and the bottom three (moduli 0..5, |L| < 2^48) in int64, then
-// S = T * P_6 + L.
-template <int kMaxP>
-__device__ __forceinline__ void garner_s128(const float (&f)[kNumModuli], int P, uint64_t& lo,
-                                            uint64_t& hi) {
-  static_assert(kNumModuli == 14, "digit pairs below assume 14 moduli");
-  float v[kNumModuli];
-#pragma unroll
-  for (int i = 0; i < kNumModuli; ++i) v[i] = 0.0f;
-  garner_digits<0, kMaxP>(f, P, v);
-  int64_t w[kNumModuli / 2];
-#pragma unroll
-  for (int k = 0; k < kNumModuli / 2; ++k)
-    w[k] = small_float_to_int(__fmaf_rn(v[2 * k + 1], static_cast<float>(modulus(2 * k)), v[2 * k]));
-  constexpr int64_t R[kNumModuli / 2] = {
-      int64_t(modulus(0)) * modulus(1), int64_t(modulus(2)) * modulus(3),
-      int64_t(modulus(4)) * modulus(5), int64_t(modulus(6)) * modulus(7),
-      int64_t(modulus(8)) * modulus(9), int64_t(modulus(10)) * modulus(11),
-      int64_t(modulus(12)) * modulus(13)};
-  const int32_t t32 = static_cast<int32_t>(w[6]) * static_cast<int32_t>(R[5]) + static_cast<int32_t>(w[5]);
-  int64_t t = static_cast<int64_t>(t32) * R[4] + w[4];
-  t = t * R[3] + w[3];
-  const int64_t l = (w[2] * R[1] + w[1]) * R[0] + w[0];
-  constexpr int64_t kP6 = R[0] * R[1] * R[2];
-  const __int128 S = static_cast<__int128>(t) * kP6 + l;
-  lo = static_cast<uint64_t>(S);
-  hi = static_cast<uint64_t>(static_cast<unsigned __int128>(S) >> 64);
 }
 
 // RNE_f32(S * 2^E) for a signed 128-bit S = (hi:lo): the binary32 rule,
@@ -726,18 +650,12 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
     for (int j = 0; j < kReconCols; ++j) {
       if (j >= ncols) break;
       const int64_t n = n0 + j;
-      const bool col_deep = ra.countB[n] != 0;
-      const int slot = col_deep ? ra.colslot[n] : -1;
-      if (col_deep && (slot < 0 || slot >= ra.slots)) continue;  // deep kernel re-reads it
+      if (ra.countB[n] != 0) continue;                            // deep column: deep kernel
       int32_t r[kNumModuli];
 #pragma unroll
       for (int i = 0; i < kNumModuli; ++i) r[i] = residue_of_word(packed[i], j);
       uint64_t slo, shi;
       crt_s128<P>(r, slo, shi);
-      if (col_deep) {                                             // the deep kernel finishes it
-        ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
-        continue;
-      }
       int emB = ra.emaxB[n];
       emB = emB == kEmaxEmpty ? 0 : emB;
       const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
@@ -746,11 +664,12 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
   }
 }
 
-// det_gemm outputs with deep entries: every output of a deep row, then every
-// output of a deep column outside the deep rows.  Dense work list, so the
-// warps stay full.
-template <int kBf16>
-__global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
+// Outputs with deep entries: every output of a deep row, then every output of
+// a deep column outside the deep rows.  Dense work list, so the warps stay
+// full.  It shares nothing with the fast kernels but the residues (read
+// only), so it runs beside them.
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
     GemmArgs g, ReconArgs ra, const int* rows,
     const int* cols, const int* nrc) {
   const int64_t MN = g.M * g.N;
@@ -761,7 +680,7 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
   const int64_t part1 = n_rows * g.N, total = part1 + band * n_cols;
   for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * kThreads) {
-    int64_t m, n, slot = -1;
+    int64_t m, n;
     if (idx < part1) {
       m = rows[idx / g.N];
       if (m < ra.m_begin || m >= ra.m_end) continue;              // another band's row
@@ -769,27 +688,19 @@ __global__ void __launch_bounds__(kThreads, 2) reconstruct_deep_kernel(
     } else {
       const int64_t j = idx - part1;
       const int64_t mb = j / n_cols;
-      slot = j - mb * n_cols;
       m = ra.m_begin + mb;
-      n = cols[slot];
+      n = cols[j - mb * n_cols];
       if (ra.countA[m] != 0) continue;                          // done with its deep row
     }
     if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's output
     int emA = ra.emaxA[m], emB = ra.emaxB[n];
     emA = emA == kEmaxEmpty ? 0 : emA;
     emB = emB == kEmaxEmpty ? 0 : emB;
-    uint64_t slo, shi;
-    if (slot >= 0 && slot < ra.slots) {          // shallow sum left by the fast kernel
-      const ulonglong2 v = ra.sbuf[m * ra.slots + slot];
-      slo = v.x;
-      shi = v.y;
-    } else {
-      float f[kNumModuli];
+    int32_t r[kNumModuli];
 #pragma unroll
-      for (int i = 0; i < kNumModuli; ++i)
-        f[i] = biased_residue(i < ra.nplanes ? static_cast<uint8_t>(ra.res[i * MN + m * g.N + n]) : 0u);
-      garner_s128<kNumModuli>(f, ra.nplanes, slo, shi);
-    }
+    for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(ra.res[i * MN + m * g.N + n]) : 0;
+    uint64_t slo, shi;
+    crt_s128<P>(r, slo, shi);
     const int E = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0) - 64;
     W192 t;
     t.w[0] = 0;
@@ -819,9 +730,7 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
   const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
   const int64_t n = int64_t(blockIdx.x) * kThreads + threadIdx.x;
   if (n >= g.N) return;
-  const bool col_deep = ra.countB[n] != 0;                    // the deep kernel finishes these
-  const int slot = col_deep ? ra.colslot[n] : -1;
-  if (col_deep && (slot < 0 || slot >= ra.slots)) return;     // ... re-reading the residues
+  if (ra.countB[n] != 0) return;                              // deep column: deep kernel
   int emB = ra.emaxB[n];
   emB = emB == kEmaxEmpty ? 0 : emB;
   for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
@@ -835,10 +744,6 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
     for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(ra.res[i * MN + idx]) : 0;
     uint64_t slo, shi;
     crt_s128<P>(r, slo, shi);
-    if (col_deep) {
-      ra.sbuf[m * ra.slots + slot] = make_ulonglong2(slo, shi);
-      continue;
-    }
     const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
     write_digits_s128(g.P + idx, MN, slo, shi, Es, g.K, nf);
   }
@@ -906,15 +811,9 @@ cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cuda
   return cudaGetLastError();
 }
 
-cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
-                               int* deep_counters, cudaStream_t stream) {
-  const int64_t MN = g.M * g.N;
-  if (MN == 0) return cudaSuccess;
-  const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
+cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream) {
   const int64_t band = ra.m_end - ra.m_begin;
-  if (band <= 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
-            static_cast<unsigned>(band < 65535 ? band : 65535));
+  if (g.M * g.N == 0 || band <= 0) return cudaSuccess;
   cudaError_t e;
   if (g.P != nullptr) {
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
@@ -924,27 +823,39 @@ cudaError_t launch_reconstruct(const GemmArgs& g, const ReconArgs& ra, int* deep
       return cudaSuccess;
     });
   } else {
+    const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
+    dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
+              static_cast<unsigned>(band < 65535 ? band : 65535));
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
       reconstruct_fast_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(g, ra);
       return cudaSuccess;
     });
   }
   if (e != cudaSuccess) return e;
+  note_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reconstruct_deep(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
+                                    int* deep_counters, cudaStream_t stream) {
+  const int64_t band = ra.m_end - ra.m_begin;
+  if (g.M * g.N == 0 || band <= 0) return cudaSuccess;
   // deep rows and columns: index lists [M] and [N] and their two counters,
-  // filled by the routing step
-  int* rows = deep_lists;
-  int* cols = deep_lists + g.M;
-  int* nrc = deep_counters;
+  // filled by the routing step.  One block per SM: the kernel waits on
+  // memory most of the time, and leaves room for the fast kernel beside it.
+  const int* rows = deep_lists;
+  const int* cols = deep_lists + g.M;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (sms <= 0) sms = 1;
-  const unsigned dgrid = static_cast<unsigned>(sms) * 4;
-  if (g.bf16)
-    reconstruct_deep_kernel<1><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
-  else
-    reconstruct_deep_kernel<0><<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, nrc);
-  note_launch(2);
+  const unsigned dgrid = static_cast<unsigned>(sms > 0 ? sms : 1);
+  const cudaError_t e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
+    reconstruct_deep_kernel<decltype(B)::value, decltype(P)::value>
+        <<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, deep_counters);
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  note_launch();
   return cudaGetLastError();
 }
 
