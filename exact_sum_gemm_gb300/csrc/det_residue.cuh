@@ -215,6 +215,9 @@ struct ReconArgs {
 
 int residue_planes_needed(const GemmArgs& g);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
+// Two operands' planes in one launch (one grid covering both).
+cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1, int bf16, int nplanes,
+                             cudaStream_t stream);
 // The outputs of a band whose row of A and column of B hold no deep element.
 cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream);
 // The band's other outputs (independent of the fast kernel: both may run at

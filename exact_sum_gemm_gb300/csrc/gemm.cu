@@ -250,14 +250,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   if (e != cudaSuccess) return e;
   // the residue kernels' deep-list counters double as the rows' deep counts,
   // from which the tiles are routed
-  auto planes_of_band = [&](int b) {
+  auto operand_of_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
     const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
-    ResidueOperand ra{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
-                      planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
-                      counts + m0, listA + m0 * cap, cap};
-    return launch_residues(ra, g.bf16, nplanes, stream);
+    return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
+                          planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
+                          counts + m0, listA + m0 * cap, cap};
   };
+  auto planes_of_band = [&](int b) { return launch_residues(operand_of_band(b), g.bf16, nplanes, stream); };
   auto gemm_of_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
     StageScope t(kStageResidueGemm, hi);
@@ -273,9 +273,9 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   };
   {
     StageScope t(kStageResiduePlanes, stream);
+    // B's planes and band 0's A planes in one launch
     ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
-    e = launch_residues(rb, g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = planes_of_band(0);
+    e = launch_residues2(rb, operand_of_band(0), g.bf16, nplanes, stream);
   }
   if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[0], stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, bs->planes_done[0], 0);

@@ -78,13 +78,19 @@ __device__ __forceinline__ void write_residue_pairs(uint32_t* dst, float x0, flo
 // pair as P 4-byte words 4 KB apart (a warp covers one row's stage: one
 // 128-byte line per plane).  Padding rows get zero residues.  Every deep or
 // non-finite element is counted (and listed while there is room).
+// Two operands may share a launch: blocks with blockIdx.y below `split` take
+// o0, the others o1 (row block blockIdx.y - split).
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
+__global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, ResidueOperand o1,
+                                                           unsigned split) {
   static_assert(kTileK == kStageK && kTileRows == kPlaneRows, "one block covers one plane block");
   __shared__ uint32_t tile[kTileRows][kTileK + 1];
   __shared__ int row_emax[kTileRows];
+  const bool second = blockIdx.y >= split;
+  const ResidueOperand o = second ? o1 : o0;
+  const int64_t by = second ? blockIdx.y - split : blockIdx.y;
   const int tid = threadIdx.x;
-  const int64_t r0 = int64_t(blockIdx.y) * kTileRows;
+  const int64_t r0 = by * kTileRows;
   const int64_t k0 = int64_t(blockIdx.x) * kTileK;
 #pragma unroll
   for (int u = 0; u < kTileRows * kTileK / kThreads; ++u) {
@@ -126,7 +132,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o) {
       }
     }
     uint32_t* dst = reinterpret_cast<uint32_t*>(
-        o.planes + (int64_t(blockIdx.y) * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
+        o.planes + (by * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
         r * kStageK + kk);
     write_residue_pairs<0, P>(dst, x[0], pw[0], x[1], pw[1]);
   }
@@ -152,9 +158,13 @@ __device__ __forceinline__ void write_residue_quads(uint2* dst, const float (&x)
 // (one 16-byte f32 or 8-byte bf16 load each) and writes each plane as one
 // 8-byte word, so a half-warp stores one 128-byte plane row.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o) {
+__global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o0, ResidueOperand o1,
+                                                                unsigned split) {
+  const bool second = blockIdx.y >= split;
+  const ResidueOperand o = second ? o1 : o0;
+  const int64_t by = second ? blockIdx.y - split : blockIdx.y;
   const int tid = threadIdx.x;
-  const int64_t r0 = int64_t(blockIdx.y) * kTileRows;
+  const int64_t r0 = by * kTileRows;
   const int64_t k0 = int64_t(blockIdx.x) * kTileK;
   const int64_t nkb = o.Kp / kStageK;
 #pragma unroll 1
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
       }
     }
     uint2* dst = reinterpret_cast<uint2*>(
-        o.planes + (int64_t(blockIdx.y) * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
+        o.planes + (by * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
         r * kStageK + kq);
     write_residue_quads<0, P>(dst, x, pw);
   }
@@ -540,9 +550,23 @@ __device__ __noinline__ uint32_t round_s128_exact(uint64_t lo, uint64_t hi, int 
   return sign | bits;
 }
 
+// The binary32 pattern of a 64-bit integer t in [2^63, 2^64), rounded to
+// nearest even, in 32-bit integer steps (a 64-bit integer-to-float
+// conversion would run on the narrow fp64 pipe): bits 63..40 are the
+// significand, bit 39 the rounding bit, bits 38..0 the sticky bits.  The
+// exponent field is 190 (2^63); a significand that rounds up to 2^24 carries
+// into it.
+__host__ __device__ __forceinline__ uint32_t f32_bits_of_top(uint64_t t) {
+  const uint32_t t_hi = static_cast<uint32_t>(t >> 32), t_lo = static_cast<uint32_t>(t);
+  const uint32_t mant = t_hi >> 8;                                  // in [2^23, 2^24)
+  const uint32_t sticky = ((t_hi & 0x7Fu) | t_lo) != 0u ? 1u : 0u;
+  const uint32_t up = (t_hi >> 7) & (sticky | mant) & 1u;
+  return (189u << 23) + mant + up;
+}
+
 // RNE_f32(S * 2^E), fast form.  The leading 64 bits of |S|, with every bit
 // below them ORed into bit 0 (a sticky bit well below the rounding position),
-// convert to binary32 with the same round-to-nearest-even decision as |S|
+// round to binary32 with the same round-to-nearest-even decision as |S|
 // itself; the exact power-of-two scaling is then an exponent add.  Results
 // that would be subnormal or zero go to the bit-by-bit routine.
 __device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) {
@@ -563,7 +587,7 @@ __device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) 
   } else {
     top = alo << (lz - 64);
   }
-  const uint32_t f = __float_as_uint(__ull2float_rn(top));     // |S| * 2^(lz-64), rounded
+  const uint32_t f = f32_bits_of_top(top);                      // |S| * 2^(lz-64), rounded
   const int shift = E + 64 - lz;
   const int ef = static_cast<int>(f >> 23) + shift;             // biased exponent of the result
   if (ef >= 1 && ef <= 254) return (neg ? 0x80000000u : 0u) | (f + (static_cast<uint32_t>(shift) << 23));
@@ -615,7 +639,7 @@ constexpr int kReconCols = 4;                       // outputs per thread (one r
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
+__global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;    // the tensor-core kernel gave up
@@ -790,25 +814,51 @@ int residue_planes_needed(const GemmArgs& g) {
   return -1;
 }
 
-cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream) {
-  if (o.rows == 0 || o.Kp == 0) return cudaSuccess;
-  dim3 grid(static_cast<unsigned>((o.Kp + kTileK - 1) / kTileK),
-            static_cast<unsigned>((o.rows + kTileRows - 1) / kTileRows));
+namespace {
+
+bool rows_layout(const ResidueOperand& o, int bf16) {
   // vector loads: K-contiguous rows whose every row start is 16-byte (f32) or
   // 8-byte (bf16) aligned
   const uintptr_t vec = bf16 ? 8 : 16;
-  const bool rows_ok = o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
-                       (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
+  return o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
+         (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
+}
+
+// one launch over o0's row blocks, then o1's (both of the same layout)
+cudaError_t residues_launch(const ResidueOperand& o0, const ResidueOperand& o1, int64_t blocks0,
+                            int64_t blocks1, bool rows, int bf16, int nplanes, cudaStream_t stream) {
+  dim3 grid(static_cast<unsigned>((o0.Kp + kTileK - 1) / kTileK), static_cast<unsigned>(blocks0 + blocks1));
+  const unsigned split = static_cast<unsigned>(blocks0);
   const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
-    if (rows_ok)
-      residue_rows_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
+    if (rows)
+      residue_rows_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o0, o1, split);
     else
-      residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o);
+      residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o0, o1, split);
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream) {
+  if (o.rows == 0 || o.Kp == 0) return cudaSuccess;
+  return residues_launch(o, o, (o.rows + kTileRows - 1) / kTileRows, 0, rows_layout(o, bf16), bf16,
+                         nplanes, stream);
+}
+
+cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1, int bf16, int nplanes,
+                             cudaStream_t stream) {
+  const bool r0 = rows_layout(o0, bf16), r1 = rows_layout(o1, bf16);
+  if (o0.rows == 0 || o1.rows == 0 || r0 != r1 || o0.Kp != o1.Kp) {
+    cudaError_t e = launch_residues(o0, bf16, nplanes, stream);
+    return e == cudaSuccess ? launch_residues(o1, bf16, nplanes, stream) : e;
+  }
+  if (o0.Kp == 0) return cudaSuccess;
+  return residues_launch(o0, o1, (o0.rows + kTileRows - 1) / kTileRows,
+                         (o1.rows + kTileRows - 1) / kTileRows, r0, bf16, nplanes, stream);
 }
 
 cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream) {
