@@ -105,19 +105,22 @@ __host__ __device__ constexpr int32_t crt_W(int P, int i) {
 }
 constexpr int kCrtWeightBits = 20;
 
+// The top limb of every C_i and of -M is below 2^14 in magnitude (M < 2^110),
+// so its sum stays within 32 bits: 14 * 127 * 2^14 + 2^10 * 2^14 < 2^25.
 template <int P, int i>
-__host__ __device__ __forceinline__ void crt_terms(const int32_t (&r)[kNumModuli], int64_t (&acc)[4],
-                                                   int32_t& Q) {
+__host__ __device__ __forceinline__ void crt_terms(const int32_t (&r)[kNumModuli], int64_t (&acc)[3],
+                                                   int32_t& acc3, int32_t& Q) {
   if constexpr (i < P) {
     constexpr int32_t c0 = crt_C_limb(P, i, 0), c1 = crt_C_limb(P, i, 1);
     constexpr int32_t c2 = crt_C_limb(P, i, 2), c3 = crt_C_limb(P, i, 3);
+    static_assert(c3 < (1 << 14) && c3 > -(1 << 14), "top limb below 2^14");
     constexpr int32_t w = crt_W(P, i);
     acc[0] += static_cast<int64_t>(r[i]) * c0;
     acc[1] += static_cast<int64_t>(r[i]) * c1;
     acc[2] += static_cast<int64_t>(r[i]) * c2;
-    acc[3] += static_cast<int64_t>(r[i]) * c3;
+    acc3 += r[i] * c3;
     Q += r[i] * w;
-    crt_terms<P, i + 1>(r, acc, Q);
+    crt_terms<P, i + 1>(r, acc, acc3, Q);
   }
 }
 
@@ -129,21 +132,22 @@ template <int P>
 __host__ __device__ __forceinline__ void crt_s128(const int32_t (&r)[kNumModuli], uint64_t& lo,
                                                   uint64_t& hi) {
   static_assert(P >= 1 && P <= kNumModuli, "moduli in use");
-  int64_t acc[4] = {0, 0, 0, 0};
-  int32_t Q = 0;                                   // |Q| < 14 * 127 * 2^19 < 2^30
-  crt_terms<P, 0>(r, acc, Q);
+  int64_t acc[3] = {0, 0, 0};
+  int32_t acc3 = 0, Q = 0;                         // |Q| < 14 * 127 * 2^19 < 2^30
+  crt_terms<P, 0>(r, acc, acc3, Q);
   const int32_t q = (Q + (1 << (kCrtWeightBits - 1))) >> kCrtWeightBits;
+  static_assert(crt_negM_limb(P, 3) < (1 << 14) && crt_negM_limb(P, 3) > -(1 << 14), "top limb");
   acc[0] += static_cast<int64_t>(q) * crt_negM_limb(P, 0);
   acc[1] += static_cast<int64_t>(q) * crt_negM_limb(P, 1);
   acc[2] += static_cast<int64_t>(q) * crt_negM_limb(P, 2);
-  acc[3] += static_cast<int64_t>(q) * crt_negM_limb(P, 3);
+  acc3 += q * crt_negM_limb(P, 3);
   // S = acc0 + acc1 2^32 + acc2 2^64 + acc3 2^96 (mod 2^128); |acc_l| < 2^43
   const uint64_t a0 = static_cast<uint64_t>(acc[0]);
   const uint64_t a1lo = static_cast<uint64_t>(acc[1]) << 32;
   lo = a0 + a1lo;
   const uint64_t carry = lo < a0 ? 1u : 0u;
   hi = static_cast<uint64_t>(acc[0] >> 63) + static_cast<uint64_t>(acc[1] >> 32) + carry +
-       static_cast<uint64_t>(acc[2]) + (static_cast<uint64_t>(acc[3]) << 32);
+       static_cast<uint64_t>(acc[2]) + (static_cast<uint64_t>(static_cast<uint32_t>(acc3)) << 32);
 }
 
 // Exact modular reduction in binary32 (integers below 2^24 are exact there,

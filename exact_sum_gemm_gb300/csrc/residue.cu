@@ -497,9 +497,16 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
 // products, crt_s128 (det_residue.cuh): about 60 integer multiply-adds per
 // output, with compile-time constants for each count of moduli.
 
-// Byte j of a word of four residue bytes, sign-extended.
-__host__ __device__ __forceinline__ int32_t residue_of_word(uint32_t w, int j) {
-  return static_cast<int32_t>(w << (24 - 8 * j)) >> 24;
+// Byte j of a word of four residue bytes, sign-extended: one byte permute
+// whose selector copies byte j and replicates its sign bit into the three
+// bytes above (a selector nibble with its top bit set; __byte_perm keeps only
+// the low three bits of each nibble, so the instruction is written out).
+__device__ __forceinline__ int32_t residue_of_word(uint32_t w, int j) {
+  const uint32_t sj = 8u | static_cast<uint32_t>(j);
+  const uint32_t sel = (sj << 12) | (sj << 8) | (sj << 4) | static_cast<uint32_t>(j);
+  uint32_t d;
+  asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(w), "r"(sel));
+  return static_cast<int32_t>(d);
 }
 
 // RNE_f32(S * 2^E) for a signed 128-bit S = (hi:lo): the binary32 rule,
