@@ -295,6 +295,12 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageResiduePlanes, stream);
     e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M, error + 1, stream);
   }
+  if (e == cudaSuccess) {
+    // the general kernel's tiles need only the routing: it runs beside the
+    // tensor-core GEMMs (the reconstruction skips those tiles)
+    StageScope t(kStageGeneral, stream);
+    e = launch_kulisch(g, s.general, stream);
+  }
   int forked = 0;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
     e = cudaStreamWaitEvent(stream, bs->gemm_done[b], 0);
@@ -323,10 +329,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     join = bs->deep_done[0];
     if (cudaEventRecord(join, bs->side) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
-    return e;
   }
-  StageScope t(kStageGeneral, stream);
-  return launch_kulisch(g, s.general, stream);
+  return e;
 }
 
 }  // namespace
