@@ -655,9 +655,28 @@ __global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs 
   const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
   const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
                       (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
+  // the thread's columns stay fixed: their deep flags and exponents once
+  uint32_t live = 0;                     // bit j: column n0 + j is reconstructed here
+  int colE[kReconCols];
+#pragma unroll
+  for (int j = 0; j < kReconCols; ++j) {
+    colE[j] = 0;
+    if (j < ncols) {
+      const int64_t n = n0 + j;
+      if (ra.countB[n] == 0) live |= 1u << j;                     // else: deep kernel
+      int emB = ra.emaxB[n];
+      emB = emB == kEmaxEmpty ? 0 : emB;
+      colE[j] = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+    }
+  }
+  if (live == 0) return;
+  // all four outputs of a row in one 16-byte store where the layout allows
+  static_assert(kReconCols == 4, "one uint4 of outputs per row");
+  const bool store4 = live == (1u << kReconCols) - 1 && (g.ldc & 3) == 0 &&
+                      (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0;
   for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
     if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
-    if (ra.countA[m] != 0) continue;                              // deep row: full kernel
+    if (ra.countA[m] != 0) continue;                              // deep row: deep kernel
     int emA = ra.emaxA[m];
     emA = emA == kEmaxEmpty ? 0 : emA;
     const int64_t base = m * g.N + n0;
@@ -677,20 +696,25 @@ __global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs 
         }
       }
     }
+    uint32_t out[kReconCols];
 #pragma unroll
     for (int j = 0; j < kReconCols; ++j) {
-      if (j >= ncols) break;
-      const int64_t n = n0 + j;
-      if (ra.countB[n] != 0) continue;                            // deep column: deep kernel
+      out[j] = kNanBits;
+      if (((live >> j) & 1u) == 0u) continue;
       int32_t r[kNumModuli];
 #pragma unroll
       for (int i = 0; i < kNumModuli; ++i) r[i] = residue_of_word(packed[i], j);
       uint64_t slo, shi;
       crt_s128<P>(r, slo, shi);
-      int emB = ra.emaxB[n];
-      emB = emB == kEmaxEmpty ? 0 : emB;
-      const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
-      reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = failed ? kNanBits : round_s128(slo, shi, Es);
+      if (!failed) out[j] = round_s128(slo, shi, emA + colE[j]);
+    }
+    uint32_t* dst = reinterpret_cast<uint32_t*>(g.C) + m * g.ldc + n0;
+    if (store4) {
+      *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+    } else {
+#pragma unroll
+      for (int j = 0; j < kReconCols; ++j)
+        if ((live >> j) & 1u) dst[j] = out[j];
     }
   }
 }
