@@ -19,6 +19,9 @@
 //     epilogue warps of the pair arrive on the leader's acc_free[.];
 //   * each CTA's epilogue reduces its 128 x 256 accumulator modulo p in TMEM
 //     every 832 K exactly as the single-CTA kernel does.
+// Work: the (modulus, 256 x 256 tile) pairs in modulus-major order, so the
+// clusters in flight share few moduli's planes in L2.  Cluster c takes every
+// C-th of them from c on (C clusters), two at a time on the two accumulators.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records an
 // error flag, drains what is in flight and both CTAs meet at a final cluster
 // barrier before TMEM is released.
@@ -94,8 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   const int64_t tiles_n = (a.N + kTileN - 1) / kTileN;
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * tiles_n;
-  const int64_t tile_pairs = (tiles + 1) / 2;
-  const int64_t units = tile_pairs * a.nplanes;
+  const int64_t singles = tiles * a.nplanes;       // (modulus, tile), modulus-major
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -122,10 +124,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::cluster_sync();                     // both CTAs' barriers initialised
   ptx::tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
-  auto unit_at = [&](int64_t unit, int& u, int64_t& t0, int& T) {
-    u = static_cast<int>(unit / tile_pairs);
-    t0 = 2 * (unit - static_cast<int64_t>(u) * tile_pairs);
-    T = t0 + 1 < tiles ? 2 : 1;
+  // The cluster takes singles cluster, cluster + C, cluster + 2C, ... (C
+  // clusters), two at a time: unit j interleaves singles cluster + 2jC and
+  // cluster + (2j + 1)C on the two accumulators (T = 1 if the second is
+  // past the end).  A launch then ends within half a unit of its ideal
+  // length, whatever its tile count.
+  auto unit_at = [&](int64_t j, int64_t (&sg)[2], int& T) {
+    sg[0] = cluster + 2 * j * clusters;
+    sg[1] = sg[0] + clusters;
+    T = sg[1] < singles ? 2 : 1;
+    return sg[0] < singles;
+  };
+  auto single_at = [&](int64_t sgl, int& u, int64_t& t) {
+    u = static_cast<int>(sgl / tiles);
+    t = sgl - static_cast<int64_t>(u) * tiles;
   };
   auto tile_origin = [&](int64_t t, int64_t& m0, int64_t& n0) {
     m0 = (t / tiles_n) * kPairM;
@@ -137,15 +149,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it = 0;
       const uint32_t full_leader = ptx::map_to_cta(ptx::smem_addr(full), 0);
-      for (int64_t unit = cluster; unit < units && ok; unit += clusters) {
-        int u, T;
-        int64_t t0;
-        unit_at(unit, u, t0, T);
+      for (int64_t j = 0; ok; ++j) {
+        int64_t sg[2];
+        int T;
+        if (!unit_at(j, sg, T)) break;
         for (int J = 0; J < T * nch && ok; ++J) {
-          int tt, c;
+          int tt, c, u;
           job_at(J, T, tt, c);
-          int64_t m0, n0;
-          tile_origin(t0 + tt, m0, n0);
+          int64_t t, m0, n0;
+          single_at(sg[tt], u, t);
+          tile_origin(t, m0, n0);
           const int ga = static_cast<int>((m0 + kHalfM * rank) / kPlaneRows);
           const int gb = static_cast<int>((n0 + (kTileN / 2) * rank) / kPlaneRows);
           const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
@@ -183,10 +196,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       uint32_t it = 0;
       uint32_t uses[2] = {0u, 0u};
-      for (int64_t unit = cluster; unit < units && ok; unit += clusters) {
-        int u, T;
-        int64_t t0;
-        unit_at(unit, u, t0, T);
+      for (int64_t j = 0; ok; ++j) {
+        int64_t sg[2];
+        int T;
+        if (!unit_at(j, sg, T)) break;
         for (int J = 0; J < T * nch && ok; ++J) {
           int tt, c;
           job_at(J, T, tt, c);
@@ -231,15 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     uint32_t uses[2] = {0u, 0u};
     const uint32_t free_leader = ptx::map_to_cta(ptx::smem_addr(acc_free), 0);
-    for (int64_t unit = cluster; unit < units && ok; unit += clusters) {
-      int u, T;
-      int64_t t0;
-      unit_at(unit, u, t0, T);
+    for (int64_t j = 0; ok; ++j) {
+      int64_t sg[2];
+      int T;
+      if (!unit_at(j, sg, T)) break;
       for (int J = 0; J < T * nch; ++J) {
-        int tt, c;
+        int tt, c, u;
         job_at(J, T, tt, c);
-        int64_t m0, n0;
-        tile_origin(t0 + tt, m0, n0);
+        int64_t t, m0, n0;
+        single_at(sg[tt], u, t);
+        tile_origin(t, m0, n0);
         const int64_t row = m0 + kHalfM * rank + 32 * g + lane;
         const int acc = tt;
         if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
@@ -350,8 +364,8 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
       !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kTileN / 2))
     return cudaErrorInvalidValue;
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * ((a.N + kTileN - 1) / kTileN);
-  const int64_t units = (tiles + 1) / 2 * a.nplanes;
-  const int64_t clusters = units < max_clusters[dev] ? units : max_clusters[dev];
+  const int64_t singles = tiles * a.nplanes;
+  const int64_t clusters = singles < max_clusters[dev] ? singles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, tmA, tmB, a);
   note_launch();
