@@ -30,6 +30,7 @@
 #include "det_residue.cuh"
 
 #include <type_traits>
+#include <utility>
 
 namespace det {
 namespace {
@@ -402,14 +403,18 @@ __device__ __forceinline__ void write_canonical_digits(int64_t* out, int64_t MN,
 }
 
 // The canonical digits of S * 2^E for a signed 128-bit S = (hi:lo) (a
-// multiple of 2^-298 below 2^277 in magnitude), as one output's 20 planes.
-// Digit j holds bits [32j - off, 32j - off + 32) of S, off = E + 298: the
-// five words of S shifted by off mod 32 land on digits off/32 .. off/32 + 4,
-// digits below are 0 and digits above repeat the sign.  Every digit plane
-// gets its fill value first, then the five words overwrite theirs (the same
-// thread's stores to one address stay in order).
-__device__ __forceinline__ void write_digits_s128(int64_t* out, int64_t MN, uint64_t lo, uint64_t hi,
-                                                  int E, int64_t K, int64_t nf) {
+// multiple of 2^-298 below 2^277 in magnitude), as a window.  Digit j holds
+// bits [32j - off, 32j - off + 32) of S, off = E + 298: the five words of S
+// shifted by off mod 32 land on digits j0 = off/32 .. j0 + 4 (x[0..4]),
+// digits below are 0 and digits above repeat the sign word sx (digits 0-16
+// are unsigned words, digit 17 the signed top).
+struct DigitWindow {
+  int j0;
+  uint32_t x[5];
+  uint32_t sx;
+};
+
+__device__ __forceinline__ DigitWindow digit_window(uint64_t lo, uint64_t hi, int E) {
   int off = E + kLsbBias;
   if (off < 0) {                                // the low -off (< 64) bits are zero
     const int r = -off;
@@ -417,25 +422,79 @@ __device__ __forceinline__ void write_digits_s128(int64_t* out, int64_t MN, uint
     hi = static_cast<uint64_t>(static_cast<int64_t>(hi) >> r);
     off = 0;
   }
-  const int j0 = off >> 5, sh = off & 31;
+  DigitWindow d;
+  d.j0 = off >> 5;
+  const int sh = off & 31;
   const uint32_t w0 = static_cast<uint32_t>(lo), w1 = static_cast<uint32_t>(lo >> 32);
   const uint32_t w2 = static_cast<uint32_t>(hi), w3 = static_cast<uint32_t>(hi >> 32);
-  const uint32_t sx = static_cast<uint32_t>(static_cast<int32_t>(w3) >> 31);
-  const int64_t fill = static_cast<int64_t>(sx);                      // digit value above
+  d.sx = static_cast<uint32_t>(static_cast<int32_t>(w3) >> 31);
+  d.x[0] = w0 << sh;
+  d.x[1] = __funnelshift_l(w0, w1, sh);
+  d.x[2] = __funnelshift_l(w1, w2, sh);
+  d.x[3] = __funnelshift_l(w2, w3, sh);
+  d.x[4] = __funnelshift_l(w3, d.sx, sh);
+  return d;
+}
+
+// int64 value of digit plane j holding the 32-bit word w
+__device__ __forceinline__ int64_t digit_of(uint32_t w, int j) {
+  return j < kDigits - 1 ? static_cast<int64_t>(w) : static_cast<int64_t>(static_cast<int32_t>(w));
+}
+
+// Digit plane j's 32-bit word for a window starting at digit J0 (compile time).
+template <int J0, int j>
+__device__ __forceinline__ uint32_t window_word(const DigitWindow& d) {
+  if constexpr (j < J0) return 0u;
+  else if constexpr (j < J0 + 5) return d.x[j - J0];
+  else return d.sx;
+}
+
+// One output's 20 planes; the window's start J0 is a compile-time constant, so
+// every plane is one store of a known word.
+template <int J0>
+__device__ __forceinline__ void write_window_at(int64_t* out, int64_t MN, const DigitWindow& d, int64_t K,
+                                                int64_t nf) {
+  auto plane = [&](auto jc) {
+    constexpr int j = decltype(jc)::value;
+    out[j * MN] = digit_of(window_word<J0, j>(d), j);
+  };
+  [&]<int... js>(std::integer_sequence<int, js...>) {
+    (plane(std::integral_constant<int, js>{}), ...);
+  }(std::make_integer_sequence<int, kDigits>{});
+  out[kDigits * MN] = K;
+  out[(kDigits + 1) * MN] = nf;
+}
+
+// The same for any start, in the general form (words selected at run time).
+__device__ __forceinline__ void write_window_any(int64_t* out, int64_t MN, const DigitWindow& d,
+                                                 int64_t K, int64_t nf) {
 #pragma unroll
-  for (int j = 0; j < kDigits - 1; ++j) out[j * MN] = j < j0 ? 0 : fill;
-  out[(kDigits - 1) * MN] = static_cast<int64_t>(static_cast<int32_t>(sx));
-  const uint32_t x[5] = {w0 << sh, __funnelshift_l(w0, w1, sh), __funnelshift_l(w1, w2, sh),
-                         __funnelshift_l(w2, w3, sh), __funnelshift_l(w3, sx, sh)};
-  int64_t* dst = out + j0 * MN;
-#pragma unroll
-  for (int i = 0; i < 5; ++i) {
-    const int j = j0 + i;
-    if (j < kDigits - 1) dst[i * MN] = static_cast<int64_t>(x[i]);
-    else if (j == kDigits - 1) dst[i * MN] = static_cast<int64_t>(static_cast<int32_t>(x[i]));
+  for (int j = 0; j < kDigits; ++j) {
+    const int k = j - d.j0;
+    const uint32_t w = k < 0 ? 0u
+                     : k == 0 ? d.x[0] : k == 1 ? d.x[1] : k == 2 ? d.x[2] : k == 3 ? d.x[3]
+                     : k == 4 ? d.x[4] : d.sx;
+    out[j * MN] = digit_of(w, j);
   }
   out[kDigits * MN] = K;
   out[(kDigits + 1) * MN] = nf;
+}
+
+// Dispatch on the window's start.  For finite operands it is at most 14
+// (E <= 2 * 104 - 38, so off = E + 298 < 480); larger starts take the
+// general form.
+__device__ __forceinline__ void write_window(int64_t* out, int64_t MN, const DigitWindow& d, int64_t K,
+                                             int64_t nf) {
+  switch (d.j0) {
+#define DET_WINDOW_CASE(J) \
+  case J: write_window_at<J>(out, MN, d, K, nf); break;
+    DET_WINDOW_CASE(0) DET_WINDOW_CASE(1) DET_WINDOW_CASE(2) DET_WINDOW_CASE(3)
+    DET_WINDOW_CASE(4) DET_WINDOW_CASE(5) DET_WINDOW_CASE(6) DET_WINDOW_CASE(7)
+    DET_WINDOW_CASE(8) DET_WINDOW_CASE(9) DET_WINDOW_CASE(10) DET_WINDOW_CASE(11)
+    DET_WINDOW_CASE(12) DET_WINDOW_CASE(13) DET_WINDOW_CASE(14)
+#undef DET_WINDOW_CASE
+    default: write_window_any(out, MN, d, K, nf);
+  }
 }
 
 // Cold path of one output: the digit route.  Used for det_gemm_partial (the
@@ -777,7 +836,8 @@ __global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
 
 // det_gemm_partial outputs whose row of A and column of B hold no deep
 // element: CRT, then the digits.  One output per thread, so that each of the
-// 20 plane stores of a warp is one contiguous 256-byte write.
+// 20 plane stores of a warp is one contiguous 256-byte write; the digit
+// window's start selects straight-line code with one store per plane.
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
@@ -788,6 +848,7 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
   if (ra.countB[n] != 0) return;                              // deep column: deep kernel
   int emB = ra.emaxB[n];
   emB = emB == kEmaxEmpty ? 0 : emB;
+  const int colE = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
   for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
     if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's outputs
     if (ra.countA[m] != 0) continue;                            // deep row: deep kernel
@@ -799,8 +860,8 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
     for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(ra.res[i * MN + idx]) : 0;
     uint64_t slo, shi;
     crt_s128<P>(r, slo, shi);
-    const int Es = emA + emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
-    write_digits_s128(g.P + idx, MN, slo, shi, Es, g.K, nf);
+    const DigitWindow d = digit_window(slo, shi, emA + colE);
+    write_window(g.P + idx, MN, d, g.K, nf);
   }
 }
 
