@@ -30,7 +30,6 @@
 #include "det_residue.cuh"
 
 #include <type_traits>
-#include <utility>
 
 namespace det {
 namespace {
@@ -451,16 +450,18 @@ __device__ __forceinline__ uint32_t window_word(const DigitWindow& d) {
 
 // One output's 20 planes; the window's start J0 is a compile-time constant, so
 // every plane is one store of a known word.
+template <int J0, int j>
+__device__ __forceinline__ void write_window_planes(int64_t* out, int64_t MN, const DigitWindow& d) {
+  if constexpr (j < kDigits) {
+    out[j * MN] = digit_of(window_word<J0, j>(d), j);
+    write_window_planes<J0, j + 1>(out, MN, d);
+  }
+}
+
 template <int J0>
 __device__ __forceinline__ void write_window_at(int64_t* out, int64_t MN, const DigitWindow& d, int64_t K,
                                                 int64_t nf) {
-  auto plane = [&](auto jc) {
-    constexpr int j = decltype(jc)::value;
-    out[j * MN] = digit_of(window_word<J0, j>(d), j);
-  };
-  [&]<int... js>(std::integer_sequence<int, js...>) {
-    (plane(std::integral_constant<int, js>{}), ...);
-  }(std::make_integer_sequence<int, kDigits>{});
+  write_window_planes<J0, 0>(out, MN, d);
   out[kDigits * MN] = K;
   out[(kDigits + 1) * MN] = nf;
 }
@@ -705,7 +706,7 @@ constexpr int kReconCols = 4;                       // outputs per thread (one r
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
+__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;    // the tensor-core kernel gave up
@@ -733,14 +734,9 @@ __global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs 
   static_assert(kReconCols == 4, "one uint4 of outputs per row");
   const bool store4 = live == (1u << kReconCols) - 1 && (g.ldc & 3) == 0 &&
                       (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0;
-  for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += gridDim.y) {
-    if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) continue;   // general kernel's outputs
-    if (ra.countA[m] != 0) continue;                              // deep row: deep kernel
-    int emA = ra.emaxA[m];
-    emA = emA == kEmaxEmpty ? 0 : emA;
+  const bool vec = vec_ok && ncols == kReconCols;
+  auto load_row = [&](int64_t m, uint32_t (&packed)[kNumModuli]) {
     const int64_t base = m * g.N + n0;
-    uint32_t packed[kNumModuli];
-    const bool vec = vec_ok && ncols == kReconCols;
 #pragma unroll
     for (int i = 0; i < kNumModuli; ++i) {
       packed[i] = 0;
@@ -755,6 +751,12 @@ __global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs 
         }
       }
     }
+  };
+  auto finish_row = [&](int64_t m, const uint32_t (&packed)[kNumModuli]) {
+    if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) return;     // general kernel's outputs
+    if (ra.countA[m] != 0) return;                                // deep row: deep kernel
+    int emA = ra.emaxA[m];
+    emA = emA == kEmaxEmpty ? 0 : emA;
     uint32_t out[kReconCols];
 #pragma unroll
     for (int j = 0; j < kReconCols; ++j) {
@@ -775,6 +777,17 @@ __global__ void __launch_bounds__(kThreads, 5) reconstruct_fast_kernel(GemmArgs 
       for (int j = 0; j < kReconCols; ++j)
         if ((live >> j) & 1u) dst[j] = out[j];
     }
+  };
+  // two rows per step: both rows' residue loads are in flight before either
+  // row's arithmetic
+  const int64_t step = gridDim.y;
+  for (int64_t m = ra.m_begin + blockIdx.y; m < ra.m_end; m += 2 * step) {
+    const bool two = m + step < ra.m_end;
+    uint32_t p0[kNumModuli], p1[kNumModuli];
+    load_row(m, p0);
+    if (two) load_row(m + step, p1);
+    finish_row(m, p0);
+    if (two) finish_row(m + step, p1);
   }
 }
 
@@ -981,8 +994,9 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
     });
   } else {
     const int64_t cols_per_block = int64_t(kThreads) * kReconCols;
+    // blocks walk several rows, two per step (1024 per column of blocks)
     dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
-              static_cast<unsigned>(band < 65535 ? band : 65535));
+              static_cast<unsigned>(band < 1024 ? band : 1024));
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
       reconstruct_fast_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(g, ra);
       return cudaSuccess;
