@@ -282,8 +282,10 @@ __device__ __forceinline__ uint32_t round_w192(W192 t, int E) {
     q = t.w[0] << (-s);                                  // exact: fewer than 24 bits
   } else {
     const int p = s - 1;                                 // index of the rounding bit
+    // p >= 192: all of |t| lies below the rounding bit, below half the least
+    // subnormal, so it rounds to zero (the window below is then all zero)
     const int wi = p >> 6, r = p & 63;
-    const uint64_t lo = wi == 0 ? t.w[0] : (wi == 1 ? t.w[1] : t.w[2]);
+    const uint64_t lo = wi == 0 ? t.w[0] : (wi == 1 ? t.w[1] : (wi == 2 ? t.w[2] : 0u));
     const uint64_t hi = wi == 0 ? t.w[1] : (wi == 1 ? t.w[2] : 0u);
     const uint64_t win = r ? ((lo >> r) | (hi << (64 - r))) : lo;
     const uint64_t below_mask = r ? ((uint64_t(1) << r) - 1) : 0u;
@@ -596,10 +598,13 @@ __device__ __noinline__ uint32_t round_s128_exact(uint64_t lo, uint64_t hi, int 
     if (p < 64) {
       win = p ? ((lo >> p) | (hi << (64 - p))) : lo;
       sticky = p ? (lo & ((uint64_t(1) << p) - 1)) != 0 : false;
-    } else {
+    } else if (p < 128) {
       const int p2 = p - 64;
       win = hi >> p2;
       sticky = lo != 0 || (p2 ? (hi & ((uint64_t(1) << p2) - 1)) != 0 : false);
+    } else {                                             // all of |S| lies below the rounding
+      win = 0;                                           // bit: below half the least
+      sticky = true;                                     // subnormal, so it rounds to zero
     }
     const uint64_t half = win & 1u;
     q = (win >> 1) & 0xFFFFFFu;

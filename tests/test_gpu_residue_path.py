@@ -156,3 +156,18 @@ def test_banded_schedule_matches_single_band_calls(oracle_mod):
     rows = np.array([5, 1500, 2047, 2048, 4095])
     want = np_bits(oracle_mod.gemm(A[rows], B))
     assert_bits_equal(whole[rows], want, "4096^3 rows on both sides of the band edge")
+
+
+@pytest.mark.parametrize("sa,sb", [(-120, -98), (-100, -60), (-64, -32), (-30, -2), (0, 0),
+                                   (16, 48), (60, 40), (100, 30), (124, 110)])
+def test_partial_digit_windows_across_scales(oracle_mod, sa, sb):
+    # N(0,1) operands times 2^sa and 2^sb: the shallow sum S * 2^E lands on
+    # digits (E + 298) / 32 .. + 4 with E = emaxA + emaxB - 38, so these
+    # scales spread the window's first digit over 0 .. 14 (the
+    # digit writer has straight-line code per start).
+    A = wl.normal_f32((96, 512), 41, 0, scale_pow2=sa)
+    B = wl.normal_f32((80, 512), 41, 1, scale_pow2=sb)
+    a, b = dev_f32(A), dev_f32(B)
+    np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B),
+                                  err_msg=f"digits at 2^{sa} x 2^{sb}")
+    assert_bits_equal(bits_of(dg.det_gemm(a, b)), np_bits(oracle_mod.gemm(A, B)), f"2^{sa} x 2^{sb}")
