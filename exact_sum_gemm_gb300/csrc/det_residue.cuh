@@ -115,9 +115,16 @@ __host__ __device__ __forceinline__ void crt_terms(const int32_t (&r)[kNumModuli
     constexpr int32_t c2 = crt_C_limb(P, i, 2), c3 = crt_C_limb(P, i, 3);
     static_assert(c3 < (1 << 14) && c3 > -(1 << 14), "top limb below 2^14");
     constexpr int32_t w = crt_W(P, i);
+#ifdef __CUDA_ARCH__
+    // one 32 x 32 -> 64-bit signed multiply-add each
+    asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[0]) : "r"(r[i]), "n"(c0));
+    asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[1]) : "r"(r[i]), "n"(c1));
+    asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[2]) : "r"(r[i]), "n"(c2));
+#else
     acc[0] += static_cast<int64_t>(r[i]) * c0;
     acc[1] += static_cast<int64_t>(r[i]) * c1;
     acc[2] += static_cast<int64_t>(r[i]) * c2;
+#endif
     acc3 += r[i] * c3;
     Q += r[i] * w;
     crt_terms<P, i + 1>(r, acc, acc3, Q);
