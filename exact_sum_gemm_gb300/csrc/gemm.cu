@@ -165,6 +165,8 @@ constexpr int kMaxBands = 4;
 struct BandSync {
   cudaStream_t hi = nullptr;                       // tensor-core launches
   cudaStream_t side = nullptr;                     // deep-output reconstruction
+  cudaStream_t gen = nullptr;                      // general-tile kernel
+  cudaEvent_t gen_fork = nullptr, gen_done = nullptr;
   cudaEvent_t planes_done[kMaxBands] = {};         // caller's stream -> hi
   cudaEvent_t gemm_done[kMaxBands] = {};           // hi -> caller's stream
   cudaEvent_t fork[kMaxBands] = {};                // caller's stream -> side
@@ -185,6 +187,12 @@ cudaError_t band_sync(int dev, BandSync** out) {
     const int side_prio = greatest < least ? greatest + 1 : greatest;
     if (e == cudaSuccess && b.side == nullptr)
       e = cudaStreamCreateWithPriority(&b.side, cudaStreamNonBlocking, side_prio);
+    if (e == cudaSuccess && b.gen == nullptr)
+      e = cudaStreamCreateWithPriority(&b.gen, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess && b.gen_fork == nullptr)
+      e = cudaEventCreateWithFlags(&b.gen_fork, cudaEventDisableTiming);
+    if (e == cudaSuccess && b.gen_done == nullptr)
+      e = cudaEventCreateWithFlags(&b.gen_done, cudaEventDisableTiming);
     for (int i = 0; i < kMaxBands && e == cudaSuccess; ++i) {
       cudaEvent_t* ev[4] = {&b.planes_done[i], &b.gemm_done[i], &b.fork[i], &b.deep_done[i]};
       for (int k = 0; k < 4 && e == cudaSuccess; ++k)
@@ -295,11 +303,21 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageResiduePlanes, stream);
     e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M, error + 1, stream);
   }
+  bool gen_forked = false;
   if (e == cudaSuccess) {
     // the general kernel's tiles need only the routing: it runs beside the
-    // tensor-core GEMMs (the reconstruction skips those tiles)
-    StageScope t(kStageGeneral, stream);
-    e = launch_kulisch(g, s.general, stream);
+    // tensor-core GEMMs (the reconstruction skips those tiles), on a stream of
+    // its own: it uses shared memory, so it cannot share an SM with a
+    // tensor-core CTA and may wait for the GEMMs, which must not hold up the
+    // reconstruction behind it
+    e = cudaEventRecord(bs->gen_fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->gen, bs->gen_fork, 0);
+    if (e == cudaSuccess) {
+      gen_forked = true;
+      StageScope t(kStageGeneral, bs->gen);
+      e = launch_kulisch(g, s.general, bs->gen);
+    }
+    if (e == cudaSuccess) e = cudaEventRecord(bs->gen_done, bs->gen);
   }
   int forked = 0;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
@@ -323,12 +341,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     }
   }
   for (int b = 0; b < forked && e == cudaSuccess; ++b) e = cudaStreamWaitEvent(stream, bs->deep_done[b], 0);
+  if (e == cudaSuccess && gen_forked) e = cudaStreamWaitEvent(stream, bs->gen_done, 0);
   if (e != cudaSuccess) {
     // keep the caller's stream ordered after everything enqueued on hi and side
     cudaEvent_t join = bs->gemm_done[0];
     if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     join = bs->deep_done[0];
     if (cudaEventRecord(join, bs->side) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
+    if (cudaEventRecord(bs->gen_done, bs->gen) == cudaSuccess) cudaStreamWaitEvent(stream, bs->gen_done, 0);
   }
   return e;
 }
