@@ -25,6 +25,7 @@
 #include <stdint.h>
 
 #include "det_arith.cuh"
+#include "det_crt.cuh"
 #include "det_gemm_internal.cuh"
 #include "det_kernels.h"
 #include "det_residue.cuh"
@@ -556,7 +557,7 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
 //
 // The residue GEMM stores balanced residues r_i (|r_i| <= (p_i - 1)/2) as
 // two's-complement bytes.  The reconstruction rebuilds S as one sum of
-// products, crt_s128 (det_residue.cuh): about 60 integer multiply-adds per
+// products, crt_s128 (det_crt.cuh): about 60 integer multiply-adds per
 // output, with compile-time constants for each count of moduli.
 
 // Byte j of a word of four residue bytes, sign-extended: one byte permute
