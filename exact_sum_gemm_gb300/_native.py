@@ -33,6 +33,7 @@ SIGNATURES = {
     "det_kernel_launches": (ctypes.c_uint64, []),
     "det_stage_timing": (_i32, [_i32]),
     "det_residue_moduli": (_i32, [_i32, _i64]),
+    "det_moduli_used": (_i32, [ctypes.POINTER(_i32), _i32]),
     "det_stage_report": (_i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                                 ctypes.POINTER(_i32), _i32]),
     "det_stage_timeline": (_i32, [ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),

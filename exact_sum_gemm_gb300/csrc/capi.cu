@@ -82,6 +82,11 @@ int det_residue_moduli(det_dtype dtype, int64_t K) {
   return det::residue_planes_needed(a);
 }
 
+int det_moduli_used(int* out, int max) {
+  if (max < 0) return -1;
+  return det::moduli_record(out, max);
+}
+
 uint64_t det_kernel_launches(void) { return det::g_launches.load(std::memory_order_relaxed); }
 
 const char* det_status_string(det_status s) {

@@ -9,7 +9,7 @@
 namespace det {
 
 constexpr int kTile = 64;                 // band kernel output tile (and routing unit)
-constexpr int kDeepGap = 19;              // "deep" element: more than 19 binades below its row max
+constexpr int kDeepGap = 18;              // "deep" element: more than 18 binades below its row max
 constexpr int kEmaxEmpty = static_cast<int>(0x80808080u);   // memset(0x80) pattern: no live element
 
 // Device scratch of one det_gemm / det_gemm_partial call.

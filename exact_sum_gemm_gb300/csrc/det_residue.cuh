@@ -14,8 +14,8 @@ namespace det {
 // integers up to 256), so a product of two is at most 138^2 = 19044 in
 // magnitude, and 832 such products plus a reduced carry (< 131) stay below
 // 2^24, where fp32 accumulation is exact.  The product of all 14 moduli
-// exceeds 2^109, enough for |S| < 2^19 * 2^86 * 2 (f32 shallow integers are
-// below 2^(24+19)).
+// exceeds 2^109, enough for |S| < 2^19 * 2^84 * 2 (1 + 2^-7) (f32 shallow
+// integers are below 2^(24+18)).
 constexpr int kNumModuli = 14;
 __host__ __device__ constexpr int modulus(int i) {
   return i == 0 ? 255 : i == 1 ? 253 : i == 2 ? 251 : i == 3 ? 247 : i == 4 ? 241 : i == 5 ? 239
@@ -84,7 +84,16 @@ struct ResidueOperand {
   int* list_count;            // [rows], zeroed before the launch
   uint2* list;                // [rows][cap]: (k, raw bits) of deep / non-finite elements
   int cap;
+  unsigned long long* norm;   // [rows], zeroed before the launch: an upper bound of
+                              // sum_k X_int^2 / 2^kNormShift over the row's shallow elements
 };
+
+// The fewest moduli with compiled kernels (f32 12, bf16 8).
+__host__ __device__ constexpr int planes_least(int bf16) { return bf16 ? 8 : 12; }
+
+// Row norms are summed in units of 2^norm_shift (f32: |X_int| < 2^42, so a
+// row of K <= 2^19 sums below 2^51 units; bf16: |X_int| < 2^26, below 2^55).
+__host__ __device__ constexpr int norm_shift(int bf16) { return bf16 ? 16 : 52; }
 
 struct ReconArgs {
   const int8_t* res;          // [nplanes][M][N] balanced residues, |r| <= (p_i - 1) / 2
@@ -99,9 +108,26 @@ struct ReconArgs {
   int cap;
   const int* error;           // nonzero: the tensor-core kernel gave up (outputs NaN)
   int64_t m_begin, m_end;     // rows of C handled by this launch (a band)
+  const int* used;            // moduli this band uses (device int, <= nplanes), or null
 };
 
+// Moduli the worst case of this dtype and K needs (the planes are written for
+// this many), and the fewest a band may use (compiled kernel counts).
 int residue_planes_needed(const GemmArgs& g);
+int residue_planes_least(int bf16);
+// Diagnostic: the counts the last residue-path call chose, one per row band
+// (copied from device memory: synchronises with the device).  Returns the
+// number written (at most max), or -1 on a CUDA error.
+int moduli_record(int* out, int max);
+void note_moduli_bands(int bands);
+// One block: the moduli count of a row band, the smallest in [least, most]
+// whose product exceeds 2 (1 + 2^-7) sqrt(max normA * max normB) 2^shift,
+// written to *used (a Cauchy-Schwarz bound of every |S| in the band).
+// maxima: two zeroed 8-byte slots of scratch per launch.
+cudaError_t launch_moduli(const unsigned long long* normA, int64_t rowsA,
+                          const unsigned long long* normB, int64_t rowsB, int bf16, int least,
+                          int most, int* used, int band, unsigned long long* maxima,
+                          cudaStream_t stream);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
 // Two operands' planes in one launch (one grid covering both).
 cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1, int bf16, int nplanes,
@@ -123,8 +149,16 @@ struct ResGemmArgs {
   int8_t* res;                // [nplanes][.][N] balanced residues: plane u of row m at
   int64_t res_plane;          //   res + u * res_plane + m * N
   int* error;
+  const int* used;            // moduli to compute (device int, in [used_min, nplanes]), or
+  int used_min;               //   null for all nplanes; the grid is sized for used_min
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
+// Moduli a GEMM launch computes (every CTA reads the same device int).
+__device__ __forceinline__ int planes_used(const ResGemmArgs& a) {
+  if (a.used == nullptr) return a.nplanes;
+  const int u = *a.used;
+  return u < a.used_min ? a.used_min : (u > a.nplanes ? a.nplanes : u);
+}
 // The same GEMM with 256 x 256 tiles over CTA pairs (cta_group::2); returns
 // cudaErrorNotSupported (nothing enqueued) where clusters of two cannot run.
 cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream);

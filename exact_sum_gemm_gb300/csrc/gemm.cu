@@ -16,6 +16,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <math.h>
+
 #include <mutex>
 
 #include "det_arith.cuh"
@@ -127,16 +129,25 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
   return e != cudaSuccess ? e : f;
 }
 
+constexpr int kMaxBands = 4;
+
 struct ResidueScratch {
   size_t bytes;
-  size_t off_counts, off_deep_idx, off_listA, off_listB, off_planesA, off_planesB, off_res;
+  size_t off_counts, off_norms, zero_bytes, off_deep_idx, off_listA, off_listB, off_planesA,
+      off_planesB, off_res;
 };
 
 ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int cap) {
   ResidueScratch r{};
   size_t b = align_up(scratch_bytes(g, 0), 1024);
-  r.off_counts = b;                     // countA [M], countB [N], error, deep-row/col counters [2]
-  b = align_up(b + sizeof(int) * size_t(g.M + g.N + 3), 1024);
+  // zeroed together: countA [M], countB [N], error, deep-row/col counters [2],
+  // moduli per band [kMaxBands]; then the row-norm bounds normA [M], normB [N]
+  // and each band's two norm maxima [2 kMaxBands]
+  r.off_counts = b;
+  r.off_norms = align_up(b + sizeof(int) * size_t(g.M + g.N + 3 + kMaxBands), 8);
+  b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + g.N + 2 * kMaxBands);
+  r.zero_bytes = b - r.off_counts;
+  b = align_up(b, 1024);
   r.off_deep_idx = b;                    // deep rows [M], deep columns [N]
   b = align_up(b + sizeof(int) * size_t(g.M + g.N), 1024);
   r.off_listA = b;
@@ -160,10 +171,9 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
 // deep elements are reconstructed on a second library stream beside its
 // other outputs (that kernel mostly waits on memory).  Only stream order and
 // events connect the streams (no kernel waits on another).
-constexpr int kMaxBands = 4;
-
 struct BandSync {
-  cudaStream_t hi = nullptr;                       // tensor-core launches
+  cudaStream_t hi = nullptr;                       // tensor-core launches of even bands
+  cudaStream_t hi2 = nullptr;                      // ... and of odd bands
   cudaStream_t side = nullptr;                     // deep-output reconstruction
   cudaStream_t gen = nullptr;                      // general-tile kernel
   cudaEvent_t gen_fork = nullptr, gen_done = nullptr;
@@ -182,6 +192,8 @@ cudaError_t band_sync(int dev, BandSync** out) {
     cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
     cudaStream_t hi = nullptr;
     if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&hi, cudaStreamNonBlocking, greatest);
+    if (e == cudaSuccess && b.hi2 == nullptr)
+      e = cudaStreamCreateWithPriority(&b.hi2, cudaStreamNonBlocking, greatest);
     // the deep kernel's few blocks go ahead of the caller's kernels, behind
     // the tensor-core launches
     const int side_prio = greatest < least ? greatest + 1 : greatest;
@@ -209,16 +221,24 @@ cudaError_t band_sync(int dev, BandSync** out) {
 }
 
 // Row bands: two bands of whole 256-row tiles once each still fills the GPU
-// with tensor-core work.  (Measured at 4096^3: one band, or three or four,
-// including a short last band, were slower: each extra band re-reads B's
-// planes and adds a tensor-core launch with its tail.)
+// with tensor-core work.  Band 0's reconstruction runs beside band 1's GEMM,
+// band 1's after the last GEMM; a GEMM's time grows with K and a
+// reconstruction's does not, so the longer K, the larger band 0.  Measured
+// with the two GEMMs on two streams: at 4096 x 4096, 8 + 8 tiles were best
+// for K = 2048 and 11 + 5 for K = 4096 (8 + 8: 1.5 % slower; 3 or 4 bands:
+// 1.5-6 % slower); at 2048 x 4096 x 4096, 5 + 3.
 int band_bounds(const GemmArgs& g, int64_t (&edge)[kMaxBands + 1]) {
   edge[0] = 0;
   if (g.M < 2048) {
     edge[1] = g.M;
     return 1;
   }
-  edge[1] = (g.M + 1) / 2 / 256 * 256;
+  const int64_t tiles = (g.M + 255) / 256;
+  double f = 0.5 + 0.19 * log2(static_cast<double>(g.K) / 2048.0);
+  f = f < 0.5 ? 0.5 : (f > 0.69 ? 0.69 : f);
+  int64_t t0 = static_cast<int64_t>(static_cast<double>(tiles) * f);
+  t0 = t0 < 1 ? 1 : (t0 > tiles - 1 ? tiles - 1 : t0);
+  edge[1] = t0 * 256;
   edge[2] = g.M;
   return 2;
 }
@@ -234,10 +254,18 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   e = band_sync(dev, &bs);
   if (e != cudaSuccess) return e;
   const cudaStream_t hi = bs->hi;
+  // band b's GEMM on hi (even b) or hi2 (odd b): the next band's CTA pairs
+  // take the SMs that the previous band's pairs leave as they finish, instead
+  // of waiting for its last pair (a band's work rarely divides evenly among
+  // the pairs)
+  auto hi_of = [&](int b) { return (b & 1) ? bs->hi2 : hi; };
 
   const Scratch s = carve_scratch(base, g, 0);
   int* counts = reinterpret_cast<int*>(base + L.off_counts);
   int* error = counts + g.M + g.N;
+  int* used = error + 3;                                             // moduli per band
+  unsigned long long* norms = reinterpret_cast<unsigned long long*>(base + L.off_norms);
+  const int least = residue_planes_least(g.bf16);
   uint2* listA = reinterpret_cast<uint2*>(base + L.off_listA);
   uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
   __nv_bfloat16* planesA = reinterpret_cast<__nv_bfloat16*>(base + L.off_planesA);
@@ -246,14 +274,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   int* deep_rows = reinterpret_cast<int*>(base + L.off_deep_idx);   // [M] rows, then [N] columns
   int64_t edge[kMaxBands + 1];
   const int nb = band_bounds(g, edge);
+  note_moduli_bands(nb);
   const int64_t nkb = Kp / kStageK;
   const size_t es = g.bf16 ? 2 : 4;
 
   {
     StageScope t(kStagePrepass, stream);
     e = launch_emax(g, s, stream);
-    if (e == cudaSuccess)
-      e = cudaMemsetAsync(counts, 0, sizeof(int) * size_t(g.M + g.N + 3), stream);
+    if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, L.zero_bytes, stream);
   }
   if (e != cudaSuccess) return e;
   // the residue kernels' deep-list counters double as the rows' deep counts,
@@ -263,41 +291,50 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
     return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
                           planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
-                          counts + m0, listA + m0 * cap, cap};
+                          counts + m0, listA + m0 * cap, cap, norms + m0};
   };
   auto planes_of_band = [&](int b) { return launch_residues(operand_of_band(b), g.bf16, nplanes, stream); };
+  // the band's moduli count, once its rows' and B's norm bounds are complete
+  auto moduli_of_band = [&](int b) {
+    return launch_moduli(norms + edge[b], edge[b + 1] - edge[b], norms + g.M, g.N, g.bf16, least,
+                         nplanes, used + b, b, norms + g.M + g.N + 2 * b, stream);
+  };
   auto gemm_of_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
-    StageScope t(kStageResidueGemm, hi);
+    const cudaStream_t hs = hi_of(b);
+    StageScope t(kStageResidueGemm, hs);
     ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
-                   rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error};
+                   rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error, used + b, least};
     // 256 x 256 tiles on CTA pairs, unless a single 128-row tile covers M or
     // the device cannot run clusters of two
     if (rows > 128) {
-      const cudaError_t ep = launch_residue_gemm_pair(rg, hi);
+      const cudaError_t ep = launch_residue_gemm_pair(rg, hs);
       if (ep != cudaErrorNotSupported) return ep;
     }
-    return launch_residue_gemm(rg, hi);
+    return launch_residue_gemm(rg, hs);
   };
   {
     StageScope t(kStageResiduePlanes, stream);
     // B's planes and band 0's A planes in one launch
-    ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap};
+    ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
+                      norms + g.M};
     e = launch_residues2(rb, operand_of_band(0), g.bf16, nplanes, stream);
+    if (e == cudaSuccess) e = moduli_of_band(0);
   }
   if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[0], stream);
-  if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, bs->planes_done[0], 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(0), bs->planes_done[0], 0);
   if (e == cudaSuccess) e = gemm_of_band(0);
-  if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[0], hi);
+  if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[0], hi_of(0));
   for (int b = 1; b < nb && e == cudaSuccess; ++b) {
     {
       StageScope t(kStageResiduePlanes, stream);
       e = planes_of_band(b);
+      if (e == cudaSuccess) e = moduli_of_band(b);
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[b], stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi, bs->planes_done[b], 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(b), bs->planes_done[b], 0);
     if (e == cudaSuccess) e = gemm_of_band(b);
-    if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[b], hi);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[b], hi_of(b));
   }
   if (e == cudaSuccess) {
     StageScope t(kStageResiduePlanes, stream);
@@ -328,7 +365,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     forked = b + 1;
     const int64_t m0 = edge[b], m1 = edge[b + 1];
     ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
-                 error, m0, m1};
+                 error, m0, m1, used + b};
     {
       // deep-row/column lists, and their two counters right after the error flag
       StageScope t(kStageReconstruct, bs->side);
@@ -343,9 +380,10 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   for (int b = 0; b < forked && e == cudaSuccess; ++b) e = cudaStreamWaitEvent(stream, bs->deep_done[b], 0);
   if (e == cudaSuccess && gen_forked) e = cudaStreamWaitEvent(stream, bs->gen_done, 0);
   if (e != cudaSuccess) {
-    // keep the caller's stream ordered after everything enqueued on hi and side
+    // keep the caller's stream ordered after everything enqueued on hi, hi2, side and gen
     cudaEvent_t join = bs->gemm_done[0];
     if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
+    if (cudaEventRecord(join, bs->hi2) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     join = bs->deep_done[0];
     if (cudaEventRecord(join, bs->side) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     if (cudaEventRecord(bs->gen_done, bs->gen) == cudaSuccess) cudaStreamWaitEvent(stream, bs->gen_done, 0);

@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   const int64_t tiles_n = (a.N + kTileN - 1) / kTileN;
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * tiles_n;
-  const int64_t singles = tiles * a.nplanes;       // (modulus, tile), modulus-major
+  const int64_t singles = tiles * planes_used(a);  // (modulus, tile), modulus-major
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -364,7 +364,9 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
       !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kTileN / 2))
     return cudaErrorInvalidValue;
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * ((a.N + kTileN - 1) / kTileN);
-  const int64_t singles = tiles * a.nplanes;
+  // sized for the fewest moduli the launch may compute, so every cluster
+  // has at least one item whatever count the device chooses
+  const int64_t singles = tiles * (a.used != nullptr ? a.used_min : a.nplanes);
   const int64_t clusters = singles < max_clusters[dev] ? singles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, tmA, tmB, a);

@@ -4,18 +4,24 @@
 //                       (CRT) + deep products -> round once (or digits)
 //
 // Shallow elements.  For a row r of an operand with largest last-bit
-// exponent emax[r], an element m*2^e with e >= emax[r] - 19 is the integer
-//     X_int = m * 2^(e - emax[r] + 19)
-// times 2^(emax[r] - 19), with |X_int| < 2^43 (f32) or 2^27 (bf16, whose
+// exponent emax[r], an element m*2^e with e >= emax[r] - 18 is the integer
+//     X_int = m * 2^(e - emax[r] + 18)
+// times 2^(emax[r] - 18), with |X_int| < 2^42 (f32) or 2^26 (bf16, whose
 // significand has 8 bits).  So for an output (m, n) the shallow products sum
-// to 2^(emaxA[m] + emaxB[n] - 38) * S with S = sum_k A_int[m,k] * B_int[n,k],
-// an exact integer dot product, |S| < K * 2^86.  S is computed modulo
-// kNumModuli small odd pairwise-coprime moduli (residues in bf16 planes,
-// multiplied on tensor cores with exact fp32 accumulation) and rebuilt here
-// by the Chinese remainder theorem in Garner's mixed-radix form: the moduli's
-// product exceeds 2|S|.  All the small modular arithmetic runs in exact
-// binary32 on the FMA pipes.
-// Deep elements (more than 19 binades below the row max) and non-finite ones
+// to 2^(emaxA[m] + emaxB[n] - 36) * S with S = sum_k A_int[m,k] * B_int[n,k],
+// an exact integer dot product, |S| <= ||A_int[m,:]|| ||B_int[n,:]|| (Cauchy-
+// Schwarz) <= K * 2^84.  S is computed modulo P small odd pairwise-coprime
+// moduli (residues in bf16 planes, multiplied on tensor cores with exact fp32
+// accumulation) and rebuilt here by the Chinese remainder theorem: the
+// moduli's product exceeds 2|S| (1 + 2^-7).  The planes are written for the
+// count that the worst case K * 2^84 needs; the residue kernel also sums an
+// upper bound of each row's squared norm, and a one-block kernel picks per
+// row band the smallest count that the Cauchy-Schwarz bound allows (12 rather
+// than 13 for N(0,1) data at K = 4096).  The tensor-core GEMM and the
+// reconstruction read that count from device memory, so no host round trip
+// is needed.  All the small modular arithmetic runs in exact binary32 on the
+// FMA pipes.
+// Deep elements (more than 18 binades below the row max) and non-finite ones
 // are left out of the planes and listed per row; their products are added
 // exactly, one by one, during reconstruction.  Together this is the exact sum
 // of the products rounded once to fp32, as the det-train page's "Method"
@@ -30,6 +36,7 @@
 #include "det_kernels.h"
 #include "det_residue.cuh"
 
+#include <atomic>
 #include <type_traits>
 
 namespace det {
@@ -47,7 +54,7 @@ __device__ __forceinline__ float near_mod(float a) {
 }
 
 // A residue, modulo the compile-time modulus p, of the integer x * 2^s given
-// x (|x| < 2^24, exact in binary32) and pw = 2^s (s in [0, 19]):
+// x (|x| < 2^24, exact in binary32) and pw = 2^s (s in [0, 18]):
 //   r1 = x mod p (|r1| < 131),  u = r1 * 2^s (exact, |u| < 2^26),
 //   result = u mod p, with |result| <= 138.
 // A zero residue is +0 (x = +0 gives r1 = +0, and pw > 0).
@@ -72,6 +79,29 @@ __device__ __forceinline__ void write_residue_pairs(uint32_t* dst, float x0, flo
     dst[i * (kPlaneRows * kStageK / 2)] = bf16_pair(residue_f32<p>(x0, pw0), residue_f32<p>(x1, pw1));
     write_residue_pairs<i + 1, P>(dst, x0, pw0, x1, pw1);
   }
+}
+
+// Adds the shallow elements' X_int^2 / 2^norm_shift held by this thread to
+// its row's norm bound.  The kLanes neighbouring lanes that share the row
+// reduce first (every step rounds to nearest: at most 8 roundings of
+// positive values, relative error below 2^-20); one lane then adds the sum
+// scaled by 1 + 2^-19 and converted upwards, never less than the exact sum.
+// Zero, deep and padding elements carry x = 0.
+template <int kBf16, int kLanes, int kN>
+__device__ __forceinline__ void add_row_norm(const ResidueOperand& o, int64_t gr, const float (&x)[kN],
+                                             const float (&pw)[kN]) {
+  constexpr float kHalfShift = kBf16 ? 0x1p-8f : 0x1p-26f;      // 2^(-norm_shift / 2)
+  static_assert(norm_shift(kBf16) == (kBf16 ? 16 : 52), "kHalfShift squared is 2^-norm_shift");
+  float sum = 0.0f;
+#pragma unroll
+  for (int h = 0; h < kN; ++h) {
+    const float f = __fmul_rn(__fmul_rn(x[h], pw[h]), kHalfShift);   // exact
+    sum = __fmaf_rn(f, f, sum);
+  }
+#pragma unroll
+  for (int w = kLanes / 2; w >= 1; w /= 2) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, w));
+  if ((threadIdx.x & (kLanes - 1)) == 0 && gr < o.rows && sum > 0.0f && o.norm != nullptr)
+    atomicAdd(o.norm + gr, __float2ull_ru(__fmul_ru(sum, 1.0f + 0x1p-19f)));
 }
 
 // One block: one group of 32 rows x one 64-k stage of one operand; each
@@ -126,7 +156,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, Re
       // (exactly) so that |X_int| < 2^27; the reconstruction scales back by 2^32
       const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
       x[h] = static_cast<float>(deep ? 0 : mi);                        // exact: |mi| < 2^24
-      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 19]
+      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 18]
       if (deep && gk + h < o.K && gr < o.rows) {
         const int slot = atomicAdd(o.list_count + gr, 1);
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
@@ -136,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, Re
         o.planes + (by * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
         r * kStageK + kk);
     write_residue_pairs<0, P>(dst, x[0], pw[0], x[1], pw[1]);
+    add_row_norm<kBf16, 32>(o, gr, x, pw);                  // a warp covers the row's stage
   }
 }
 
@@ -218,6 +249,7 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
         o.planes + (by * nkb + int64_t(blockIdx.x)) * P * kPlaneRows * kStageK +
         r * kStageK + kq);
     write_residue_quads<0, P>(dst, x, pw);
+    add_row_norm<kBf16, 16>(o, gr, x, pw);                  // a half-warp covers the row's stage
   }
 }
 
@@ -707,12 +739,26 @@ __device__ __noinline__ bool add_deep_products(const GemmArgs& g, const ReconArg
   return fits;
 }
 
+// Calls f with the moduli count `used` as a compile-time constant, for
+// counts from the least compiled one up to P (a count outside that range
+// takes the nearer end; the host never passes one).
+template <int kBf16, int P, typename F>
+__device__ __forceinline__ void with_used_planes(int used, F&& f) {
+  if constexpr (P > planes_least(kBf16)) {
+    if (used < P) {
+      with_used_planes<kBf16, P - 1>(used, f);
+      return;
+    }
+  }
+  f(std::integral_constant<int, P>{});
+}
+
 constexpr int kReconCols = 4;                       // outputs per thread (one row)
 
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
+__device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const ReconArgs& ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;    // the tensor-core kernel gave up
@@ -797,14 +843,22 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
   }
 }
 
+// The launch is compiled for the planes' count P and runs the body for the
+// band's count (ReconArgs::used).
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
+  with_used_planes<kBf16, P>(ra.used ? *ra.used : P,
+                             [&](auto Q) { reconstruct_fast_body<kBf16, decltype(Q)::value>(g, ra); });
+}
+
 // Outputs with deep entries: every output of a deep row, then every output of
 // a deep column outside the deep rows.  Dense work list, so the warps stay
 // full.  It shares nothing with the fast kernels but the residues (read
 // only), so it runs beside them.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
-    GemmArgs g, ReconArgs ra, const int* rows,
-    const int* cols, const int* nrc) {
+__device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const ReconArgs& ra,
+                                                      const int* rows, const int* cols,
+                                                      const int* nrc) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;
@@ -853,12 +907,20 @@ __global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
   }
 }
 
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
+    GemmArgs g, ReconArgs ra, const int* rows, const int* cols, const int* nrc) {
+  with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
+    reconstruct_deep_body<kBf16, decltype(Q)::value>(g, ra, rows, cols, nrc);
+  });
+}
+
 // det_gemm_partial outputs whose row of A and column of B hold no deep
 // element: CRT, then the digits.  One output per thread, so that each of the
 // 20 plane stores of a warp is one contiguous 256-byte write; the digit
 // window's start selects straight-line code with one store per plane.
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
+__device__ __forceinline__ void partial_fast_body(const GemmArgs& g, const ReconArgs& ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
@@ -897,6 +959,12 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
   }
 }
 
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
+  with_used_planes<kBf16, P>(ra.used ? *ra.used : P,
+                             [&](auto Q) { partial_fast_body<kBf16, decltype(Q)::value>(g, ra); });
+}
+
 // Moduli counts with compiled kernels: f32 operands need 12 to 14 moduli
 // (K from 1 to 2^19), bf16 operands 8 to 10.  A call uses the smallest
 // compiled count that covers its bound (more moduli never change the result).
@@ -922,7 +990,7 @@ cudaError_t with_planes(int bf16, int P, F&& launch) {
 }  // namespace
 
 int residue_planes_needed(const GemmArgs& g) {
-  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^19.  The CRT sum needs
+  // |S| <= K * maxA * maxB with max = (2^bits - 1) * 2^18.  The CRT sum needs
   // prod > 2|S| (1 + 2^-7): the margin lets its fixed-point quotient round
   // to the right integer (crt_s128).
   const unsigned __int128 sig = g.bf16 ? 0xFFu : 0xFFFFFFu;
@@ -930,12 +998,108 @@ int residue_planes_needed(const GemmArgs& g) {
   const unsigned __int128 twice = static_cast<unsigned __int128>(g.K > 0 ? g.K : 1) * mx * mx * 2;
   const unsigned __int128 bound = twice + (twice >> 7);
   unsigned __int128 prod = 1;
-  const int least = g.bf16 ? 8 : 12;
+  const int least = planes_least(g.bf16);
   for (int i = 0; i < kNumModuli; ++i) {
     prod *= static_cast<unsigned>(modulus(i));
     if (prod > bound) return i + 1 < least ? least : i + 1;
   }
   return -1;
+}
+
+int residue_planes_least(int bf16) { return planes_least(bf16); }
+
+// The moduli counts most recently chosen per row band (a diagnostic,
+// det_moduli_used; concurrent calls overwrite one another's entries).
+constexpr int kModuliRecord = 8;
+__device__ int g_moduli_record[kModuliRecord];
+
+namespace {
+
+// One block.  With a = the largest row-norm bound of the band's rows of A and
+// b = that of B's rows (units of 2^norm_shift), every output of the band has
+// |S| <= sqrt(a b) 2^shift (Cauchy-Schwarz).  The band takes the fewest moduli
+// P in [least, most] with prod_P^2 > 4 (1 + 2^-7)^2 a b 2^(2 shift); the static
+// count `most` covers every input.  The double arithmetic below rounds to
+// nearest in a few dozen steps (relative error below 2^-47), which the factor
+// 1 + 2^-30 on the right-hand side more than covers.
+// No shared memory: a kernel that needs some cannot start on an SM whose
+// shared memory is configured for a running tensor-core GEMM, so this one
+// would wait for the GEMM to end.  The warps meet through atomicMax on two
+// zeroed slots (maxima[0..1]) instead.
+constexpr int kModuliThreads = 512;
+constexpr int kModuliUnroll = 4;
+
+__device__ __forceinline__ unsigned long long max_of_rows(const unsigned long long* v, int64_t n) {
+  unsigned long long m[kModuliUnroll] = {};
+  for (int64_t i = threadIdx.x; i < n; i += int64_t(kModuliUnroll) * kModuliThreads) {
+#pragma unroll
+    for (int u = 0; u < kModuliUnroll; ++u) {
+      const int64_t k = i + int64_t(u) * kModuliThreads;
+      if (k < n) m[u] = max(m[u], __ldcg(v + k));       // all loads of a step in flight
+    }
+  }
+#pragma unroll
+  for (int u = 1; u < kModuliUnroll; ++u) m[0] = max(m[0], m[u]);
+#pragma unroll
+  for (int w = 16; w >= 1; w /= 2) m[0] = max(m[0], __shfl_xor_sync(0xFFFFFFFFu, m[0], w));
+  return m[0];
+}
+
+__global__ void __launch_bounds__(kModuliThreads) moduli_kernel(
+    const unsigned long long* normA, int64_t rowsA, const unsigned long long* normB, int64_t rowsB,
+    int bf16, int least, int most, int* used, int band, unsigned long long* maxima) {
+  const unsigned long long a_w = max_of_rows(normA, rowsA);
+  const unsigned long long b_w = max_of_rows(normB, rowsB);
+  if ((threadIdx.x & 31) == 0) {
+    atomicMax(maxima, a_w);
+    atomicMax(maxima + 1, b_w);
+  }
+  __syncthreads();
+  if (threadIdx.x != 0) return;
+  const unsigned long long a = atomicAdd(maxima, 0ull);        // read at L2, after every warp
+  const unsigned long long b = atomicAdd(maxima + 1, 0ull);
+  const double margin = (1.0 + 0x1p-7) * (1.0 + 0x1p-7) * (1.0 + 0x1p-30);
+  const double rhs = 4.0 * margin * static_cast<double>(a) * static_cast<double>(b) *
+                     ldexp(1.0, 2 * norm_shift(bf16));
+  int P = most;
+  double prod = 1.0;
+  for (int i = 0; i < most; ++i) {
+    prod *= static_cast<double>(modulus(i));
+    if (i + 1 >= least && prod * prod > rhs) {
+      P = i + 1;
+      break;
+    }
+  }
+  *used = P;
+  if (band >= 0 && band < kModuliRecord) g_moduli_record[band] = P;
+}
+
+}  // namespace
+
+cudaError_t launch_moduli(const unsigned long long* normA, int64_t rowsA,
+                          const unsigned long long* normB, int64_t rowsB, int bf16, int least,
+                          int most, int* used, int band, unsigned long long* maxima,
+                          cudaStream_t stream) {
+  moduli_kernel<<<1, kModuliThreads, 0, stream>>>(normA, rowsA, normB, rowsB, bf16, least, most,
+                                                  used, band, maxima);
+  note_launch();
+  return cudaGetLastError();
+}
+
+namespace {
+std::atomic<int> g_moduli_bands{0};
+}  // namespace
+
+void note_moduli_bands(int bands) { g_moduli_bands.store(bands, std::memory_order_relaxed); }
+
+int moduli_record(int* out, int max) {
+  int rec[kModuliRecord];
+  if (cudaMemcpyFromSymbol(rec, g_moduli_record, sizeof(rec)) != cudaSuccess) return -1;
+  int n = g_moduli_bands.load(std::memory_order_relaxed);
+  n = n < kModuliRecord ? n : kModuliRecord;
+  n = n < max ? n : max;
+  for (int i = 0; i < n && out != nullptr; ++i) out[i] = rec[i];
+  return n;
 }
 
 namespace {

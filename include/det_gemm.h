@@ -94,6 +94,18 @@ int det_stage_timing(int enable);
  * for this dtype and K: enough that their product exceeds twice the largest
  * possible |sum of shallow products| (0 for K = 0; -1 for bad arguments). */
 int det_residue_moduli(det_dtype dtype, int64_t K);
+
+/* Diagnostic for benchmarks: the moduli counts the most recent residue-path
+ * det_gemm / det_gemm_partial call on the current device used, one per row
+ * band of C, in band order.  The planes are written for det_residue_moduli's
+ * worst-case count; each band then computes only as many moduli as a
+ * Cauchy-Schwarz bound of its exact dot products needs (|S| <= |row of A|
+ * |row of B| on the integer grid; fewer moduli for typical data).  Writes up
+ * to `max` counts to `out` (may be NULL) and returns how many the call had
+ * (capped at `max`), or -1 on a CUDA error.  Reads device memory, so it
+ * synchronises with the device; concurrent calls overwrite one another's
+ * record. */
+int det_moduli_used(int* out, int max);
 int det_stage_report(const char** names, double* total_ms, int* counts, int max);
 
 /* The same records as a timeline, in the order the stages were enqueued:

@@ -1,14 +1,17 @@
 """Parity of the tensor-core residue path against the oracle, bit for bit.
 
 det_gemm routes tiles whose rows and columns hold few "deep" elements (more
-than 19 binades below their row maximum) to the residue decomposition on the
+than 18 binades below their row maximum) to the residue decomposition on the
 tensor cores, and other tiles to the general Kulisch kernel.  These cases aim
 at the residue path's own corners: the longest K (14 moduli, 631 exact fp32
 accumulation windows reduced in TMEM), bf16 planes, deep elements handled
 from the per-row lists (inside and outside the 192-bit window), non-finite
-values next to deep ones, and matrices whose tiles are split between the two
-kernels.  Every expected value comes from the oracle.
+values next to deep ones, matrices whose tiles are split between the two
+kernels, and the per-band moduli count at the edge of its Cauchy-Schwarz
+bound.  Every expected value comes from the oracle.
 """
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -18,6 +21,54 @@ from exact_sum_gemm_gb300 import workloads as wl
 from gpu_util import assert_bits_equal, bits_of, dev_bf16, dev_f32, np_bits
 
 pytestmark = pytest.mark.gpu
+
+
+def moduli_used():
+    """Moduli counts (one per row band) of the last residue-path call."""
+    out = (ctypes.c_int * 8)()
+    n = dg.library().det_moduli_used(out, 8)
+    assert n >= 0
+    return list(out[:n])
+
+
+def edge_rows(M, K, v, seed):
+    """Rows of one element +-1 and K - 1 elements +-v, random signs.  For
+    C = A A^T the diagonal outputs' exact integer dot products S equal the
+    Cauchy-Schwarz bound |row|^2 from which the band's moduli count is chosen."""
+    g = np.random.default_rng(seed)
+    A = np.full((M, K), np.float32(v), np.float32)
+    A[:, 0] = 1.0
+    return A * np.where(g.random((M, K)) < 0.5, -1, 1).astype(np.float32)
+
+
+@pytest.mark.parametrize("v,count", [(0.84, 12), (0.845, 13)])
+def test_moduli_count_at_the_cauchy_schwarz_edge(oracle_mod, v, count):
+    # K = 4096: the worst case needs 13 moduli.  |v| = 0.84 puts the diagonal
+    # |S| = 2^93.497 just under the 12-moduli limit prod/(2 (1 + 2^-7)) =
+    # 2^93.513; |v| = 0.845 puts it just over (2^93.514), so 13 are needed
+    K = 4096
+    A = edge_rows(64, K, v, 41)
+    assert dg.library().det_residue_moduli(0, K) == 13
+    got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(A)))
+    torch.cuda.synchronize()
+    assert moduli_used() == [count]
+    assert_bits_equal(got, np_bits(oracle_mod.gemm(A, A)), f"|x| = {v}")
+    P = dg.det_gemm_partial(dev_f32(A), dev_f32(A)).cpu().numpy()
+    assert moduli_used() == [count]
+    np.testing.assert_array_equal(P, oracle_mod.gemm_digits(A, A))
+
+
+def test_normal_data_uses_fewer_moduli_in_both_bands(oracle_mod):
+    # N(0,1) at K = 4096: |S| <= |row of A| |row of B| stays below 2^93,
+    # so both row bands of a 2048-row C take 12 moduli instead of 13
+    K = 4096
+    A = wl.normal_f32((2048, K), 47, 0)
+    B = wl.normal_f32((384, K), 47, 1)
+    got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
+    torch.cuda.synchronize()
+    assert moduli_used() == [12, 12]
+    rows = np.array([0, 1, 777, 1023, 1024, 1500, 2047])
+    assert_bits_equal(got[rows], np_bits(oracle_mod.gemm(A[rows], B)), "N(0,1) 2048 x 384")
 
 
 def test_k_limit_normal_data_takes_the_tensor_core_path(oracle_mod):

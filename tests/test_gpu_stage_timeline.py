@@ -1,9 +1,10 @@
 """The stage-timing diagnostics around a banded det_gemm call.
 
-With timing on, a call at M >= 2048 records its stages on three streams: the
-call's own (pre-pass, planes, reconstruction, general kernel), the library's
-tensor-core stream (one record per band) and its deep-output stream (one
-reconstruction record per band).  The timeline lists them
+With timing on, a call at M >= 2048 records its stages on several streams:
+the call's own (pre-pass, planes, reconstruction), the library's two
+tensor-core streams (one record per band, the bands alternating between
+them), its deep-output stream (one reconstruction record per band) and its
+general-kernel stream.  The timeline lists them
 in enqueue order from the first record's start; the report sums the same
 records per stage.
 """
