@@ -42,6 +42,16 @@ __device__ __forceinline__ Decoded decode_f32_bits(uint32_t bits) {
   return d;
 }
 
+// Exponent key of a binary32 pattern (a bf16 widened to binary32): the
+// biased exponent, with subnormals counted as 1 (their last-bit exponent,
+// -149, is that of biased exponent 1), and 0 for zero and non-finite values.
+// For a live element, key - 150 is the exponent e of its last significand bit.
+__device__ __forceinline__ int exp_key(uint32_t bits) {
+  const uint32_t a = bits & 0x7FFFFFFFu;
+  const int key = max(static_cast<int>(a >> 23), 1);
+  return (a == 0u || a >= 0x7F800000u) ? 0 : key;
+}
+
 template <int kBf16>
 __device__ __forceinline__ uint32_t load_bits(const void* base, int64_t idx) {
   if (kBf16) {

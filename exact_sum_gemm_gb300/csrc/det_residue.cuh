@@ -78,15 +78,35 @@ struct ResidueOperand {
   int64_t rows;
   int64_t K;
   int64_t Kp;                 // K rounded up to kStageK (zero padded)
-  const int* emax;            // [rows]
+  int* emax;                  // [rows] (written by the fused kernel, read by the others)
   __nv_bfloat16* planes;      // [rows/32][Kp/64][nplanes][32][64] (rows padded to 32, see
                               // kPlaneRows)
   int* list_count;            // [rows], zeroed before the launch
   uint2* list;                // [rows][cap]: (k, raw bits) of deep / non-finite elements
   int cap;
   unsigned long long* norm;   // [rows], zeroed before the launch: an upper bound of
-                              // sum_k X_int^2 / 2^kNormShift over the row's shallow elements
+                              // sum_k X_int^2 / 2^norm_shift over the row's shallow elements
+  unsigned* keymax;           // fused kernel: [rows], zeroed (row maxima of exponent keys)
+  unsigned long long* norm_max;  // fused kernel: zeroed slot for the largest norm of these rows
 };
+
+// Thresholds of the moduli choice: P moduli suffice for a row band whose
+// largest row-norm bounds are a (A) and b (B) when the 128-bit a * b is below
+// t[P] = (hi[P], lo[P]), an integer no larger than
+//   prod_P^2 / (2^(2 norm_shift + 2) (1 + 2^-7)^2 (1 + 2^-29)),
+// so that prod_P > 2 (1 + 2^-7) sqrt(a b) 2^norm_shift >= 2 (1 + 2^-7) |S|.
+struct ModuliThresholds {
+  unsigned long long hi[kNumModuli + 1];
+  unsigned long long lo[kNumModuli + 1];
+};
+ModuliThresholds moduli_thresholds(int bf16);
+__device__ __forceinline__ int choose_moduli(unsigned long long a, unsigned long long b, int least,
+                                             int most, const ModuliThresholds& t) {
+  const unsigned long long phi = __umul64hi(a, b), plo = a * b;
+  for (int P = least; P < most; ++P)
+    if (phi < t.hi[P] || (phi == t.hi[P] && plo < t.lo[P])) return P;
+  return most;
+}
 
 // The fewest moduli with compiled kernels (f32 12, bf16 8).
 __host__ __device__ constexpr int planes_least(int bf16) { return bf16 ? 8 : 12; }
@@ -120,6 +140,25 @@ int residue_planes_least(int bf16);
 // number written (at most max), or -1 on a CUDA error.
 int moduli_record(int* out, int max);
 void note_moduli_bands(int bands);
+// The fused path for K-contiguous, vector-aligned operands with K <= kFusedK:
+// one launch per row band computes the rows' exponent maxima, deep lists,
+// residue planes and norm bounds (no separate exponent pre-pass), and its
+// last block writes the band's moduli count.  maxA / maxB: the zeroed slots
+// of the band's A rows and of B's rows (B's filled by band 0's launch, which
+// also covers B); done: a zeroed block counter per launch.
+constexpr int kFusedK = 4096;
+struct FusedBand {
+  const unsigned long long* maxA;
+  const unsigned long long* maxB;
+  unsigned* done;
+  int* used;
+  int band, least, most;
+  ModuliThresholds thr;
+};
+bool fused_residues_ok(const ResidueOperand& o, int bf16);
+// Band 0 with B (o1 null: a band b >= 1 alone).
+cudaError_t launch_residues_fused(const ResidueOperand& o0, const ResidueOperand* o1, int bf16,
+                                  int nplanes, const FusedBand& fb, cudaStream_t stream);
 // One block: the moduli count of a row band, the smallest in [least, most]
 // whose product exceeds 2 (1 + 2^-7) sqrt(max normA * max normB) 2^shift,
 // written to *used (a Cauchy-Schwarz bound of every |S| in the band).

@@ -141,10 +141,11 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   ResidueScratch r{};
   size_t b = align_up(scratch_bytes(g, 0), 1024);
   // zeroed together: countA [M], countB [N], error, deep-row/col counters [2],
-  // moduli per band [kMaxBands]; then the row-norm bounds normA [M], normB [N]
-  // and each band's two norm maxima [2 kMaxBands]
+  // moduli per band [kMaxBands], fused-launch block counters [kMaxBands],
+  // exponent-key maxima keymaxA [M], keymaxB [N]; then the row-norm bounds
+  // normA [M], normB [N] and each band's two norm maxima [2 kMaxBands]
   r.off_counts = b;
-  r.off_norms = align_up(b + sizeof(int) * size_t(g.M + g.N + 3 + kMaxBands), 8);
+  r.off_norms = align_up(b + sizeof(int) * size_t(2 * (g.M + g.N) + 3 + 2 * kMaxBands), 8);
   b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + g.N + 2 * kMaxBands);
   r.zero_bytes = b - r.off_counts;
   b = align_up(b, 1024);
@@ -264,7 +265,10 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   int* counts = reinterpret_cast<int*>(base + L.off_counts);
   int* error = counts + g.M + g.N;
   int* used = error + 3;                                             // moduli per band
+  unsigned* done = reinterpret_cast<unsigned*>(used + kMaxBands);    // fused-launch counters
+  unsigned* keymax = done + kMaxBands;                               // [M] then [N]
   unsigned long long* norms = reinterpret_cast<unsigned long long*>(base + L.off_norms);
+  unsigned long long* maxima = norms + g.M + g.N;                    // [2 b]: band b's A, [1]: B
   const int least = residue_planes_least(g.bf16);
   uint2* listA = reinterpret_cast<uint2*>(base + L.off_listA);
   uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
@@ -278,12 +282,23 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   const int64_t nkb = Kp / kStageK;
   const size_t es = g.bf16 ? 2 : 4;
 
+  // K-contiguous, aligned operands with K <= kFusedK take the fused kernel:
+  // exponent maxima, planes, norms and the moduli count in one launch per
+  // band (no separate pre-pass over A and B)
+  const ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
+                          norms + g.M, keymax + g.M, maxima + 1};
+  const bool fused = fused_residues_ok(rb, g.bf16) &&
+                     fused_residues_ok(ResidueOperand{g.A, g.lda, g.opA, g.M, g.K, Kp}, g.bf16);
   {
     StageScope t(kStagePrepass, stream);
-    e = launch_emax(g, s, stream);
+    e = fused ? cudaSuccess : launch_emax(g, s, stream);
     if (e == cudaSuccess) e = cudaMemsetAsync(counts, 0, L.zero_bytes, stream);
   }
   if (e != cudaSuccess) return e;
+  const ModuliThresholds thr = moduli_thresholds(g.bf16);
+  auto fused_band = [&](int b) {
+    return FusedBand{maxima + 2 * b, maxima + 1, done + b, used + b, b, least, nplanes, thr};
+  };
   // the residue kernels' deep-list counters double as the rows' deep counts,
   // from which the tiles are routed
   auto operand_of_band = [&](int b) {
@@ -291,13 +306,18 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
     return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
                           planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
-                          counts + m0, listA + m0 * cap, cap, norms + m0};
+                          counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0, maxima + 2 * b};
   };
-  auto planes_of_band = [&](int b) { return launch_residues(operand_of_band(b), g.bf16, nplanes, stream); };
   // the band's moduli count, once its rows' and B's norm bounds are complete
   auto moduli_of_band = [&](int b) {
     return launch_moduli(norms + edge[b], edge[b + 1] - edge[b], norms + g.M, g.N, g.bf16, least,
-                         nplanes, used + b, b, norms + g.M + g.N + 2 * b, stream);
+                         nplanes, used + b, b, maxima + 2 * b, stream);
+  };
+  auto planes_of_band = [&](int b) {
+    const ResidueOperand oa = operand_of_band(b);
+    if (fused) return launch_residues_fused(oa, nullptr, g.bf16, nplanes, fused_band(b), stream);
+    cudaError_t ep = launch_residues(oa, g.bf16, nplanes, stream);
+    return ep == cudaSuccess ? moduli_of_band(b) : ep;
   };
   auto gemm_of_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
@@ -316,10 +336,13 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   {
     StageScope t(kStageResiduePlanes, stream);
     // B's planes and band 0's A planes in one launch
-    ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
-                      norms + g.M};
-    e = launch_residues2(rb, operand_of_band(0), g.bf16, nplanes, stream);
-    if (e == cudaSuccess) e = moduli_of_band(0);
+    const ResidueOperand oa = operand_of_band(0);
+    if (fused) {
+      e = launch_residues_fused(rb, &oa, g.bf16, nplanes, fused_band(0), stream);
+    } else {
+      e = launch_residues2(rb, oa, g.bf16, nplanes, stream);
+      if (e == cudaSuccess) e = moduli_of_band(0);
+    }
   }
   if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[0], stream);
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(0), bs->planes_done[0], 0);
@@ -329,7 +352,6 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     {
       StageScope t(kStageResiduePlanes, stream);
       e = planes_of_band(b);
-      if (e == cudaSuccess) e = moduli_of_band(b);
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[b], stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(b), bs->planes_done[b], 0);

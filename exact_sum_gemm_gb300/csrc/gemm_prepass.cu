@@ -41,16 +41,6 @@ __device__ __forceinline__ int row_emax(const int* emax, int64_t r) {
   return v == kEmaxEmpty ? 0 : v;
 }
 
-// Exponent key of a binary32 pattern (a bf16 widened to binary32): the
-// biased exponent, with subnormals counted as 1 (their last-bit exponent,
-// -149, is that of biased exponent 1), and 0 for zero and non-finite values.
-// For a live element, key - 150 is the exponent e of its last significand bit.
-__device__ __forceinline__ int exp_key(uint32_t bits) {
-  const uint32_t a = bits & 0x7FFFFFFFu;
-  const int key = max(static_cast<int>(a >> 23), 1);
-  return (a == 0u || a >= 0x7F800000u) ? 0 : key;
-}
-
 // emax of one full kRowChunk of a K-contiguous row whose chunk start is
 // 16-byte aligned: 16-byte loads, exponent keys only.
 template <int kBf16>

@@ -40,7 +40,21 @@
 #include <type_traits>
 
 namespace det {
+
+// The moduli counts most recently chosen per row band (a diagnostic,
+// det_moduli_used; concurrent calls overwrite one another's entries).
+constexpr int kModuliRecord = 8;
+__device__ int g_moduli_record[kModuliRecord];
+
 namespace {
+
+bool rows_layout(const ResidueOperand& o, int bf16) {
+  // vector loads: K-contiguous rows whose every row start is 16-byte (f32) or
+  // 8-byte (bf16) aligned
+  const uintptr_t vec = bf16 ? 8 : 16;
+  return o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
+         (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
+}
 
 constexpr int kThreads = 256;
 constexpr int kTileRows = 32;
@@ -251,6 +265,115 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
     write_residue_quads<0, P>(dst, x, pw);
     add_row_norm<kBf16, 16>(o, gr, x, pw);                  // a half-warp covers the row's stage
   }
+}
+
+// Fused exponent pass and residue planes, for K-contiguous rows that start on
+// a vector boundary, with K <= kFusedK: one block per row, the whole row held
+// in registers (four runs of four neighbouring k per thread), so the operand
+// is read once.  The block takes the row's largest exponent key (one
+// atomicMax per warp on a zeroed slot, read back after a barrier: no shared
+// memory, so the launch for a later band can run beside a tensor-core GEMM),
+// then writes the residues exactly as residue_rows_kernel does, lists the
+// deep elements, and adds the row's norm bound.  Once the row's norm is
+// complete the block folds it into its operand's maximum; the launch's last
+// block then picks the band's moduli count.  Blocks at or beyond `split`
+// take o1.  Rows past `rows` (up to the plane layout's multiple of 32) get
+// zero residues.
+constexpr int kFusedRuns = kFusedK / (4 * kThreads);
+
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand o0, ResidueOperand o1,
+                                                                  unsigned split, FusedBand fb) {
+  const bool second = blockIdx.x >= split;
+  const ResidueOperand& o = second ? o1 : o0;
+  const int64_t r = second ? blockIdx.x - split : blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31;
+  const bool live_row = r < o.rows;
+  uint32_t bits[kFusedRuns][4];
+  int key = 0;
+#pragma unroll
+  for (int v = 0; v < kFusedRuns; ++v) {
+    const int64_t k = (int64_t(v) * kThreads + tid) * 4;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) bits[v][h] = 0u;
+    if (live_row && k < o.K) {
+      if (k + 4 <= o.K) {
+        if (kBf16) {
+          const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(o.X) +
+                                                               r * o.ld + k));
+          bits[v][0] = w.x << 16;
+          bits[v][1] = w.x & 0xFFFF0000u;
+          bits[v][2] = w.y << 16;
+          bits[v][3] = w.y & 0xFFFF0000u;
+        } else {
+          const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(o.X) +
+                                                               r * o.ld + k));
+          bits[v][0] = w.x;
+          bits[v][1] = w.y;
+          bits[v][2] = w.z;
+          bits[v][3] = w.w;
+        }
+      } else {
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          if (k + h < o.K) bits[v][h] = load_bits<kBf16>(o.X, r * o.ld + k + h);
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < 4; ++h) key = max(key, exp_key(bits[v][h]));
+  }
+  key = __reduce_max_sync(0xFFFFFFFFu, key);
+  if (lane == 0 && key != 0 && live_row) atomicMax(o.keymax + r, static_cast<unsigned>(key));
+  __syncthreads();                                  // every warp's maximum is in place
+  const int kmax = live_row ? static_cast<int>(__ldcg(o.keymax + r)) : 0;
+  if (tid == 0 && live_row) o.emax[r] = kmax != 0 ? kmax - 150 : kEmaxEmpty;
+  const int em = kmax != 0 ? kmax - 150 : 0;
+  const int64_t nkb = o.Kp / kStageK;
+  float sum = 0.0f;                                 // this thread's X_int^2 / 2^norm_shift
+  constexpr float kHalfShift = kBf16 ? 0x1p-8f : 0x1p-26f;
+#pragma unroll
+  for (int v = 0; v < kFusedRuns; ++v) {
+    const int64_t k = (int64_t(v) * kThreads + tid) * 4;
+    if (k >= o.Kp) break;                           // the whole run lies past the padded K
+    float x[4], pw[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const Decoded d = decode_f32_bits(bits[v][h]);
+      const int sh = d.e - em + kDeepGap;
+      const bool deep = d.nonfinite || (d.m != 0 && sh < 0);
+      const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
+      x[h] = static_cast<float>(deep ? 0 : mi);
+      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : sh + 127) << 23);
+      if (deep && k + h < o.K && live_row) {
+        const int slot = atomicAdd(o.list_count + r, 1);
+        if (slot < o.cap) o.list[r * o.cap + slot] = make_uint2(static_cast<uint32_t>(k + h), bits[v][h]);
+      }
+      const float f = __fmul_rn(__fmul_rn(x[h], pw[h]), kHalfShift);   // exact
+      sum = __fmaf_rn(f, f, sum);
+    }
+    uint2* dst = reinterpret_cast<uint2*>(
+        o.planes + ((r / kPlaneRows) * nkb + k / kStageK) * P * kPlaneRows * kStageK +
+        (r % kPlaneRows) * kStageK + (k % kStageK));
+    write_residue_quads<0, P>(dst, x, pw);
+  }
+  // the row's norm bound: 16 roundings in the thread, 5 in the warp (all to
+  // nearest, positive values: relative error below 2^-19), scaled by
+  // 1 + 2^-16 and converted upwards
+#pragma unroll
+  for (int w = 16; w >= 1; w /= 2) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, w));
+  if (lane == 0 && live_row && sum > 0.0f)
+    atomicAdd(o.norm + r, __float2ull_ru(__fmul_ru(sum, 1.0f + 0x1p-16f)));
+  __syncthreads();                                  // the row's norm is complete
+  if (tid != 0) return;
+  if (live_row) atomicMax(o.norm_max, __ldcg(o.norm + r));
+  __threadfence();
+  if (atomicAdd(fb.done, 1u) != gridDim.x - 1) return;
+  // the launch's last block: every row's maximum is in place
+  const unsigned long long a = atomicAdd(const_cast<unsigned long long*>(fb.maxA), 0ull);
+  const unsigned long long b = atomicAdd(const_cast<unsigned long long*>(fb.maxB), 0ull);
+  const int Pn = choose_moduli(a, b, fb.least, fb.most, fb.thr);
+  *fb.used = Pn;
+  if (fb.band >= 0 && fb.band < kModuliRecord) g_moduli_record[fb.band] = Pn;
 }
 
 // ---------------------------------------------------------------- reconstruction
@@ -1008,20 +1131,30 @@ int residue_planes_needed(const GemmArgs& g) {
 
 int residue_planes_least(int bf16) { return planes_least(bf16); }
 
-// The moduli counts most recently chosen per row band (a diagnostic,
-// det_moduli_used; concurrent calls overwrite one another's entries).
-constexpr int kModuliRecord = 8;
-__device__ int g_moduli_record[kModuliRecord];
+ModuliThresholds moduli_thresholds(int bf16) {
+  // every step below rounds to nearest in double (relative error below
+  // 2^-48 in all); the factor 1 - 2^-40 keeps each threshold under the exact
+  // quotient, and the conversion to a 128-bit integer is exact
+  ModuliThresholds t{};
+  double prod = 1.0;
+  for (int P = 1; P <= kNumModuli; ++P) {
+    prod *= static_cast<double>(modulus(P - 1));
+    const double q = prod * prod / ldexp(1.0, 2 * norm_shift(bf16) + 2) / (129.0 / 128.0) /
+                     (129.0 / 128.0) / (1.0 + 0x1p-29) * (1.0 - 0x1p-40);
+    const double hi = floor(q / 0x1p64);
+    t.hi[P] = static_cast<unsigned long long>(hi);
+    t.lo[P] = static_cast<unsigned long long>(q - hi * 0x1p64);
+  }
+  return t;
+}
 
 namespace {
 
 // One block.  With a = the largest row-norm bound of the band's rows of A and
 // b = that of B's rows (units of 2^norm_shift), every output of the band has
 // |S| <= sqrt(a b) 2^shift (Cauchy-Schwarz).  The band takes the fewest moduli
-// P in [least, most] with prod_P^2 > 4 (1 + 2^-7)^2 a b 2^(2 shift); the static
-// count `most` covers every input.  The double arithmetic below rounds to
-// nearest in a few dozen steps (relative error below 2^-47), which the factor
-// 1 + 2^-30 on the right-hand side more than covers.
+// P in [least, most] with a b below the threshold t[P] (moduli_thresholds);
+// the static count `most` covers every input.
 // No shared memory: a kernel that needs some cannot start on an SM whose
 // shared memory is configured for a running tensor-core GEMM, so this one
 // would wait for the GEMM to end.  The warps meet through atomicMax on two
@@ -1047,7 +1180,7 @@ __device__ __forceinline__ unsigned long long max_of_rows(const unsigned long lo
 
 __global__ void __launch_bounds__(kModuliThreads) moduli_kernel(
     const unsigned long long* normA, int64_t rowsA, const unsigned long long* normB, int64_t rowsB,
-    int bf16, int least, int most, int* used, int band, unsigned long long* maxima) {
+    int least, int most, int* used, int band, unsigned long long* maxima, ModuliThresholds thr) {
   const unsigned long long a_w = max_of_rows(normA, rowsA);
   const unsigned long long b_w = max_of_rows(normB, rowsB);
   if ((threadIdx.x & 31) == 0) {
@@ -1058,18 +1191,7 @@ __global__ void __launch_bounds__(kModuliThreads) moduli_kernel(
   if (threadIdx.x != 0) return;
   const unsigned long long a = atomicAdd(maxima, 0ull);        // read at L2, after every warp
   const unsigned long long b = atomicAdd(maxima + 1, 0ull);
-  const double margin = (1.0 + 0x1p-7) * (1.0 + 0x1p-7) * (1.0 + 0x1p-30);
-  const double rhs = 4.0 * margin * static_cast<double>(a) * static_cast<double>(b) *
-                     ldexp(1.0, 2 * norm_shift(bf16));
-  int P = most;
-  double prod = 1.0;
-  for (int i = 0; i < most; ++i) {
-    prod *= static_cast<double>(modulus(i));
-    if (i + 1 >= least && prod * prod > rhs) {
-      P = i + 1;
-      break;
-    }
-  }
+  const int P = choose_moduli(a, b, least, most, thr);
   *used = P;
   if (band >= 0 && band < kModuliRecord) g_moduli_record[band] = P;
 }
@@ -1080,8 +1202,28 @@ cudaError_t launch_moduli(const unsigned long long* normA, int64_t rowsA,
                           const unsigned long long* normB, int64_t rowsB, int bf16, int least,
                           int most, int* used, int band, unsigned long long* maxima,
                           cudaStream_t stream) {
-  moduli_kernel<<<1, kModuliThreads, 0, stream>>>(normA, rowsA, normB, rowsB, bf16, least, most,
-                                                  used, band, maxima);
+  moduli_kernel<<<1, kModuliThreads, 0, stream>>>(normA, rowsA, normB, rowsB, least, most, used,
+                                                  band, maxima, moduli_thresholds(bf16));
+  note_launch();
+  return cudaGetLastError();
+}
+
+bool fused_residues_ok(const ResidueOperand& o, int bf16) {
+  return o.K <= kFusedK && rows_layout(o, bf16);
+}
+
+cudaError_t launch_residues_fused(const ResidueOperand& o0, const ResidueOperand* o1, int bf16,
+                                  int nplanes, const FusedBand& fb, cudaStream_t stream) {
+  const int64_t b0 = plane_rows(o0.rows), b1 = o1 != nullptr ? plane_rows(o1->rows) : 0;
+  if (b0 + b1 == 0 || b0 + b1 > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  const dim3 grid(static_cast<unsigned>(b0 + b1));
+  const ResidueOperand& second = o1 != nullptr ? *o1 : o0;
+  const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
+    residue_fused_kernel<decltype(B)::value, decltype(P)::value>
+        <<<grid, kThreads, 0, stream>>>(o0, second, static_cast<unsigned>(b0), fb);
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
   note_launch();
   return cudaGetLastError();
 }
@@ -1104,13 +1246,6 @@ int moduli_record(int* out, int max) {
 
 namespace {
 
-bool rows_layout(const ResidueOperand& o, int bf16) {
-  // vector loads: K-contiguous rows whose every row start is 16-byte (f32) or
-  // 8-byte (bf16) aligned
-  const uintptr_t vec = bf16 ? 8 : 16;
-  return o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
-         (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
-}
 
 // one launch over o0's row blocks, then o1's (both of the same layout)
 cudaError_t residues_launch(const ResidueOperand& o0, const ResidueOperand& o1, int64_t blocks0,
