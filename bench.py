@@ -186,10 +186,11 @@ def cpu_baseline(workload, rows, seed=0):
 # fingerprint; otherwise "traffic" is null.
 CAPTURED_TRAFFIC = {
     # det_gemm at 4096^3 runs the tensor-core kernel once per row band (two
-    # bands); bytes are per launch, the mean of the call's two launches
-    "residue_gemm": {"fingerprint": "5ed18466622e9d47", "mnk": (4096, 4096, 4096),
+    # bands of 2816 and 1280 rows); bytes are per launch, the mean of the
+    # call's two launches
+    "residue_gemm": {"fingerprint": "7a7d5766ef567b96", "mnk": (4096, 4096, 4096),
                      "workload": "normal", "launches_per_call": 2,
-                     "bytes": (921027584 + 104829952 + 920887808 + 101702144) // 2},
+                     "bytes": (984250368 + 130921728 + 698002944 + 52186112) // 2},
 }
 KERNEL_SOURCES = {
     "residue_gemm": ["gemm_tc2.cu", "gemm_tc.cu", "tc_ptx.cuh", "det_residue.cuh"],

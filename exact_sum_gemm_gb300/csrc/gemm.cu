@@ -177,11 +177,12 @@ struct BandSync {
   cudaStream_t hi2 = nullptr;                      // ... and of odd bands
   cudaStream_t side = nullptr;                     // deep-output reconstruction
   cudaStream_t gen = nullptr;                      // general-tile kernel
-  cudaEvent_t gen_fork = nullptr, gen_done = nullptr;
+  cudaStream_t fast2 = nullptr;                    // fast reconstruction of bands >= 1
+  cudaEvent_t gen_fork = nullptr, gen_done = nullptr;   // after the routing; general kernel done
   cudaEvent_t planes_done[kMaxBands] = {};         // caller's stream -> hi
   cudaEvent_t gemm_done[kMaxBands] = {};           // hi -> caller's stream
-  cudaEvent_t fork[kMaxBands] = {};                // caller's stream -> side
   cudaEvent_t deep_done[kMaxBands] = {};           // side -> caller's stream
+  cudaEvent_t fast_done[kMaxBands] = {};           // fast2 -> caller's stream
 };
 std::mutex g_band_mu[kMaxDevices];
 BandSync g_band[kMaxDevices];
@@ -202,12 +203,16 @@ cudaError_t band_sync(int dev, BandSync** out) {
       e = cudaStreamCreateWithPriority(&b.side, cudaStreamNonBlocking, side_prio);
     if (e == cudaSuccess && b.gen == nullptr)
       e = cudaStreamCreateWithPriority(&b.gen, cudaStreamNonBlocking, least);
+    // (a priority above the caller's let the last band's reconstruction
+    // crowd band 0's: measured slower)
+    if (e == cudaSuccess && b.fast2 == nullptr)
+      e = cudaStreamCreateWithPriority(&b.fast2, cudaStreamNonBlocking, least);
     if (e == cudaSuccess && b.gen_fork == nullptr)
       e = cudaEventCreateWithFlags(&b.gen_fork, cudaEventDisableTiming);
     if (e == cudaSuccess && b.gen_done == nullptr)
       e = cudaEventCreateWithFlags(&b.gen_done, cudaEventDisableTiming);
     for (int i = 0; i < kMaxBands && e == cudaSuccess; ++i) {
-      cudaEvent_t* ev[4] = {&b.planes_done[i], &b.gemm_done[i], &b.fork[i], &b.deep_done[i]};
+      cudaEvent_t* ev[4] = {&b.planes_done[i], &b.gemm_done[i], &b.deep_done[i], &b.fast_done[i]};
       for (int k = 0; k < 4 && e == cudaSuccess; ++k)
         if (*ev[k] == nullptr) e = cudaEventCreateWithFlags(ev[k], cudaEventDisableTiming);
     }
@@ -378,11 +383,18 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->gen_done, bs->gen);
   }
-  int forked = 0;
+  // Band b's reconstruction needs the routing (gen_fork, recorded on the
+  // caller's stream after it) and band b's GEMM.  Its deep outputs go to the
+  // side stream; its other outputs to the caller's stream for band 0 and to
+  // fast2 for later bands, so that the last band's starts when its GEMM ends
+  // even while band 0's is still running.
+  int forked = 0, fast_forked = 0;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
-    e = cudaStreamWaitEvent(stream, bs->gemm_done[b], 0);
-    if (e == cudaSuccess) e = cudaEventRecord(bs->fork[b], stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->side, bs->fork[b], 0);
+    e = cudaStreamWaitEvent(bs->side, bs->gen_fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->side, bs->gemm_done[b], 0);
+    const cudaStream_t fs = b == 0 ? stream : bs->fast2;
+    if (e == cudaSuccess && b > 0) e = cudaStreamWaitEvent(fs, bs->gen_fork, 0);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(fs, bs->gemm_done[b], 0);
     if (e != cudaSuccess) break;
     forked = b + 1;
     const int64_t m0 = edge[b], m1 = edge[b + 1];
@@ -395,19 +407,27 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->deep_done[b], bs->side);
     if (e == cudaSuccess) {
-      StageScope t(kStageReconstruct, stream);
-      e = launch_reconstruct_fast(g, rc, stream);
+      StageScope t(kStageReconstruct, fs);
+      e = launch_reconstruct_fast(g, rc, fs);
+    }
+    if (e == cudaSuccess && b > 0) {
+      e = cudaEventRecord(bs->fast_done[b], fs);
+      if (e == cudaSuccess) fast_forked = b + 1;
     }
   }
   for (int b = 0; b < forked && e == cudaSuccess; ++b) e = cudaStreamWaitEvent(stream, bs->deep_done[b], 0);
+  for (int b = 1; b < fast_forked && e == cudaSuccess; ++b)
+    e = cudaStreamWaitEvent(stream, bs->fast_done[b], 0);
   if (e == cudaSuccess && gen_forked) e = cudaStreamWaitEvent(stream, bs->gen_done, 0);
   if (e != cudaSuccess) {
-    // keep the caller's stream ordered after everything enqueued on hi, hi2, side and gen
+    // keep the caller's stream ordered after everything enqueued on hi, hi2, side, fast2 and gen
     cudaEvent_t join = bs->gemm_done[0];
     if (cudaEventRecord(join, hi) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     if (cudaEventRecord(join, bs->hi2) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     join = bs->deep_done[0];
     if (cudaEventRecord(join, bs->side) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
+    join = bs->fast_done[0];
+    if (cudaEventRecord(join, bs->fast2) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     if (cudaEventRecord(bs->gen_done, bs->gen) == cudaSuccess) cudaStreamWaitEvent(stream, bs->gen_done, 0);
   }
   return e;
