@@ -81,7 +81,7 @@ constexpr int kCrtWeightBits = 20;
 
 // The top limb of every C_i and of -M is below 2^14 in magnitude (M < 2^110),
 // so its sum stays within 32 bits: 14 * 127 * 2^14 + 2^10 * 2^14 < 2^25.
-template <int P, int i>
+template <int P, int i, bool kTop>
 __host__ __device__ __forceinline__ void crt_terms(const int32_t (&r)[kNumModuli], int64_t (&acc)[3],
                                                    int32_t& acc3, int32_t& Q) {
   if constexpr (i < P) {
@@ -99,10 +99,19 @@ __host__ __device__ __forceinline__ void crt_terms(const int32_t (&r)[kNumModuli
     acc[1] += static_cast<int64_t>(r[i]) * c1;
     acc[2] += static_cast<int64_t>(r[i]) * c2;
 #endif
-    acc3 += r[i] * c3;
+    if constexpr (kTop) acc3 += r[i] * c3;
     Q += r[i] * w;
-    crt_terms<P, i + 1>(r, acc, acc3, Q);
+    crt_terms<P, i + 1, kTop>(r, acc, acc3, Q);
   }
+}
+
+// Whether |S| < M / 2 fits a 96-bit two's-complement value (M < 2^95), so
+// that the sum modulo 2^96 -- three limbs -- determines it: the first 12
+// moduli (M < 2^94.6, every f32 band at the least count) and every bf16 count.
+__host__ __device__ constexpr bool crt_three_limbs(int P) {
+  double m = 1.0;
+  for (int i = 0; i < P; ++i) m *= static_cast<double>(modulus(i));
+  return m < 0x1p95;
 }
 
 // S (two's complement, hi:lo) from the balanced residues r_0 .. r_{P-1}
@@ -113,22 +122,29 @@ template <int P>
 __host__ __device__ __forceinline__ void crt_s128(const int32_t (&r)[kNumModuli], uint64_t& lo,
                                                   uint64_t& hi) {
   static_assert(P >= 1 && P <= kNumModuli, "moduli in use");
+  constexpr bool kTop = !crt_three_limbs(P);
   int64_t acc[3] = {0, 0, 0};
   int32_t acc3 = 0, Q = 0;                         // |Q| < 14 * 127 * 2^19 < 2^30
-  crt_terms<P, 0>(r, acc, acc3, Q);
+  crt_terms<P, 0, kTop>(r, acc, acc3, Q);
   const int32_t q = (Q + (1 << (kCrtWeightBits - 1))) >> kCrtWeightBits;
   static_assert(crt_negM_limb(P, 3) < (1 << 14) && crt_negM_limb(P, 3) > -(1 << 14), "top limb");
   acc[0] += static_cast<int64_t>(q) * crt_negM_limb(P, 0);
   acc[1] += static_cast<int64_t>(q) * crt_negM_limb(P, 1);
   acc[2] += static_cast<int64_t>(q) * crt_negM_limb(P, 2);
-  acc3 += q * crt_negM_limb(P, 3);
+  if constexpr (kTop) acc3 += q * crt_negM_limb(P, 3);
   // S = acc0 + acc1 2^32 + acc2 2^64 + acc3 2^96 (mod 2^128); |acc_l| < 2^43
   const uint64_t a0 = static_cast<uint64_t>(acc[0]);
   const uint64_t a1lo = static_cast<uint64_t>(acc[1]) << 32;
   lo = a0 + a1lo;
   const uint64_t carry = lo < a0 ? 1u : 0u;
   hi = static_cast<uint64_t>(acc[0] >> 63) + static_cast<uint64_t>(acc[1] >> 32) + carry +
-       static_cast<uint64_t>(acc[2]) + (static_cast<uint64_t>(static_cast<uint32_t>(acc3)) << 32);
+       static_cast<uint64_t>(acc[2]);
+  if constexpr (kTop) {
+    hi += static_cast<uint64_t>(static_cast<uint32_t>(acc3)) << 32;
+  } else {
+    // S modulo 2^96, sign-extended from bit 95
+    hi = static_cast<uint64_t>(static_cast<int64_t>(hi << 32) >> 32);
+  }
 }
 
 }  // namespace det
