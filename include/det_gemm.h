@@ -89,10 +89,23 @@ uint64_t det_kernel_launches(void);
  * --, total milliseconds, number of timed launches), clears the record and
  * returns the number of entries.  Any output pointer may be NULL. */
 int det_stage_timing(int enable);
+int det_stage_report(const char** names, double* total_ms, int* counts, int max);
 
-/* Number of moduli (bf16 tensor-core GEMMs) the residue path of det_gemm uses
- * for this dtype and K: enough that their product exceeds twice the largest
- * possible |sum of shallow products| (0 for K = 0; -1 for bad arguments). */
+/* The same records as a timeline, in the order the stages were enqueued:
+ * stage name, start and stop in milliseconds from the first record's start.
+ * Tensor-core launches ("residue_gemm") sit on two library streams and
+ * overlap the stages on the call's stream (and, at a band change, one
+ * another); a record starts when its stream reaches it, which may precede
+ * its first kernel's start.  Writes up to `max`
+ * entries, clears the record and returns the number written.  Any output
+ * pointer may be NULL. */
+int det_stage_timeline(const char** names, double* start_ms, double* stop_ms, int max);
+
+/* Worst-case number of moduli (bf16 tensor-core GEMMs) of det_gemm's residue
+ * path for this dtype and K: enough that their product exceeds twice the
+ * largest possible |sum of shallow products|.  The residue planes are written
+ * for this many; a row band may compute fewer (det_moduli_used).  0 for
+ * K = 0; -1 for bad arguments. */
 int det_residue_moduli(det_dtype dtype, int64_t K);
 
 /* Diagnostic for benchmarks: the moduli counts the most recent residue-path
@@ -106,16 +119,6 @@ int det_residue_moduli(det_dtype dtype, int64_t K);
  * synchronises with the device; concurrent calls overwrite one another's
  * record. */
 int det_moduli_used(int* out, int max);
-int det_stage_report(const char** names, double* total_ms, int* counts, int max);
-
-/* The same records as a timeline, in the order the stages were enqueued:
- * stage name, start and stop in milliseconds from the first record's start.
- * Tensor-core launches ("residue_gemm") sit on a library stream and overlap
- * the stages on the call's stream; a record starts when its stream reaches
- * it, which may precede its first kernel's start.  Writes up to `max`
- * entries, clears the record and returns the number written.  Any output
- * pointer may be NULL. */
-int det_stage_timeline(const char** names, double* start_ms, double* stop_ms, int max);
 
 /*
  * det_gemm -- C = RNE_f32( sum_k A(m,k) * B(n,k) ), computed exactly.
