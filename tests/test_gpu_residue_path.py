@@ -222,3 +222,26 @@ def test_partial_digit_windows_across_scales(oracle_mod, sa, sb):
     np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B),
                                   err_msg=f"digits at 2^{sa} x 2^{sb}")
     assert_bits_equal(bits_of(dg.det_gemm(a, b)), np_bits(oracle_mod.gemm(A, B)), f"2^{sa} x 2^{sb}")
+
+
+def test_fused_and_two_pass_planes_agree(oracle_mod):
+    # K-contiguous operands (K <= 4096) take the fused kernel: row maxima,
+    # planes, norm bounds and the band's moduli count in one launch.  The same
+    # operands stored K-minor take the two-pass kernels (row maxima, plane
+    # kernel, moduli kernel).  Both give the same bits and the same counts.
+    K = 3000
+    A = wl.normal_f32((2304, K), 53, 0)
+    B = wl.normal_f32((320, K), 53, 1)
+    A[7, 11] = np.float32(3e-9)                 # deep elements on both sides
+    B[5, 2999] = np.float32(-2e-10)
+    fused = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
+    torch.cuda.synchronize()
+    used_fused = moduli_used()
+    at = dev_f32(np.ascontiguousarray(A.T)).t()      # logical [M, K], K-minor
+    bt = dev_f32(np.ascontiguousarray(B.T)).t()
+    two_pass = bits_of(dg.det_gemm(at, bt))
+    torch.cuda.synchronize()
+    assert moduli_used() == used_fused == [12, 12]
+    assert_bits_equal(two_pass, fused, "K-minor operands against K-contiguous ones")
+    rows = np.array([0, 7, 1279, 1280, 2303])
+    assert_bits_equal(fused[rows], np_bits(oracle_mod.gemm(A[rows], B)), "fused planes")
