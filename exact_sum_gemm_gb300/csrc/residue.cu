@@ -384,7 +384,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
 //         S = S' mod M (balanced);
 //   T   = S * 2^64 plus every product involving a deep element, exact, as a
 //         192-bit two's-complement integer whose bit 0 weighs 2^E with
-//         E = emaxA + emaxB - 38 - 64 (+32 for bf16 planes);
+//         E = emaxA + emaxB - 36 - 64 (+32 for bf16 planes);
 //   out = RNE_f32(T * 2^E), or T placed into canonical digits.
 // A deep product whose lowest bit lies below 2^E (more than 64 bits under the
 // shallow grid) or that would leave the window is handled by the full
