@@ -1142,6 +1142,10 @@ ModuliThresholds moduli_thresholds(int bf16) {
     const double q = prod * prod / ldexp(1.0, 2 * norm_shift(bf16) + 2) / (129.0 / 128.0) /
                      (129.0 / 128.0) / (1.0 + 0x1p-29) * (1.0 - 0x1p-40);
     const double hi = floor(q / 0x1p64);
+    if (hi >= 0x1p64) {                 // beyond 128 bits (bf16 counts above any in use)
+      t.hi[P] = t.lo[P] = ~0ull;
+      continue;
+    }
     t.hi[P] = static_cast<unsigned long long>(hi);
     t.lo[P] = static_cast<unsigned long long>(q - hi * 0x1p64);
   }
