@@ -86,3 +86,30 @@ def test_python_layer_rejects_host_tensors():
     import torch
     with pytest.raises(ValueError, match="CUDA"):
         dg.det_gemm(torch.ones(2, 3), torch.ones(2, 3))
+
+
+# The residue path's moduli, odd and pairwise coprime in [197, 255], in the
+# order the library uses them.
+MODULI = [255, 253, 251, 247, 241, 239, 233, 229, 227, 223, 217, 211, 199, 197]
+
+
+@pytest.mark.parametrize("dtype,bits,least", [(0, 24, 12), (1, 8, 8)])
+def test_worst_case_moduli_count_from_the_bound(dtype, bits, least):
+    # Shallow elements are integers below 2^(bits + 18) on their row's grid, so
+    # |S| <= K (2^bits - 1)^2 2^36; the CRT needs prod > 2 |S| (1 + 2^-7).
+    # Big-integer arithmetic here, independent of the library's own.
+    from math import gcd
+    assert all(gcd(p, q) == 1 for i, p in enumerate(MODULI) for q in MODULI[i + 1:])
+    lib = dg.library()
+    for K in [1, 2, 63, 64, 2048, 4096, 4097, 1 << 17, (1 << 19) - 1, 1 << 19]:
+        bound = K * ((1 << bits) - 1) ** 2 * (1 << 36)
+        prod, want = 1, None
+        for i, p in enumerate(MODULI):
+            prod *= p
+            if 128 * prod > 2 * 129 * bound:        # prod > 2 (1 + 2^-7) |S|
+                want = max(i + 1, least)
+                break
+        assert lib.det_residue_moduli(dtype, K) == want, (dtype, K)
+    assert lib.det_residue_moduli(dtype, 0) == 0
+    assert lib.det_residue_moduli(dtype, (1 << 19) + 1) == -1
+    assert lib.det_residue_moduli(7, 64) == -1
