@@ -58,6 +58,9 @@ def parse_args():
                    help="rows of the 4096^3 problem the CPU baseline samples")
     p.add_argument("--no-extras", action="store_true",
                    help="skip the e2e, sharded and CPU-baseline measurements")
+    p.add_argument("--configs", action="store_true",
+                   help="time each workload configuration (one JSON line each) instead of "
+                        "the headline run")
     p.add_argument("--mnk", type=int, nargs=3, default=None, metavar=("M", "N", "K"),
                    help="override the problem size (profiling of small cases only)")
     args = p.parse_args()
@@ -597,10 +600,103 @@ def measure_extras(args, dg, a, b, c, A, B, dev, stream):
     return out
 
 
+def run_configs(args):
+    """Each workload configuration timed on one GPU, inputs resident in HBM:
+    CUDA events on the current stream around `steps` calls after `warmup`
+    calls (no L2 flush: several of these problems fit in L2).  One JSON line
+    per configuration; exact GFLOP/s counts 2MNK per GEMM."""
+    import torch
+    import exact_sum_gemm_gb300 as dg
+    from exact_sum_gemm_gb300 import workloads as wl
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    steps, warm = max(1, args.steps), max(1, args.warmup)
+
+    def timed(fn, n=steps):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(n):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / n
+
+    def emit(name, ms, flops, **extra):
+        line = {"config": name, "ms": round(ms, 4),
+                "exact_gflops": round(flops / (ms * 1e-3) / 1e9, 2), "data": "synthetic"}
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
+    # 64^3 f32 N(0,1): det_gemm, and 16 equal K-shards through partial/combine/finalize
+    a, b = f32(wl.normal_f32((64, 64), 0, 0)), f32(wl.normal_f32((64, 64), 0, 1))
+    emit("det_gemm f32 64x64x64 N(0,1)", timed(lambda: dg.det_gemm(a, b)), 2.0 * 64 ** 3)
+    cuts = wl.equal_cuts(64, 16)
+    emit("det_gemm_partial x16 + det_combine + det_finalize, f32 64^3",
+         timed(lambda: dg.det_gemm_sharded(a, b, cuts)), 2.0 * 64 ** 3)
+    # bf16 512x512x4096, exponents U{-60..60}, cancelling column pairs; 8 random K-shards
+    ab, bb, _ = wl.bf16_wide_with_cancellation(512, 512, 4096, 1)
+    ab, bb = wl.to_torch_bf16(ab, dev), wl.to_torch_bf16(bb, dev)
+    fl = 2.0 * 512 * 512 * 4096
+    emit("det_gemm bf16 512x512x4096, exponents U{-60..60}, cancelling pairs",
+         timed(lambda: dg.det_gemm(ab, bb)), fl)
+    rcuts = wl.kshard_cuts(4096, 8, 1)
+    emit("det_gemm_partial x8 (random cuts) + combine + finalize, same bf16 workload",
+         timed(lambda: dg.det_gemm_sharded(ab, bb, rcuts)), fl)
+    # DetLinear 4096 -> 4096 on a 2048 x 4096 batch: forward, dgrad, wgrad
+    x_np, w_np = wl.detlinear_inputs()
+    x, w = f32(x_np), f32(w_np)
+    y = dg.det_linear_forward(x, w)
+    dy = (y * 2.0 ** -22).contiguous()
+    fl = 2.0 * 2048 * 4096 * 4096
+    emit("DetLinear forward f32 2048x4096 -> 4096", timed(lambda: dg.det_linear_forward(x, w)), fl)
+    emit("DetLinear dgrad f32", timed(lambda: dg.det_linear_dgrad(dy, w)), fl)
+    emit("DetLinear wgrad f32", timed(lambda: dg.det_linear_wgrad(dy, x)), fl)
+    del x, w, y, dy
+    # f32 256x256, K = 2^19, |x| = 2^U[-100,100]
+    K = 1 << 19
+    a4 = f32(wl.loguniform_f32((256, K), 3, 0))
+    b4 = f32(wl.loguniform_f32((256, K), 3, 1))
+    emit("det_gemm f32 256x256x524288, |x| = 2^U[-100,100]",
+         timed(lambda: dg.det_gemm(a4, b4), n=max(1, steps // 2)), 2.0 * 256 * 256 * K)
+    del a4, b4
+    # one training step of the 1024 -> 4096 -> 1024 MLP, batch 256 (targets
+    # from the teacher through det_gemm, forward, backward, SGD update)
+    relu = lambda t: torch.clamp_min(t, 0.0)
+    w1, w2 = wl.mlp_init(stream=0)
+    t1, t2 = wl.mlp_init(stream=1)
+    t1d, t2d = f32(t1), f32(t2)
+    xb = f32(wl.mlp_batch(0))
+    lr = torch.tensor(1e-2, dtype=torch.float32, device=dev)
+    for shards in (1, 4):
+        l1 = dg.DetLinear(1024, 4096, device=dev, k_shards=shards, weight=torch.from_numpy(w1))
+        l2 = dg.DetLinear(4096, 1024, device=dev, k_shards=shards, weight=torch.from_numpy(w2))
+
+        def step():
+            with torch.no_grad():
+                target = dg.det_gemm(relu(dg.det_gemm(xb, t1d)), t2d)
+            loss = (l2(relu(l1(xb))) - target).square().mean()
+            for q in (l1.weight, l2.weight):
+                q.grad = None
+            loss.backward()
+            with torch.no_grad():
+                for q in (l1.weight, l2.weight):
+                    q.sub_(q.grad * lr)
+        # 2 teacher + 2 forward + 1 dgrad + 2 wgrad GEMMs of 256 x 1024 x 4096
+        emit(f"MLP 1024->4096->1024 training step, batch 256, k_shards={shards}",
+             timed(step), 7 * 2.0 * 256 * 1024 * 4096)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.configs:
+        return run_configs(args)
     return run_ours(args)
 
 

@@ -44,12 +44,17 @@ cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deep
                             cudaStream_t stream);
 cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream);
 // General kernel over the 64x64 tiles listed in general (count first).
-cudaError_t launch_kulisch(const GemmArgs& g, const int* general, cudaStream_t stream);
+// allow_split: when the grid would hold few tiles and K is long, K may be
+// split among CTAs with a scratch slot per tile from the library's pool
+// (false: allocate nothing).
+cudaError_t launch_kulisch(const GemmArgs& g, const int* general, bool allow_split,
+                           cudaStream_t stream);
 
 // Pre-pass + band + general kernels with caller-provided scratch of at least
-// scratch_bytes(g, slots) bytes (256-byte aligned).
+// scratch_bytes(g, slots) bytes (256-byte aligned); allow_alloc lets the
+// general kernel take a K-split slot from the library's pool.
 cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slots,
-                                  cudaStream_t stream);
+                                  bool allow_alloc, cudaStream_t stream);
 
 // det_gemm_partial_noalloc: scratch from a fixed static device array.
 bool noalloc_fits(const GemmArgs& g);

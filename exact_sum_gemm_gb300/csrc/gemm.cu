@@ -93,7 +93,7 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots) {
 }
 
 cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slots,
-                                  cudaStream_t stream) {
+                                  bool allow_alloc, cudaStream_t stream) {
   const Scratch s = carve_scratch(scratch, g, slots);
   cudaError_t e;
   {
@@ -107,7 +107,7 @@ cudaError_t run_gemm_with_scratch(const GemmArgs& g, void* scratch, int64_t slot
   }
   if (e != cudaSuccess) return e;
   StageScope t(kStageGeneral, stream);
-  return launch_kulisch(g, s.general, stream);
+  return launch_kulisch(g, s.general, allow_alloc, stream);
 }
 
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream) {
@@ -124,7 +124,7 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
   void* scratch = nullptr;
   cudaError_t e = pool_alloc(&scratch, scratch_bytes(g, slots), stream);
   if (e != cudaSuccess) return e;
-  e = run_gemm_with_scratch(g, scratch, slots, stream);
+  e = run_gemm_with_scratch(g, scratch, slots, true, stream);
   cudaError_t f = cudaFreeAsync(scratch, stream);
   return e != cudaSuccess ? e : f;
 }
@@ -379,7 +379,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     if (e == cudaSuccess) {
       gen_forked = true;
       StageScope t(kStageGeneral, bs->gen);
-      e = launch_kulisch(g, s.general, bs->gen);
+      e = launch_kulisch(g, s.general, true, bs->gen);
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->gen_done, bs->gen);
   }

@@ -18,6 +18,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
+
 #include "det_arith.cuh"
 #include "det_gemm_internal.cuh"
 #include "det_kernels.h"
@@ -32,6 +34,7 @@ constexpr int kThreads = 256;
 constexpr int kOutputs = kBM * kBN;                 // 1024 outputs per CTA
 constexpr int kPad = kBM + 1;                       // staging row stride (bank spread)
 constexpr int kNormChunks = (1 << 15) / kBK;        // normalise every 2^15 products
+constexpr int kMaxSplits = 64;                      // K-splits of one tile (their sum < 2^39)
 
 constexpr size_t kAccBytes = size_t(kDigits) * kOutputs * sizeof(int64_t);
 constexpr size_t kStageBytes = size_t(2) * kBK * kPad * sizeof(int2);
@@ -75,8 +78,9 @@ __device__ __forceinline__ void normalise_in_place(int64_t* acc_o) {
 // listed in general (general[0] = their count), so a call with no such tile
 // costs one launch.
 template <int kBf16>
-__global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
-                                                                    const int* general) {
+__global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p, const int* general,
+                                                                    int splits, int64_t* accg,
+                                                                    unsigned* qdone) {
   extern __shared__ __align__(16) unsigned char smem[];
   int64_t* acc = reinterpret_cast<int64_t*>(smem);
   int2* As = reinterpret_cast<int2*>(smem + kAccBytes);
@@ -88,14 +92,26 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
   const int64_t quarters = int64_t(*general) * 4;
   const int tid = threadIdx.x;
   const int ty = tid >> 4, tx = tid & 15;
+  __shared__ int last_split;
+  // work items: (quarter, K-split); with splits > 1 each item adds its
+  // normalised digits to the quarter's slot in accg with 64-bit atomics (an
+  // exact integer sum, so the order does not matter) and the item that
+  // completes the quarter rounds it
+  const int64_t nchunks_all = (p.K + kBK - 1) / kBK;
+  const int64_t chunks_per_split = (nchunks_all + splits - 1) / splits;
 
-  for (int64_t w = blockIdx.x; w < quarters; w += gridDim.x) {
+  for (int64_t item = blockIdx.x; item < quarters * splits; item += gridDim.x) {
+  const int64_t w = item / splits;
+  const int64_t split = item - w * splits;
   const int64_t parent = general[1 + (w >> 2)];
   const int64_t ptm = parent / parents_n;
   const int64_t tm = 2 * ptm + ((w >> 1) & 1);
   const int64_t tn = 2 * (parent - ptm * parents_n) + (w & 1);
   const int64_t m0 = tm * kBM, n0 = tn * kBN;
   if (m0 >= p.M || n0 >= p.N) continue;               // ragged edge: quarter outside
+  const int64_t c_begin = split * chunks_per_split;
+  const int64_t c_end = c_begin + chunks_per_split < nchunks_all ? c_begin + chunks_per_split
+                                                                  : nchunks_all;
 
   __syncthreads();                                    // previous tile done with smem
   for (int i = tid; i < kDigits * kOutputs; i += kThreads) acc[i] = 0;
@@ -156,18 +172,18 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
   for (int s = 0; s < 4; ++s) acc_o[s] = acc + s * kThreads + tid;
   int nf_count[4] = {0, 0, 0, 0};
 
-  const int64_t nchunks = (p.K + kBK - 1) / kBK;
+  const int64_t nchunks = c_end > c_begin ? c_end - c_begin : 0;
   Staging st;
   int cur_nf = 0;
   if (nchunks > 0) {
-    load_chunk(0, st);
+    load_chunk(c_begin * kBK, st);
     cur_nf = store_chunk(0, st);
   }
   cur_nf = __syncthreads_or(cur_nf);
 
   for (int64_t c = 0; c < nchunks; ++c) {
     const int buf = static_cast<int>(c & 1);
-    if (c + 1 < nchunks) load_chunk((c + 1) * kBK, st);
+    if (c + 1 < nchunks) load_chunk((c_begin + c + 1) * kBK, st);
 
     const int2* Ab = As + buf * kBK * kPad;
     const int2* Bb = Bs + buf * kBK * kPad;
@@ -203,6 +219,37 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
     cur_nf = __syncthreads_or(next_nf);
   }
 
+  if (splits > 1) {
+    // this split's digits, normalised (words below 2^32, a small top digit),
+    // into the quarter's slot; a sum of up to 64 stays far inside int64
+    int64_t* slot = accg + w * (int64_t(kDigits + 1) * kOutputs);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      normalise_in_place(acc_o[s]);
+      const int o = s * kThreads + tid;
+#pragma unroll
+      for (int j = 0; j < kDigits; ++j)
+        atomicAdd(reinterpret_cast<unsigned long long*>(slot + j * kOutputs + o),
+                  static_cast<unsigned long long>(acc_o[s][j * kOutputs]));
+      if (nf_count[s])
+        atomicAdd(reinterpret_cast<unsigned long long*>(slot + kDigits * kOutputs + o),
+                  static_cast<unsigned long long>(nf_count[s]));
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last_split = atomicAdd(qdone + w, 1u) == unsigned(splits - 1);
+    __syncthreads();
+    if (!last_split) continue;
+    __threadfence();
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int o = s * kThreads + tid;
+#pragma unroll
+      for (int j = 0; j < kDigits; ++j) acc_o[s][j * kOutputs] = __ldcg(slot + j * kOutputs + o);
+      nf_count[s] = static_cast<int>(__ldcg(slot + kDigits * kOutputs + o));
+    }
+  }
+
   // epilogue: normalise, then round once (det_gemm) or write the digits
   const int64_t MN = p.M * p.N;
 #pragma unroll
@@ -232,7 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p,
 }
 
 template <int kBf16>
-cudaError_t launch_kulisch_t(const GemmArgs& a, const int* general, cudaStream_t stream) {
+cudaError_t launch_kulisch_t(const GemmArgs& a, const int* general, bool allow_split,
+                             cudaStream_t stream) {
   static bool configured = false;
   if (!configured) {
     cudaError_t e = cudaFuncSetAttribute(kulisch_smem_kernel<kBf16>,
@@ -244,18 +292,65 @@ cudaError_t launch_kulisch_t(const GemmArgs& a, const int* general, cudaStream_t
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (sms <= 0) sms = 1;
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
-  const int64_t grid = tiles < sms ? tiles : (sms > 0 ? sms : 1);
-  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(a, general);
+  // Too few 32x32 tiles to fill the GPU twice and a long K: split K among
+  // CTAs (the routed tiles are at most all of them; their count is known on
+  // the device only).  The splits' digits meet in a zeroed pool slot per
+  // quarter of every 64x64 tile.
+  // The count is the one that fills the grid's waves best, at least 1024 of
+  // K per split (each item zeroes its accumulator and adds it atomically).
+  int splits = 1;
+  if (allow_split && tiles < 2 * int64_t(sms) && a.K >= 2 * 1024) {
+    const int64_t most = std::min<int64_t>(kMaxSplits, a.K / 1024);
+    double best = 0.0;
+    for (int64_t sp = 2; sp <= most; ++sp) {
+      const int64_t items = tiles * sp;
+      const int64_t waves = (items + sms - 1) / sms;
+      const double fill = static_cast<double>(items) / static_cast<double>(waves * sms);
+      if (fill > best + 1e-9) {
+        best = fill;
+        splits = static_cast<int>(sp);
+      }
+    }
+  }
+  int64_t* accg = nullptr;
+  unsigned* qdone = nullptr;
+  void* scratch = nullptr;
+  if (splits > 1) {
+    const int64_t slots = 4 * ((a.M + 2 * kBM - 1) / (2 * kBM)) * ((a.N + 2 * kBN - 1) / (2 * kBN));
+    const size_t acc_bytes = sizeof(int64_t) * size_t(slots) * (kDigits + 1) * kOutputs;
+    const size_t bytes = acc_bytes + sizeof(unsigned) * size_t(slots);
+    cudaError_t e = pool_alloc(&scratch, bytes, stream);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(scratch, 0, bytes, stream);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(scratch, stream);
+      return e;
+    }
+    accg = static_cast<int64_t*>(scratch);
+    qdone = reinterpret_cast<unsigned*>(static_cast<char*>(scratch) + acc_bytes);
+  }
+  const int64_t items = tiles * splits;
+  const int64_t grid = items < sms ? items : sms;
+  kulisch_smem_kernel<kBf16><<<static_cast<unsigned>(grid), kThreads, kSmemBytes, stream>>>(
+      a, general, splits, accg, qdone);
   note_launch();
-  return cudaGetLastError();
+  cudaError_t e = cudaGetLastError();
+  if (scratch != nullptr) {
+    const cudaError_t f = cudaFreeAsync(scratch, stream);
+    if (e == cudaSuccess) e = f;
+  }
+  return e;
 }
 
 }  // namespace
 
-cudaError_t launch_kulisch(const GemmArgs& a, const int* general, cudaStream_t stream) {
+cudaError_t launch_kulisch(const GemmArgs& a, const int* general, bool allow_split,
+                           cudaStream_t stream) {
   if (a.M == 0 || a.N == 0) return cudaSuccess;
-  return a.bf16 ? launch_kulisch_t<1>(a, general, stream) : launch_kulisch_t<0>(a, general, stream);
+  return a.bf16 ? launch_kulisch_t<1>(a, general, allow_split, stream)
+                : launch_kulisch_t<0>(a, general, allow_split, stream);
 }
 
 }  // namespace det

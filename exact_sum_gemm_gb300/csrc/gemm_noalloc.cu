@@ -59,7 +59,7 @@ cudaError_t launch_gemm_partial_noalloc(const GemmArgs& g, cudaStream_t stream) 
   cudaError_t e = scratch_address(&scratch);
   if (e != cudaSuccess) return e;
   const int64_t slots = band_slots(g);      // partials keep fallback digits in P itself
-  return run_gemm_with_scratch(g, scratch, slots, stream);
+  return run_gemm_with_scratch(g, scratch, slots, false, stream);   // no pool slot either
 }
 
 }  // namespace det

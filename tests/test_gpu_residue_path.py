@@ -245,3 +245,18 @@ def test_fused_and_two_pass_planes_agree(oracle_mod):
     assert_bits_equal(two_pass, fused, "K-minor operands against K-contiguous ones")
     rows = np.array([0, 7, 1279, 1280, 2303])
     assert_bits_equal(fused[rows], np_bits(oracle_mod.gemm(A[rows], B)), "fused planes")
+
+
+def test_general_kernel_split_over_k(oracle_mod):
+    # Wide exponents route every tile to the general kernel; with few tiles
+    # (96 x 96: nine 32 x 32 tiles, some quarters of the 64 x 64 tiles outside
+    # C) and a long K it splits K among CTAs and sums their digits exactly.
+    # A non-finite element checks the count through the split as well.
+    K = 12288
+    A = wl.loguniform_f32((96, K), 59, 0, lo=-60, hi=60)
+    B = wl.loguniform_f32((96, K), 59, 1, lo=-60, hi=60)
+    A[5, 7000] = np.float32(np.inf)
+    a, b = dev_f32(A), dev_f32(B)
+    assert_bits_equal(bits_of(dg.det_gemm(a, b)), np_bits(oracle_mod.gemm(A, B)), "split K")
+    np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(),
+                                  oracle_mod.gemm_digits(A, B))
