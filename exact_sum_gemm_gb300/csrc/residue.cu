@@ -1259,8 +1259,20 @@ cudaError_t residues_launch(const ResidueOperand& o0, const ResidueOperand& o1, 
   const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
     if (rows)
       residue_rows_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o0, o1, split);
-    else
+    else {
+      // its shared-memory tile must not keep it off SMs whose shared memory a
+      // running tensor-core GEMM has configured for itself: with the default
+      // carveout a later band's planes waited for the GEMM to end (DetLinear
+      // wgrad 842 -> 831 us with the largest carveout preferred)
+      static bool carveout = false;
+      if (!carveout) {
+        carveout = true;
+        cudaFuncSetAttribute(residue_kernel<decltype(B)::value, decltype(P)::value>,
+                             cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+      }
       residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o0, o1, split);
+    }
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
