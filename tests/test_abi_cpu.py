@@ -113,3 +113,19 @@ def test_worst_case_moduli_count_from_the_bound(dtype, bits, least):
     assert lib.det_residue_moduli(dtype, 0) == 0
     assert lib.det_residue_moduli(dtype, (1 << 19) + 1) == -1
     assert lib.det_residue_moduli(7, 64) == -1
+
+
+def test_bench_stage_spans_take_the_union_of_overlapping_records():
+    # bench.py reports a stage's busy time per call as the union of its
+    # records' intervals: two tensor-core launches that overlap at a band
+    # change count once, separate calls add up.
+    import importlib.util
+    spec = importlib.util.spec_from_file_location("bench_mod", os.path.join(ROOT, "bench.py"))
+    bench = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(bench)
+    tl = [("residue_gemm", 0.2, 0.8), ("reconstruct", 0.8, 1.1), ("residue_gemm", 0.3, 1.2),
+          ("residue_gemm", 2.0, 2.5), ("reconstruct", 0.9, 1.0), ("residue_gemm", 2.4, 3.0)]
+    spans = bench.stage_spans(tl, 2)
+    assert spans["residue_gemm"][0] == pytest.approx(((1.2 - 0.2) + (3.0 - 2.0)) / 2)
+    assert spans["residue_gemm"][1] == pytest.approx(2.0)            # records per call
+    assert spans["reconstruct"][0] == pytest.approx(0.3 / 2)
