@@ -778,20 +778,6 @@ __device__ __noinline__ uint32_t round_s128_exact(uint64_t lo, uint64_t hi, int 
   return sign | bits;
 }
 
-// The binary32 pattern of a 64-bit integer t in [2^63, 2^64), rounded to
-// nearest even, in 32-bit integer steps (a 64-bit integer-to-float
-// conversion would run on the narrow fp64 pipe): bits 63..40 are the
-// significand, bit 39 the rounding bit, bits 38..0 the sticky bits.  The
-// exponent field is 190 (2^63); a significand that rounds up to 2^24 carries
-// into it.
-__host__ __device__ __forceinline__ uint32_t f32_bits_of_top(uint64_t t) {
-  const uint32_t t_hi = static_cast<uint32_t>(t >> 32), t_lo = static_cast<uint32_t>(t);
-  const uint32_t mant = t_hi >> 8;                                  // in [2^23, 2^24)
-  const uint32_t sticky = ((t_hi & 0x7Fu) | t_lo) != 0u ? 1u : 0u;
-  const uint32_t up = (t_hi >> 7) & (sticky | mant) & 1u;
-  return (189u << 23) + mant + up;
-}
-
 // RNE_f32(S * 2^E), fast form.  The leading 64 bits of |S|, with every bit
 // below them ORed into bit 0 (a sticky bit well below the rounding position),
 // round to binary32 with the same round-to-nearest-even decision as |S|

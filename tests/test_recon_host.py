@@ -1,11 +1,12 @@
-"""The reconstruction's CRT sum checked on the host (no GPU).
+"""Reconstruction routines checked on the host (no GPU).
 
 The CUDA path rebuilds each exact dot product S from its balanced residues
 with one sum of products (three or four 32-bit limbs and a fixed-point
-quotient).  The routine is host-and-device code, so it is compiled here as a
-host program (tests/crt_host_check.cu) and checked against exact 128-bit
+quotient), then rounds the leading 64 bits of |S| to binary32 in integer
+steps.  Both routines are host-and-device code, so they are compiled here as
+a host program (tests/recon_host_check.cu) and checked against exact 128-bit
 arithmetic for every compiled count of moduli, up to the bound the moduli
-count keeps.
+count keeps, and against the host's own rounding conversion.
 """
 import os
 import shutil
@@ -15,7 +16,7 @@ import tempfile
 import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
-SRC = os.path.join(ROOT, "tests", "crt_host_check.cu")
+SRC = os.path.join(ROOT, "tests", "recon_host_check.cu")
 CSRC = os.path.join(ROOT, "exact_sum_gemm_gb300", "csrc")
 
 
@@ -26,12 +27,12 @@ def _nvcc():
     return None
 
 
-def test_crt_sum_rebuilds_every_value_in_range():
+def test_crt_sum_and_window_rounding():
     nvcc = _nvcc()
     if nvcc is None:
         pytest.skip("nvcc not found")
     with tempfile.TemporaryDirectory() as tmp:
-        exe = os.path.join(tmp, "crt_host_check")
+        exe = os.path.join(tmp, "recon_host_check")
         build = subprocess.run([nvcc, "-std=c++17", "-O2", "-I", CSRC, SRC, "-o", exe],
                                capture_output=True, text=True)
         assert build.returncode == 0, build.stderr
