@@ -76,6 +76,8 @@ def test_host_side_validation_without_gpu():
     assert lib.det_gemm_strided_batched(0, 3, 2, 2, 4, 4, 4, 0, 8, 4, 4, 0, 8, 6, 2, 4, S) == 6
     # bias: the widened K (in + 1) must stay within the per-call limit
     assert lib.det_linear_forward_bias(0, 2, 1 << 19, 2, 4, 4, 4, 4, S) == 4
+    # the moduli diagnostic rejects a negative count before touching CUDA
+    assert lib.det_moduli_used(None, -1) == -1
     assert lib.det_linear_forward_bias(0, 2, 4, 2, 4, 4, 6, 4, S) == 6       # misaligned bias
     assert lib.det_linear_bias_grad((1 << 19) + 1, 4, 4, 4, S) == 4          # K = batch
     assert lib.det_linear_bias_grad(4, -1, 4, 4, S) == 3
