@@ -132,7 +132,8 @@ __host__ __device__ __forceinline__ void crt_s128(const int32_t (&r)[kNumModuli]
   acc[1] += static_cast<int64_t>(q) * crt_negM_limb(P, 1);
   acc[2] += static_cast<int64_t>(q) * crt_negM_limb(P, 2);
   if constexpr (kTop) acc3 += q * crt_negM_limb(P, 3);
-  // S = acc0 + acc1 2^32 + acc2 2^64 + acc3 2^96 (mod 2^128); |acc_l| < 2^43
+  // S = acc0 + acc1 2^32 + acc2 2^64 (+ acc3 2^96) modulo 2^128 (2^96 with
+  // three limbs); |acc_l| < 2^43
   const uint64_t a0 = static_cast<uint64_t>(acc[0]);
   const uint64_t a1lo = static_cast<uint64_t>(acc[1]) << 32;
   lo = a0 + a1lo;

@@ -167,7 +167,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, Re
       const int s = d.e - em + kDeepGap;
       const bool deep = d.nonfinite || (d.m != 0 && s < 0);
       // a bf16 significand widened to binary32 carries 16 zero bits: drop them
-      // (exactly) so that |X_int| < 2^27; the reconstruction scales back by 2^32
+      // (exactly) so that |X_int| < 2^26; the reconstruction scales back by 2^32
       const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
       x[h] = static_cast<float>(deep ? 0 : mi);                        // exact: |mi| < 2^24
       pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 18]
