@@ -44,6 +44,9 @@ SMI_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.act
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 REASON_NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+DTYPE_DETAIL = ("inputs and output f32; products of bf16 residues (|r| <= 138) on the tensor "
+                "cores with exact fp32 accumulation, reduced modulo p; int64 CRT rebuild and "
+                "one rounding (the digits are exact integers throughout)")
 
 
 def parse_args():
@@ -245,7 +248,7 @@ def stage_spans(timeline, calls):
     return out
 
 
-def roofline_for(stage_ms, stages, props, peaks, lib, workload="normal"):
+def roofline_for(stage_ms, stages, props, peaks, lib, workload="normal", pipes=None):
     """Roofline of the dominant stage (by device time per step)."""
     if not stage_ms:
         return None
@@ -283,33 +286,99 @@ def roofline_for(stage_ms, stages, props, peaks, lib, workload="normal"):
                 "executed_tensor_tflops": round(executed / t / 1e12, 2),
                 "executed_frac": round(executed / t / 1e12 / peak, 4),
                 "kernel_ms": round(stage_ms[dom], 4)}
-    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    peak = alu_peak_gops(props.multi_processor_count, clock_mhz)
-    achieved = exact_flops / t / 1e9
-    return {"kernel": dom, "bound": "alu", "achieved": round(achieved, 3), "peak": round(peak, 1),
-            "unit": "Gop/s", "frac": round(achieved / peak, 5), "traffic": None,
-            "peak_source": f"derived: {props.multi_processor_count} SMs x 128 INT32 lanes x "
-                           f"{clock_mhz:.0f} MHz x 2 ops per exact MAC",
-            "kernel_ms": round(stage_ms[dom], 4)}
+    return alu_roofline(dom, exact_flops / 2.0, stage_ms[dom], pipes)
 
 
-def pipe_fractions(gflops, props, peaks):
-    """The metric's reference pipes: exact work per second against the INT32 issue
-    peak (one exact multiply-add per lane per clock, counted as 2 ops like 2MNK)
-    and against GB300's nominal FP64 rate.  Above 1.0 means the tensor-core
-    residue path outruns any CUDA-core Kulisch kernel's ceiling."""
-    clock_mhz = float(peaks.get("sm_max_mhz", 2070.0))
-    int_peak = alu_peak_gops(props.multi_processor_count, clock_mhz)
-    fp64_peak = 1250.0
-    return {"int32_issue": round(gflops / int_peak, 4), "int32_issue_peak_gops": round(int_peak, 1),
-            "fp64": round(gflops / fp64_peak, 2), "fp64_peak_gflops": fp64_peak,
-            "basis": f"{props.multi_processor_count} SMs x 128 INT32 lanes x {clock_mhz:.0f} MHz x "
-                     "2 ops per exact MAC; FP64 nominal 1.25 TFLOP/s"}
+def alu_roofline(kernel, macs, ms, pipes):
+    """A CUDA-core exact kernel against the measured INT32 issue peak: exact
+    MACs per second over instructions per second (one per MAC is the bound)."""
+    achieved = macs / (ms * 1e-3) / 1e9
+    if pipes:
+        peak = max(pipes["kinds"]["iadd"]["gops"], pipes["kinds"]["lop3"]["gops"])
+        src = "measured in this run: max(iadd, lop3) instructions/s (pipe_peaks)"
+    else:
+        peak = alu_peak_gops(152, 2070.0) / 2.0
+        src = "fallback: 152 SMs x 128 lanes x 2070 MHz (no measurement in this run)"
+    return {"kernel": kernel, "bound": "alu", "achieved": round(achieved, 3), "peak": peak,
+            "unit": "G exact MAC/s vs G instr/s", "frac": round(achieved / peak, 5),
+            "traffic": None, "peak_source": src, "kernel_ms": round(ms, 4)}
+
+
+PIPE_KINDS = {"iadd": 0, "lop3": 1, "imad": 2, "imad_wide": 3, "ffma": 4, "dfma": 5}
+
+
+def measure_pipe_peaks(lib, dev, uuid=None, target_s=0.6):
+    """Measured throughput of the CUDA-core pipes an exact accumulation could
+    run on: one launch per instruction kind (det_pipe_benchmark: 8 blocks of
+    256 threads per SM, dependency rings of 8 accumulators per thread), timed
+    with CUDA events over a launch of about `target_s` seconds after a short
+    calibration launch; nvidia-smi samples the SM clock meanwhile."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    threads = lib.det_pipe_benchmark_threads_per_block()
+    per_iter = lib.det_pipe_benchmark_ops_per_thread_iter()
+    blocks = sms * 8
+    out = torch.empty(blocks * threads, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.3)
+    res = {}
+
+    def timed(kind, iters):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        st = lib.det_pipe_benchmark(kind, iters, blocks, out.data_ptr(), stream.cuda_stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        if st != 0:
+            raise RuntimeError(f"det_pipe_benchmark({kind}) returned {st}")
+        return e0.elapsed_time(e1) * 1e-3
+
+    for name, kind in PIPE_KINDS.items():
+        iters = 256
+        t = timed(kind, iters)
+        while t < 0.05:                      # calibrate on a launch long enough to time
+            iters *= 4
+            t = timed(kind, iters)
+        iters = max(iters, int(iters * target_s / t))
+        t = timed(kind, iters)
+        ops = float(iters) * per_iter * threads * blocks
+        res[name] = {"gops": round(ops / t / 1e9, 1), "seconds": round(t, 3),
+                     "per_sm_per_clk": None}
+    clocks = sampler.stop()
+    mhz = clocks["sm_mhz"] if clocks else None
+    for r in res.values():
+        if mhz:
+            r["per_sm_per_clk"] = round(r["gops"] * 1e9 / (sms * mhz * 1e6), 2)
+    return {"kinds": res, "sms": sms, "clocks": clocks,
+            "how": "det_pipe_benchmark: one launch per kind, 8 x 256 threads per SM, rings of 8 "
+                   "independent accumulators, one PTX instruction per operation; ops / CUDA-event "
+                   "time of a launch of about 0.6 s"}
+
+
+def pipe_fractions(gflops, pipes):
+    """The metric's reference pipes, from the measured peaks: exact MACs per
+    second (GFLOP/s / 2) against the INT32 issue peak (the faster of the
+    measured integer add and logic rates: one instruction per exact MAC is an
+    upper bound for any CUDA-core Kulisch kernel), and exact GFLOP/s against the
+    measured FP64 FMA flop rate (2 flops per fma), the pipe the page's kernel
+    runs on.  Above 1.0 means the tensor-core residue path outruns that pipe's
+    ceiling."""
+    k = pipes["kinds"]
+    int_peak = max(k["iadd"]["gops"], k["lop3"]["gops"])
+    fp64 = 2.0 * k["dfma"]["gops"]
+    return {"int32_issue": round(gflops / 2.0 / int_peak, 4),
+            "int32_issue_peak_gops": int_peak,
+            "fp64": round(gflops / fp64, 2), "fp64_peak_gflops": round(fp64, 1),
+            "basis": "measured in this run (pipe_peaks): INT32 = max(iadd, lop3) instructions/s, "
+                     "one per exact MAC; FP64 = 2 x dfma/s"}
 
 
 def alu_peak_gops(sm_count, clock_mhz):
-    """Integer-ALU issue peak: SMs x 128 lanes x clock, one instruction per exact
-    multiply-add counted as 2 ops (the same convention as 2MNK)."""
+    """Nominal integer-ALU issue rate: SMs x 128 lanes x clock, one instruction
+    per exact multiply-add counted as 2 ops (the same convention as 2MNK); only
+    a fallback when no measured peak is at hand."""
     return 2.0 * sm_count * 128 * clock_mhz * 1e6 / 1e9
 
 
@@ -435,18 +504,19 @@ def run_ours(args):
     if rank != 0:
         return 0
 
+    pipes = measure_pipe_peaks(lib, dev, uuid) if not args.no_extras else None
     peaks = measured_peaks()
     kern_avg = statistics.mean(kern_ms)
     # per det_gemm call: the time covered by a stage's records (a stage may
     # run once per row band, on several streams at once), so the stages need
     # not add up to the step
     stage_ms = {k: v[0] for k, v in stages.items()}
-    roofline = roofline_for(stage_ms, stages, props, peaks, lib, args.workload)
+    roofline = roofline_for(stage_ms, stages, props, peaks, lib, args.workload, pipes)
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
-        "data": "synthetic",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "dtype_detail": DTYPE_DETAIL, "data": "synthetic",
         "config": workload_config(args.workload, {"parallelism": f"{world} independent replicas"
                                                   if world > 1 else "single GPU"}),
         "gpu_launches": int(launches),
@@ -456,7 +526,8 @@ def run_ours(args):
         "det_gemm_ms": round(kern_avg, 4),
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "roofline": roofline,
-        "pipe_fractions": pipe_fractions(value / world, props, peaks),
+        "pipe_fractions": pipe_fractions(value / world, pipes) if pipes else None,
+        "pipe_peaks": pipes,
         "clocks": clocks,
     }
     line.update(extras)

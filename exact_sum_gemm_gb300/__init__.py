@@ -26,12 +26,40 @@ __all__ = [
     "det_gemm_batched", "det_linear_forward", "det_linear_forward_bias", "det_linear_dgrad",
     "det_linear_wgrad", "det_linear_bias_grad", "DetLinear",
     "DetError", "DET_DIGITS", "DET_PLANES", "DET_K_MAX", "DET_MAX_COMBINE", "library",
+    "device_status", "release_scratch", "set_scratch_retention", "scratch_stats",
 ]
 
 
 def library():
     """The loaded C-ABI library (ctypes handle); builds it on first use."""
     return _native.lib()
+
+
+def device_status(clear=False):
+    """'ok', or 'timeout' if a bounded wait in one of the library's kernels ran
+    out on the current device since the status was last cleared (that call's
+    outputs are NaN).  Synchronises the device."""
+    st = _native.lib().det_device_status(1 if clear else 0)
+    if st == 9:
+        return "timeout"
+    _native.check("det_device_status", st)
+    return "ok"
+
+
+def release_scratch():
+    """Synchronise the current device and return the library's unused scratch."""
+    _native.check("det_release_scratch", _native.lib().det_release_scratch())
+
+
+def set_scratch_retention(nbytes):
+    """Bytes of freed scratch the library's pools keep reserved (default: all)."""
+    _native.check("det_set_scratch_retention",
+                  _native.lib().det_set_scratch_retention(int(nbytes)))
+
+
+def scratch_stats():
+    """(allocations so far, reserved bytes, used bytes) of the library's scratch pool."""
+    return _native.scratch_stats()
 
 
 def _torch():

@@ -22,7 +22,7 @@ DET_MAX_COMBINE = 1 << 20
 STATUS_NAMES = {
     0: "DET_OK", 1: "DET_ERR_INVALID_ARG", 2: "DET_ERR_DTYPE", 3: "DET_ERR_SHAPE",
     4: "DET_ERR_K_LIMIT", 5: "DET_ERR_OVERFLOW", 6: "DET_ERR_ALIGNMENT", 7: "DET_ERR_CUDA",
-    8: "DET_ERR_NOALLOC_LIMIT",
+    8: "DET_ERR_NOALLOC_LIMIT", 9: "DET_ERR_TIMEOUT",
 }
 
 # symbol -> (restype, argtypes); mirrors include/det_gemm.h
@@ -49,6 +49,15 @@ SIGNATURES = {
     "det_linear_wgrad": (_i32, [_i64, _i64, _i64, _vp, _vp, _vp, _vp]),
     "det_linear_forward_bias": (_i32, [_i32, _i64, _i64, _i64, _vp, _vp, _vp, _vp, _vp]),
     "det_linear_bias_grad": (_i32, [_i64, _i64, _vp, _vp, _vp]),
+    "det_device_status": (_i32, [_i32]),
+    "det_selftest_wait_timeout": (_i32, [ctypes.c_uint64, _vp]),
+    "det_release_scratch": (_i32, []),
+    "det_set_scratch_retention": (_i32, [ctypes.c_uint64]),
+    "det_scratch_stats": (_i32, [ctypes.POINTER(ctypes.c_uint64), ctypes.POINTER(ctypes.c_uint64),
+                                 ctypes.POINTER(ctypes.c_uint64)]),
+    "det_pipe_benchmark": (_i32, [_i32, _i64, _i64, _vp, _vp]),
+    "det_pipe_benchmark_ops_per_thread_iter": (_i32, []),
+    "det_pipe_benchmark_threads_per_block": (_i32, []),
     "det_gemm_strided_batched": (_i32, [_i32, _i64, _i64, _i64, _i64, _vp, _i64, _i32, _i64, _vp,
                                         _i64, _i32, _i64, _vp, _i64, _i64, _vp]),
 }
@@ -104,6 +113,14 @@ def stage_timeline(n_max: int = 4096):
     t1 = (ctypes.c_double * n_max)()
     n = lib().det_stage_timeline(names, t0, t1, n_max)
     return [(names[i].decode(), t0[i], t1[i]) for i in range(n)]
+
+
+def scratch_stats():
+    """(allocations taken from the library's pools, reserved bytes, used bytes)
+    for the current device."""
+    vals = [ctypes.c_uint64(0) for _ in range(3)]
+    check("det_scratch_stats", lib().det_scratch_stats(*[ctypes.byref(v) for v in vals]))
+    return tuple(int(v.value) for v in vals)
 
 
 def check(fn_name: str, status: int) -> None:

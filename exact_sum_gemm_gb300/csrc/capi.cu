@@ -102,8 +102,20 @@ const char* det_status_string(det_status s) {
     case DET_ERR_NOALLOC_LIMIT:
       return "DET_ERR_NOALLOC_LIMIT: problem needs more scratch than det_gemm_partial_noalloc's "
              "fixed array (DET_NOALLOC_SCRATCH_BYTES)";
+    case DET_ERR_TIMEOUT:
+      return "DET_ERR_TIMEOUT: a bounded wait inside a kernel ran out; that call's outputs are NaN";
   }
   return "DET_ERR_UNKNOWN";
+}
+
+det_status det_release_scratch(void) { return from_cuda(det::pool_release()); }
+
+det_status det_set_scratch_retention(uint64_t bytes) {
+  return from_cuda(det::pool_set_retention(bytes));
+}
+
+det_status det_scratch_stats(uint64_t* allocations, uint64_t* reserved_bytes, uint64_t* used_bytes) {
+  return from_cuda(det::pool_stats(allocations, reserved_bytes, used_bytes));
 }
 
 det_status det_gemm(det_dtype dtype, int64_t M, int64_t N, int64_t K, const void* A, int64_t lda,

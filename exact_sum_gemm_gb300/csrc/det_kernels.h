@@ -4,7 +4,43 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <mutex>
+
 namespace det {
+
+// Devices a process may use this library on (per-device state is kept in
+// arrays of this size).
+constexpr int kMaxDevices = 64;
+
+// One-time set-up per device: run(init) calls init(dev) with the current
+// device `dev`, once per device and under a lock, until it succeeds.  Function
+// attributes (cudaFuncSetAttribute) belong to the device that was current when
+// they were set, so they are configured through one of these.
+class PerDeviceOnce {
+ public:
+  template <class F>
+  cudaError_t run(F&& init) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu_);
+    if (done_[dev]) return cudaSuccess;
+    e = init(dev);
+    if (e == cudaSuccess) done_[dev] = true;
+    return e;
+  }
+
+ private:
+  std::mutex mu_;
+  bool done_[kMaxDevices] = {};
+};
+
+// Sticky device-side status word of this library on the current device
+// (bit kStatusTimeout: a bounded wait in one of its kernels ran out).  The
+// address is looked up once per device.
+constexpr unsigned kStatusTimeout = 1u;
+cudaError_t device_status_word(unsigned** out);
 
 // Count one enqueued kernel (diagnostic; see det_kernel_launches).
 void note_launch(int n = 1);
@@ -48,6 +84,13 @@ cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
 // Stream-ordered scratch from the library's memory pool (one per device, kept
 // reserved between calls); release with cudaFreeAsync on the same stream.
 cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream);
+// Allocations taken so far (all devices) and the current device's pool's
+// reserved and used bytes (0 before its first allocation).
+cudaError_t pool_stats(uint64_t* allocations, uint64_t* reserved, uint64_t* used);
+// Synchronise the current device, then return its pool's unused memory.
+cudaError_t pool_release();
+// Bytes every pool keeps reserved after its frees (default: all of them).
+cudaError_t pool_set_retention(uint64_t bytes);
 
 // y = RNE_f32(x W^T + bias): the bias enters as one more exact product,
 // 1 * bias[o], through [x | 1] and [W | bias] built in pool scratch.

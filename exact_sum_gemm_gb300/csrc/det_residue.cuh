@@ -187,7 +187,8 @@ struct ResGemmArgs {
   int nplanes;
   int8_t* res;                // [nplanes][.][N] balanced residues: plane u of row m at
   int64_t res_plane;          //   res + u * res_plane + m * N
-  int* error;
+  int* error;                 // per-call flag: a bounded wait ran out (outputs become NaN)
+  unsigned* status;           // the library's sticky device status word, or null
   const int* used;            // moduli to compute (device int, in [used_min, nplanes]), or
   int used_min;               //   null for all nplanes; the grid is sized for used_min
 };

@@ -18,6 +18,7 @@
 
 #include <math.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "det_arith.cuh"
@@ -28,9 +29,10 @@
 namespace det {
 namespace {
 
-constexpr int kMaxDevices = 64;
 std::mutex g_pool_mu;
 cudaMemPool_t g_pool[kMaxDevices] = {};
+uint64_t g_retention = ~uint64_t(0);          // release threshold of the pools (bytes kept)
+std::atomic<uint64_t> g_pool_allocs{0};       // allocations taken from the pools
 
 cudaError_t device_pool(cudaMemPool_t* out) {
   int dev = 0;
@@ -46,7 +48,7 @@ cudaError_t device_pool(cudaMemPool_t* out) {
     cudaMemPool_t pool;
     e = cudaMemPoolCreate(&pool, &props);
     if (e != cudaSuccess) return e;
-    uint64_t keep = ~uint64_t(0);
+    uint64_t keep = g_retention;
     e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
     if (e != cudaSuccess) return e;
     g_pool[dev] = pool;
@@ -114,7 +116,54 @@ cudaError_t pool_alloc(void** p, size_t bytes, cudaStream_t stream) {
   cudaMemPool_t pool;
   cudaError_t e = device_pool(&pool);
   if (e != cudaSuccess) return e;
+  g_pool_allocs.fetch_add(1, std::memory_order_relaxed);
   return cudaMallocFromPoolAsync(p, bytes, pool, stream);
+}
+
+cudaError_t pool_stats(uint64_t* allocations, uint64_t* reserved, uint64_t* used) {
+  if (allocations != nullptr) *allocations = g_pool_allocs.load(std::memory_order_relaxed);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  cudaMemPool_t pool;
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mu);
+    pool = g_pool[dev];
+  }
+  uint64_t r = 0, u = 0;
+  if (pool != nullptr) {
+    e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrReservedMemCurrent, &r);
+    if (e == cudaSuccess) e = cudaMemPoolGetAttribute(pool, cudaMemPoolAttrUsedMemCurrent, &u);
+    if (e != cudaSuccess) return e;
+  }
+  if (reserved != nullptr) *reserved = r;
+  if (used != nullptr) *used = u;
+  return cudaSuccess;
+}
+
+cudaError_t pool_release() {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  // every stream-ordered free must have run before its memory can go back
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  return g_pool[dev] != nullptr ? cudaMemPoolTrimTo(g_pool[dev], 0) : cudaSuccess;
+}
+
+cudaError_t pool_set_retention(uint64_t bytes) {
+  std::lock_guard<std::mutex> lock(g_pool_mu);
+  g_retention = bytes;
+  for (int d = 0; d < kMaxDevices; ++d) {
+    if (g_pool[d] == nullptr) continue;
+    uint64_t keep = bytes;
+    const cudaError_t e = cudaMemPoolSetAttribute(g_pool[d], cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 namespace {
@@ -266,6 +315,9 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // the pairs)
   auto hi_of = [&](int b) { return (b & 1) ? bs->hi2 : hi; };
 
+  unsigned* status = nullptr;                     // sticky expiry record of the TC kernels
+  e = device_status_word(&status);
+  if (e != cudaSuccess) return e;
   const Scratch s = carve_scratch(base, g, 0);
   int* counts = reinterpret_cast<int*>(base + L.off_counts);
   int* error = counts + g.M + g.N;
@@ -329,7 +381,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     const cudaStream_t hs = hi_of(b);
     StageScope t(kStageResidueGemm, hs);
     ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
-                   rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error, used + b, least};
+                   rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error, status, used + b, least};
     // 256 x 256 tiles on CTA pairs, unless a single 128-row tile covers M or
     // the device cannot run clusters of two
     if (rows > 128) {

@@ -330,18 +330,25 @@ constexpr size_t kSmemBytes = sizeof(BandSmem);
 
 template <int kBf16>
 cudaError_t configure_t(int* per_sm) {
-  static int cached = 0;
-  if (cached == 0) {
-    cudaError_t e = cudaFuncSetAttribute(band_kernel<kBf16>,
+  // the shared-memory attribute is per device, and so is the occupancy it allows
+  static PerDeviceOnce once;
+  static int cached[kMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = once.run([&](int d) {
+    cudaError_t r = cudaFuncSetAttribute(band_kernel<kBf16>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
+    if (r != cudaSuccess) return r;
     int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, band_kernel<kBf16>, kThreads, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    cached = n > 0 ? n : 1;
-  }
-  *per_sm = cached;
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, band_kernel<kBf16>, kThreads, kSmemBytes);
+    if (r != cudaSuccess) return r;
+    cached[d] = n > 0 ? n : 1;
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  *per_sm = cached[dev];
   return cudaSuccess;
 }
 

@@ -281,14 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p, c
 template <int kBf16>
 cudaError_t launch_kulisch_t(const GemmArgs& a, const int* general, bool allow_split,
                              cudaStream_t stream) {
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(kulisch_smem_kernel<kBf16>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;                 // the attribute is per device
+  cudaError_t ce = configured.run([](int) {
+    return cudaFuncSetAttribute(kulisch_smem_kernel<kBf16>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes));
+  });
+  if (ce != cudaSuccess) return ce;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);

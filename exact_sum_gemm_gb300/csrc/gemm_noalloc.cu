@@ -23,7 +23,6 @@ namespace {
 // One array per device that loads the library; kept until the process exits.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[DET_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_addr[kMaxDevices] = {};
 

@@ -55,19 +55,15 @@ constexpr uint32_t kTmemCols = 512;
 constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  return ptx::mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
 
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
+// A bounded wait ran out: the call's outputs become NaN (per-call flag) and
+// the library's device status records the expiry (det_device_status).
+__device__ __forceinline__ void report_timeout(const ResGemmArgs& a) {
+  atomicExch(a.error, 1);
+  if (a.status != nullptr) atomicOr(a.status, kStatusTimeout);
 }
 
 // Job J of a unit holding T (1 or 2) tiles -> (tile index tt < T, K chunk c):
@@ -172,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_bounded(&empty[j % kStages], (j / kStages) & 1u)) ok = false;
         }
       }
-      if (!ok) atomicExch(a.error, 1);
+      if (!ok) report_timeout(a);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -219,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::mma_commit(&acc_ready[acc]);  // chunk c of modulus u is in TMEM
       }
       }
-      if (!ok) atomicExch(a.error, 1);
+      if (!ok) report_timeout(a);
     }
   } else {
     const int g = warp & 3;                // TMEM lanes 32g .. 32g+31
@@ -290,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) ptx::mbar_arrive(&acc_free[acc]);
     }
     }
-    if (!ok && lane == 0) atomicExch(a.error, 1);
+    if (!ok && lane == 0) report_timeout(a);
   }
 
   ptx::tc_fence_before();
@@ -344,14 +340,12 @@ bool make_plane_map(CUtensorMap* map, const void* base, int64_t rows, int64_t Kp
 
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
-  static bool configured = false;
-  if (!configured) {
-    cudaError_t e = cudaFuncSetAttribute(residue_gemm_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (e != cudaSuccess) return e;
-    configured = true;
-  }
+  static PerDeviceOnce configured;                 // the attribute is per device
+  cudaError_t ce = configured.run([](int) {
+    return cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(kSmemBytes));
+  });
+  if (ce != cudaSuccess) return ce;
   CUtensorMap tmA, tmB;
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kBlockM) ||
       !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kBlockN))

@@ -57,19 +57,15 @@ constexpr size_t kSmemBytes = size_t(kStages) * kStageBytes + 1024 + 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 static_assert(kHalfM % kPlaneRows == 0 && (kTileN / 2) % kPlaneRows == 0, "whole row groups");
 
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
+  return ptx::mbar_wait_ns(bar, parity, kWaitLimitNs);
 }
 
-__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((i & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) return false;
-  }
+// A bounded wait ran out: the call's outputs become NaN (per-call flag) and
+// the library's device status records the expiry (det_device_status).
+__device__ __forceinline__ void report_timeout(const ResGemmArgs& a) {
+  atomicExch(a.error, 1);
+  if (a.status != nullptr) atomicOr(a.status, kStatusTimeout);
 }
 
 __device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
@@ -188,7 +184,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (uint32_t j = first; j < it; ++j)
           if (!wait_bounded(&empty[j % kStages], (j / kStages) & 1u)) ok = false;
       }
-      if (!ok) atomicExch(a.error, 1);
+      if (!ok) report_timeout(a);
     }
   }
   else if (warp == 1) {
@@ -236,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mma_commit_pair(&acc_ready[acc]);   // window c of modulus u in both TMEMs
         }
       }
-      if (!ok) atomicExch(a.error, 1);
+      if (!ok) report_timeout(a);
       ptx::mma_commit_pair(fin);                   // every MMA of this CTA pair has completed
     }
   } else {
@@ -311,7 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ptx::mbar_arrive_cluster(free_leader + static_cast<uint32_t>(acc * sizeof(uint64_t)));
       }
     }
-    if (!ok && lane == 0) atomicExch(a.error, 1);
+    if (!ok && lane == 0) report_timeout(a);
   }
 
   // this CTA's roles are done; then every MMA of the pair has finished
@@ -320,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   ptx::tc_fence_before();
   __syncthreads();
   if (warp == 1) {
-    if (!wait_bounded(fin, 0) && lane == 0) atomicExch(a.error, 1);
+    if (!wait_bounded(fin, 0) && lane == 0) report_timeout(a);
   }
   ptx::cluster_sync();
   ptx::tc_fence_after();
@@ -331,12 +327,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
-  constexpr int kMaxDevices = 64;
-  static int max_clusters[kMaxDevices] = {};            // 0: not yet queried, -1: unusable
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorNotSupported;
+  static PerDeviceOnce queried;
+  static int max_clusters[kMaxDevices] = {};            // -1: clusters of two unusable
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -348,16 +340,23 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (max_clusters[dev] == 0) {
+  cudaError_t e = queried.run([&](int d) {
     int n = 0, sms = 0;
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    e = cudaFuncSetAttribute(residue_gemm_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kSmemBytes));
-    cfg.gridDim = dim3(static_cast<unsigned>(sms > 1 ? sms / 2 * 2 : 2), 1, 1);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel, &cfg);
-    max_clusters[dev] = (e == cudaSuccess && n > 0) ? n : -1;
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
+    cudaError_t r = cudaFuncSetAttribute(residue_gemm_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    cudaLaunchConfig_t q = cfg;
+    q.gridDim = dim3(static_cast<unsigned>(sms > 1 ? sms / 2 * 2 : 2), 1, 1);
+    if (r == cudaSuccess) r = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel, &q);
+    max_clusters[d] = (r == cudaSuccess && n > 0) ? n : -1;
     cudaGetLastError();                                 // a failed query is not the caller's error
-  }
+    return cudaSuccess;
+  });
+  if (e != cudaSuccess) return e == cudaErrorInvalidDevice ? cudaErrorNotSupported : e;
+  int dev = 0;
+  e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
   if (max_clusters[dev] < 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kHalfM) ||

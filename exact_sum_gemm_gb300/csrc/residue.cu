@@ -1250,13 +1250,14 @@ cudaError_t residues_launch(const ResidueOperand& o0, const ResidueOperand& o1, 
       // running tensor-core GEMM has configured for itself: with the default
       // carveout a later band's planes waited for the GEMM to end (DetLinear
       // wgrad 842 -> 831 us with the largest carveout preferred)
-      static bool carveout = false;
-      if (!carveout) {
-        carveout = true;
+      static PerDeviceOnce carveout;             // the attribute is per device
+      carveout.run([](int) {
         cudaFuncSetAttribute(residue_kernel<decltype(B)::value, decltype(P)::value>,
                              cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
-      }
+        cudaGetLastError();                      // a preference only: never the caller's error
+        return cudaSuccess;
+      });
       residue_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(o0, o1, split);
     }
     return cudaSuccess;

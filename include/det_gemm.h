@@ -57,7 +57,8 @@ typedef enum {
   DET_ERR_OVERFLOW = 5,    /* digit headroom would be exceeded (combine of too many parts) */
   DET_ERR_ALIGNMENT = 6,   /* a pointer is not aligned to its element size */
   DET_ERR_CUDA = 7,        /* a CUDA call or kernel launch failed */
-  DET_ERR_NOALLOC_LIMIT = 8 /* problem too large for det_gemm_partial_noalloc's fixed scratch */
+  DET_ERR_NOALLOC_LIMIT = 8, /* problem too large for det_gemm_partial_noalloc's fixed scratch */
+  DET_ERR_TIMEOUT = 9        /* a bounded wait inside a kernel ran out (det_device_status) */
 } det_status;
 
 typedef enum { DET_F32 = 0, DET_BF16 = 1 } det_dtype;
@@ -100,6 +101,72 @@ int det_stage_report(const char** names, double* total_ms, int* counts, int max)
  * entries, clears the record and returns the number written.  Any output
  * pointer may be NULL. */
 int det_stage_timeline(const char** names, double* start_ms, double* stop_ms, int max);
+
+/* Device-side status of the library on the current device.  The tensor-core
+ * kernels bound every wait on a barrier (about 2 s); if one runs out, that
+ * call's outputs are the canonical NaN and the kernel records the expiry in a
+ * per-device word, which stays set until cleared.  det_device_status returns
+ * DET_ERR_TIMEOUT if it is set, DET_OK if not (DET_ERR_CUDA if it cannot be
+ * read), and resets it when `clear` is nonzero.  It synchronises the device
+ * first, so it sees every call enqueued before it.  A diagnostic, not part of
+ * the page's calls. */
+det_status det_device_status(int clear);
+
+/* Self-test of that mechanism: enqueues on `stream` one small kernel that
+ * waits, with the same bounded-wait routine as the tensor-core kernels, on a
+ * barrier that nothing ever releases; after limit_ns nanoseconds (1 ..
+ * 10^9, else DET_ERR_INVALID_ARG) the wait gives up, records the expiry in the
+ * status word as those kernels do, and the kernel returns.  No memory is
+ * written but that word; the device stays usable. */
+det_status det_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* Scratch memory.  det_gemm and det_gemm_partial (and the bias variants)
+ * take their working memory per call, stream-ordered, from a memory pool that
+ * the library creates per device; it is released on the call's stream when
+ * the call's work is done.  By default the pool keeps the freed memory
+ * reserved for the next call (a 4096^3 f32 det_gemm uses about 1.1 GB), so
+ * repeated calls do not go back to the driver.
+ *   det_release_scratch: synchronises the current device, then returns all
+ *     of its pool's unused memory to the device.
+ *   det_set_scratch_retention: bytes each pool keeps reserved after its
+ *     memory is freed; 0 returns freed scratch at the next synchronisation
+ *     (slower repeated calls), UINT64_MAX (the default) keeps it all.
+ *   det_scratch_stats: allocations the library has taken from its pools so
+ *     far (all devices), and the current device's reserved and in-use pool
+ *     bytes (0 before its first allocation).  Any pointer may be NULL.
+ * Stream use: besides the caller's stream, the residue path runs on five
+ * library streams per device (two of the greatest priority for the
+ * tensor-core launches, and three for overlapped reconstruction and general
+ * tiles), joined back to the caller's stream by events before the call
+ * returns.  Calls from different caller streams on one device share those
+ * streams, so their tensor-core work runs one call after the other; the
+ * enqueue itself is serialised by a lock. */
+det_status det_release_scratch(void);
+det_status det_set_scratch_retention(uint64_t bytes);
+det_status det_scratch_stats(uint64_t* allocations, uint64_t* reserved_bytes,
+                             uint64_t* used_bytes);
+
+/* Pipe-throughput microbenchmark (a diagnostic: the roofline denominators of
+ * exact accumulation on the CUDA cores; the page's kernel runs on the fp64
+ * scalar cores, section "Measured").  Enqueues on `stream` one launch of
+ * `blocks` blocks of det_pipe_benchmark_threads_per_block() threads; each
+ * thread performs iters * det_pipe_benchmark_ops_per_thread_iter()
+ * operations of one kind, each a single instruction in a dependency ring of
+ * independent accumulators, and writes one 32-bit word to out[thread] (a
+ * device buffer of blocks * threads words, so the work cannot be dropped).
+ * The caller times the launch (CUDA events) and divides the operation count
+ * by the time.  iters >= 1, 1 <= blocks <= 2^20. */
+enum {
+  DET_PIPE_IADD = 0,        /* 32-bit integer add (add.u32) */
+  DET_PIPE_LOP3 = 1,        /* three-input logic op (lop3.b32) */
+  DET_PIPE_IMAD = 2,        /* 32-bit integer multiply-add, low half (mad.lo.u32) */
+  DET_PIPE_IMAD_WIDE = 3,   /* 32 x 32 -> 64-bit multiply-add (mad.wide.u32) */
+  DET_PIPE_FFMA = 4,        /* fp32 fused multiply-add */
+  DET_PIPE_DFMA = 5         /* fp64 fused multiply-add */
+};
+det_status det_pipe_benchmark(int kind, int64_t iters, int64_t blocks, void* out, void* stream);
+int det_pipe_benchmark_ops_per_thread_iter(void);
+int det_pipe_benchmark_threads_per_block(void);
 
 /* Worst-case number of moduli (bf16 tensor-core GEMMs) of det_gemm's residue
  * path for this dtype and K: enough that their product exceeds twice the
@@ -177,10 +244,15 @@ det_status det_finalize(int64_t M, int64_t N, const int64_t* P, float* C, int64_
  * The working memory (per-row exponent maxima, deep-element counts and the
  * tile routing table) lives in one fixed array of DET_NOALLOC_SCRATCH_BYTES
  * bytes that is a static device variable of this library: every GPU that
- * loads the library holds it until the process exits.  A call needs
- * 8 * (M + N) bytes plus one byte per 64x64 output tile (each part rounded up
- * to 256 bytes); larger problems (M = N = 32768 fits, M = N = 49152 does not)
- * return DET_ERR_NOALLOC_LIMIT before anything is enqueued.
+ * loads the library holds it until the process exits.  With Tm = ceil(M/64),
+ * Tn = ceil(N/64), T = Tm * Tn and a(x) = x rounded up to a multiple of 256,
+ * a call needs
+ *     2 a(4 (M + N)) + a(T) + a(4 (T + 1)) + a(4 (Tm + Tn))   bytes
+ * (exponent maxima and deep counts of every row and column; one routing byte
+ * and one list entry per 64x64 output tile; the largest deep count per
+ * 64-row and 64-column block).  M = N = 20000 fits (812,544 bytes); M = N =
+ * 24576 does not (1,133,824); with M = 1, N may reach 128,767.  Larger
+ * problems return DET_ERR_NOALLOC_LIMIT before anything is enqueued.
  *
  * The first call on each device looks up the array's device address (with
  * that device current); make that first call before any stream capture.

@@ -78,6 +78,18 @@ def test_host_side_validation_without_gpu():
     assert lib.det_linear_forward_bias(0, 2, 1 << 19, 2, 4, 4, 4, 4, S) == 4
     # the moduli diagnostic rejects a negative count before touching CUDA
     assert lib.det_moduli_used(None, -1) == -1
+    # the bounded-wait self-test takes limits of 1 ns .. 1 s
+    assert lib.det_selftest_wait_timeout(0, S) == 1
+    assert lib.det_selftest_wait_timeout(1_000_000_001, S) == 1
+    # the pipe microbenchmark: kind, iteration and block counts, output alignment
+    assert lib.det_pipe_benchmark(6, 1, 1, 4, S) == 1
+    assert lib.det_pipe_benchmark(0, 0, 1, 4, S) == 1
+    assert lib.det_pipe_benchmark(0, 1, 0, 4, S) == 1
+    assert lib.det_pipe_benchmark(0, 1, (1 << 20) + 1, 4, S) == 1
+    assert lib.det_pipe_benchmark(0, 1, 1, None, S) == 1
+    assert lib.det_pipe_benchmark(0, 1, 1, 6, S) == 6
+    assert lib.det_pipe_benchmark_ops_per_thread_iter() == 8
+    assert lib.det_pipe_benchmark_threads_per_block() == 256
     assert lib.det_linear_forward_bias(0, 2, 4, 2, 4, 4, 6, 4, S) == 6       # misaligned bias
     assert lib.det_linear_bias_grad((1 << 19) + 1, 4, 4, 4, S) == 4          # K = batch
     assert lib.det_linear_bias_grad(4, -1, 4, 4, S) == 3

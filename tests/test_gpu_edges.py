@@ -68,9 +68,13 @@ SHAPES = [(1, 1, 1), (1, 1, 0), (3, 2, 0), (2, 3, 7), (7, 33, 3), (33, 7, 33), (
           (65, 31, 100), (31, 97, 129), (100, 1, 1000)]
 
 
-@pytest.mark.parametrize("mode", ["normal", "wide", "subnormal", "zeros"])
+# one fixed seed per mode, so every run draws the same inputs
+MODE_SEEDS = {"normal": 101, "wide": 102, "subnormal": 103, "zeros": 104}
+
+
+@pytest.mark.parametrize("mode", list(MODE_SEEDS))
 def test_tiny_and_ragged_shapes(oracle_mod, mode):
-    g = np.random.default_rng(hash(mode) % 1000)
+    g = np.random.default_rng(MODE_SEEDS[mode])
     for M, N, K in SHAPES:
         A = _rand(g, (M, K), mode)
         B = _rand(g, (N, K), mode)
