@@ -498,13 +498,17 @@ def run_ours(args):
     extras = {}
     if rank == 0 and not args.no_extras:
         extras = measure_extras(args, dg, a, b, c, A, B, dev, stream)
+    pipes = measure_pipe_peaks(lib, dev, uuid) if rank == 0 and not args.no_extras else None
+    if rank == 0 and not args.no_extras and args.workload == "normal":
+        del a, b, c
+        torch.cuda.empty_cache()
+        extras["workloads"] = measure_workloads(args, dev, pipes, with_cpu=True)
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
     if rank != 0:
         return 0
 
-    pipes = measure_pipe_peaks(lib, dev, uuid) if not args.no_extras else None
     peaks = measured_peaks()
     kern_avg = statistics.mean(kern_ms)
     # per det_gemm call: the time covered by a stage's records (a stage may
@@ -671,17 +675,33 @@ def measure_extras(args, dg, a, b, c, A, B, dev, stream):
     return out
 
 
-def run_configs(args):
-    """Each workload configuration timed on one GPU, inputs resident in HBM:
-    CUDA events on the current stream around `steps` calls after `warmup`
-    calls (no L2 flush: several of these problems fit in L2).  One JSON line
-    per configuration; exact GFLOP/s counts 2MNK per GEMM."""
+def oracle_time(fn, macs, cores, sample):
+    """The CPU oracle as it stands, timed once on the host cores."""
+    t0 = time.perf_counter()
+    fn()
+    dt = time.perf_counter() - t0
+    return {"value": round(2.0 * macs / dt / 1e9, 4), "unit": UNIT, "cores": cores,
+            "kind": "oracle", "sample": f"{sample}; {dt:.2f} s wall on {cores} threads",
+            "seconds": round(dt, 2)}
+
+
+def measure_workloads(args, dev, pipes=None, with_cpu=True):
+    """Every workload configuration, timed on one GPU with inputs resident in
+    HBM: CUDA events on the current stream around `steps` calls after `warmup`
+    calls (no L2 flush: the small problems fit in L2 by design).  Exact GFLOP/s
+    counts 2MNK per GEMM.  Beside each, the exact work rate against the
+    measured INT32 issue and FP64 peaks, and the CPU oracle timed on the host
+    cores (full problems, or a stated sample)."""
     import torch
     import exact_sum_gemm_gb300 as dg
     from exact_sum_gemm_gb300 import workloads as wl
-    dev = torch.device("cuda", 0)
     torch.cuda.set_device(dev)
-    steps, warm = max(1, args.steps), max(1, args.warmup)
+    steps, warm = max(2, min(args.steps, 5)), max(1, min(args.warmup, 2))
+    cores = os.cpu_count() or 1
+    if with_cpu:
+        import oracle
+        oracle.build()
+    out = {}
 
     def timed(fn, n=steps):
         for _ in range(warm):
@@ -695,53 +715,102 @@ def run_configs(args):
         torch.cuda.synchronize(dev)
         return e0.elapsed_time(e1) / n
 
-    def emit(name, ms, flops, **extra):
-        line = {"config": name, "ms": round(ms, 4),
-                "exact_gflops": round(flops / (ms * 1e-3) / 1e9, 2), "data": "synthetic"}
-        line.update(extra)
-        print(json.dumps(line), flush=True)
+    def entry(name, desc, ms, flops, cpu=None, **extra):
+        g = flops / (ms * 1e-3) / 1e9
+        e = {"workload": desc, "ms": round(ms, 4), "exact_gflops": round(g, 2)}
+        if pipes:
+            pf = pipe_fractions(g, pipes)
+            e["vs_int32_issue"] = pf["int32_issue"]
+            e["vs_fp64"] = pf["fp64"]
+        if cpu is not None:
+            e["cpu_baseline"] = cpu
+        e.update(extra)
+        out[name] = e
+        if args.configs:
+            print(json.dumps({"config": name, **e, "data": "synthetic"}), flush=True)
 
     f32 = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev)
     # 64^3 f32 N(0,1): det_gemm, and 16 equal K-shards through partial/combine/finalize
-    a, b = f32(wl.normal_f32((64, 64), 0, 0)), f32(wl.normal_f32((64, 64), 0, 1))
-    emit("det_gemm f32 64x64x64 N(0,1)", timed(lambda: dg.det_gemm(a, b)), 2.0 * 64 ** 3)
+    A1, B1 = wl.normal_f32((64, 64), 0, 0), wl.normal_f32((64, 64), 0, 1)
+    a, b = f32(A1), f32(B1)
+    cpu = oracle_time(lambda: oracle.gemm(A1, B1, nthreads=cores), 64 ** 3, cores,
+                      "the full 64^3 problem") if with_cpu else None
+    entry("c1_det_gemm", "det_gemm f32 64x64x64 N(0,1), seed 0",
+          timed(lambda: dg.det_gemm(a, b)), 2.0 * 64 ** 3, cpu)
     cuts = wl.equal_cuts(64, 16)
-    emit("det_gemm_partial x16 + det_combine + det_finalize, f32 64^3",
-         timed(lambda: dg.det_gemm_sharded(a, b, cuts)), 2.0 * 64 ** 3)
+    entry("c1_shards16", "det_gemm_partial x16 + det_combine + det_finalize, same problem",
+          timed(lambda: dg.det_gemm_sharded(a, b, cuts)), 2.0 * 64 ** 3)
     # bf16 512x512x4096, exponents U{-60..60}, cancelling column pairs; 8 random K-shards
-    ab, bb, _ = wl.bf16_wide_with_cancellation(512, 512, 4096, 1)
-    ab, bb = wl.to_torch_bf16(ab, dev), wl.to_torch_bf16(bb, dev)
+    A2, B2, _ = wl.bf16_wide_with_cancellation(512, 512, 4096, 1)
+    ab, bb = wl.to_torch_bf16(A2, dev), wl.to_torch_bf16(B2, dev)
     fl = 2.0 * 512 * 512 * 4096
-    emit("det_gemm bf16 512x512x4096, exponents U{-60..60}, cancelling pairs",
-         timed(lambda: dg.det_gemm(ab, bb)), fl)
+    cpu = oracle_time(lambda: oracle.gemm(A2, B2, dtype="bf16", nthreads=cores), fl / 2, cores,
+                      "the full 512x512x4096 problem") if with_cpu else None
+    entry("c2_det_gemm", "det_gemm bf16 512x512x4096, exponents U{-60..60}, cancelling pairs, "
+          "seed 1", timed(lambda: dg.det_gemm(ab, bb)), fl, cpu)
     rcuts = wl.kshard_cuts(4096, 8, 1)
-    emit("det_gemm_partial x8 (random cuts) + combine + finalize, same bf16 workload",
-         timed(lambda: dg.det_gemm_sharded(ab, bb, rcuts)), fl)
+    entry("c2_shards8", "det_gemm_partial x8 (random cuts) + combine + finalize, same problem",
+          timed(lambda: dg.det_gemm_sharded(ab, bb, rcuts)), fl)
     # DetLinear 4096 -> 4096 on a 2048 x 4096 batch: forward, dgrad, wgrad
     x_np, w_np = wl.detlinear_inputs()
     x, w = f32(x_np), f32(w_np)
     y = dg.det_linear_forward(x, w)
     dy = (y * 2.0 ** -22).contiguous()
     fl = 2.0 * 2048 * 4096 * 4096
-    emit("DetLinear forward f32 2048x4096 -> 4096", timed(lambda: dg.det_linear_forward(x, w)), fl)
-    emit("DetLinear dgrad f32", timed(lambda: dg.det_linear_dgrad(dy, w)), fl)
-    emit("DetLinear wgrad f32", timed(lambda: dg.det_linear_wgrad(dy, x)), fl)
+    cpu_f = cpu_d = cpu_w = None
+    if with_cpu:
+        cpu_f = oracle_time(lambda: oracle.gemm(x_np, w_np, nthreads=cores), fl / 2, cores,
+                            "the full forward GEMM (2048x4096x4096)")
+        # the oracle's time does not depend on which upstream gradient it is
+        # given: a generator draw of the same scale stands in for dy
+        dy_np = wl.normal_f32((256, 4096), 2, 5, scale_pow2=-22)
+        w_t = np.ascontiguousarray(w_np.T)
+        cpu_d = oracle_time(lambda: oracle.gemm(dy_np, w_t, nthreads=cores), 256 * 4096 * 4096,
+                            cores, "256 of the 2048 rows of dgrad (each row costs the same)")
+        dyt = wl.normal_f32((256, 2048), 2, 6, scale_pow2=-22)
+        x_t = np.ascontiguousarray(x_np.T)
+        cpu_w = oracle_time(lambda: oracle.gemm(dyt, x_t, nthreads=cores), 256 * 4096 * 2048,
+                            cores, "256 of the 4096 rows of wgrad (each row costs the same)")
+    entry("c3_forward", "DetLinear 4096->4096 forward, x 2048x4096 N(0,1), W N(0,1)/64, seed 2",
+          timed(lambda: dg.det_linear_forward(x, w)), fl, cpu_f)
+    entry("c3_dgrad", "DetLinear dgrad (dy = 2y/numel)", timed(lambda: dg.det_linear_dgrad(dy, w)),
+          fl, cpu_d)
+    entry("c3_wgrad", "DetLinear wgrad", timed(lambda: dg.det_linear_wgrad(dy, x)), fl, cpu_w)
     del x, w, y, dy
     # f32 256x256, K = 2^19, |x| = 2^U[-100,100]
-    K = 1 << 19
-    a4 = f32(wl.loguniform_f32((256, K), 3, 0))
-    b4 = f32(wl.loguniform_f32((256, K), 3, 1))
-    emit("det_gemm f32 256x256x524288, |x| = 2^U[-100,100]",
-         timed(lambda: dg.det_gemm(a4, b4), n=max(1, steps // 2)), 2.0 * 256 * 256 * K)
-    del a4, b4
+    KL = 1 << 19
+    A4, B4 = wl.loguniform_f32((256, KL), 3, 0), wl.loguniform_f32((256, KL), 3, 1)
+    a4, b4 = f32(A4), f32(B4)
+    cpu = oracle_time(lambda: oracle.gemm(A4, B4, nthreads=cores), 256 * 256 * KL, cores,
+                      "the full 256x256x524288 problem") if with_cpu else None
+    entry("c4_det_gemm", "det_gemm f32 256x256x524288, |x| = 2^U[-100,100], seed 3",
+          timed(lambda: dg.det_gemm(a4, b4), n=2), 2.0 * 256 * 256 * KL, cpu)
+    del a4, b4, A4, B4
+    # the headline shape with wide exponents: |x| = 2^U[-40,40]
+    Aw = wl.loguniform_f32((4096, 4096), 0, 0, lo=-40, hi=40)
+    Bw = wl.loguniform_f32((4096, 4096), 0, 1, lo=-40, hi=40)
+    aw, bw = f32(Aw), f32(Bw)
+    cpu = oracle_time(lambda: oracle.gemm(np.ascontiguousarray(Aw[::64]), Bw, nthreads=cores),
+                      64 * 4096 * 4096, cores, "64 evenly spaced rows of the 4096^3 problem") \
+        if with_cpu else None
+    entry("wide_4096", "det_gemm f32 4096^3, |x| = 2^U[-40,40], seed 0",
+          timed(lambda: dg.det_gemm(aw, bw), n=3), 2.0 * 4096 ** 3, cpu)
+    del aw, bw, Aw, Bw
     # one training step of the 1024 -> 4096 -> 1024 MLP, batch 256 (targets
     # from the teacher through det_gemm, forward, backward, SGD update)
     relu = lambda t: torch.clamp_min(t, 0.0)
     w1, w2 = wl.mlp_init(stream=0)
     t1, t2 = wl.mlp_init(stream=1)
     t1d, t2d = f32(t1), f32(t2)
-    xb = f32(wl.mlp_batch(0))
+    x5 = wl.mlp_batch(0)
+    xb = f32(x5)
     lr = torch.tensor(1e-2, dtype=torch.float32, device=dev)
+    cpu = None
+    if with_cpu:
+        h_np = np.ascontiguousarray(x5[:32])
+        cpu = oracle_time(lambda: oracle.gemm(h_np, t1, nthreads=cores), 32 * 4096 * 1024, cores,
+                          "32 of the 256 rows of the step's first GEMM (each of the seven GEMMs "
+                          "is 256x4096x1024 or its transpose, so the rate carries over)")
     for shards in (1, 4):
         l1 = dg.DetLinear(1024, 4096, device=dev, k_shards=shards, weight=torch.from_numpy(w1))
         l2 = dg.DetLinear(4096, 1024, device=dev, k_shards=shards, weight=torch.from_numpy(w2))
@@ -757,8 +826,16 @@ def run_configs(args):
                 for q in (l1.weight, l2.weight):
                     q.sub_(q.grad * lr)
         # 2 teacher + 2 forward + 1 dgrad + 2 wgrad GEMMs of 256 x 1024 x 4096
-        emit(f"MLP 1024->4096->1024 training step, batch 256, k_shards={shards}",
-             timed(step), 7 * 2.0 * 256 * 1024 * 4096)
+        entry(f"c5_step_shards{shards}", f"MLP 1024->4096->1024 training step, batch 256, "
+              f"k_shards={shards}, seed 7", timed(step), 7 * 2.0 * 256 * 1024 * 4096,
+              cpu if shards == 1 else None)
+    return out
+
+
+def run_configs(args):
+    """Each workload configuration timed on one GPU (one JSON line each)."""
+    import torch
+    measure_workloads(args, torch.device("cuda", 0), None, with_cpu=False)
     return 0
 
 

@@ -31,6 +31,8 @@ SIGNATURES = {
     "det_abi_version": (_i32, []),
     "det_status_string": (ctypes.c_char_p, [_i32]),
     "det_kernel_launches": (ctypes.c_uint64, []),
+    "det_tile_routes": (_i32, [ctypes.POINTER(_i64)]),
+    "det_set_wide_path": (_i32, [_i32]),
     "det_stage_timing": (_i32, [_i32]),
     "det_residue_moduli": (_i32, [_i32, _i64]),
     "det_moduli_used": (_i32, [ctypes.POINTER(_i32), _i32]),
@@ -121,6 +123,14 @@ def scratch_stats():
     vals = [ctypes.c_uint64(0) for _ in range(3)]
     check("det_scratch_stats", lib().det_scratch_stats(*[ctypes.byref(v) for v in vals]))
     return tuple(int(v.value) for v in vals)
+
+
+def tile_routes():
+    """{tiles, general, wide, kulisch} of the last residue-path call (synchronises)."""
+    out = (_i64 * 4)()
+    if lib().det_tile_routes(out) != 0:
+        raise DetError("det_tile_routes", 7)
+    return {"tiles": out[0], "general": out[1], "wide": out[2], "kulisch": out[3]}
 
 
 def check(fn_name: str, status: int) -> None:

@@ -87,6 +87,16 @@ int det_moduli_used(int* out, int max) {
   return det::moduli_record(out, max);
 }
 
+int det_set_wide_path(int enable) { return det::set_wide_path(enable); }
+
+int det_tile_routes(int64_t* out) {
+  if (out == nullptr) return -1;
+  long long rec[4];
+  if (det::route_record(rec) != 0) return -1;
+  for (int i = 0; i < 4; ++i) out[i] = rec[i];
+  return 0;
+}
+
 uint64_t det_kernel_launches(void) { return det::g_launches.load(std::memory_order_relaxed); }
 
 const char* det_status_string(det_status s) {

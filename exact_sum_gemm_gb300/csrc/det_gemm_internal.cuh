@@ -1,6 +1,7 @@
 // Shared constants and launch plumbing of the exact GEMM kernels.
 #pragma once
 
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -49,6 +50,34 @@ cudaError_t launch_band(const GemmArgs& g, const Scratch& s, cudaStream_t stream
 // (false: allocate nothing).
 cudaError_t launch_kulisch(const GemmArgs& g, const int* general, bool allow_split,
                            cudaStream_t stream);
+
+// The general tiles of a residue-path call (route and list in s): the wide
+// residue path where the tiles' rows span at most its window and are finite,
+// the general kernel for the rest.  wide_prepare: statistics, norms and
+// planes on `stream`, then ev_planes; wide_finish: the wide tensor-core GEMM,
+// its reconstruction and the general kernel on `tail`, after ev_planes.
+struct WidePlan {
+  bool active;                // false: the problem is too large, general kernel only
+  const int* general;         // the narrow routing's list of general tiles
+  void* mem;                  // scratch, released on the tail stream
+  int* wide;                  // wide tiles (count first)
+  int* rest;                  // tiles left for the general kernel (count first)
+  void* ctl;                  // moduli count, error flag, counters
+  __nv_bfloat16* planesA;
+  __nv_bfloat16* planesB;
+  int8_t* res;
+  const int* loA;             // exponent keys of the rows' smallest elements
+  const int* loB;
+  int pmax;
+  int64_t Kp;
+};
+cudaError_t wide_prepare(const GemmArgs& g, const Scratch& s, cudaStream_t stream,
+                         cudaEvent_t ev_planes, WidePlan* plan);
+cudaError_t wide_finish(const GemmArgs& g, const WidePlan& plan, cudaStream_t tail,
+                        cudaEvent_t ev_planes);
+// Diagnostic: the last residue-path call's 64x64 tiles (all, general before
+// the wide split, wide, left for the general kernel); synchronises.
+int route_record(long long* out);
 
 // Pre-pass + band + general kernels with caller-provided scratch of at least
 // scratch_bytes(g, slots) bytes (256-byte aligned); allow_alloc lets the

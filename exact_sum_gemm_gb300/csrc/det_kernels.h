@@ -47,7 +47,8 @@ void note_launch(int n = 1);
 
 // Stages timed by det_stage_timing / det_stage_report.
 enum Stage { kStagePrepass = 0, kStageResiduePlanes, kStageResidueGemm, kStageReconstruct,
-             kStageGeneral, kStageBand, kNumStages };
+             kStageGeneral, kStageBand, kStageWideStats, kStageWidePlanes, kStageWideGemm,
+             kStageWideReconstruct, kNumStages };
 
 // Records a CUDA event pair around its scope on `stream` while stage timing is on.
 class StageScope {
@@ -77,6 +78,9 @@ struct GemmArgs {
   int64_t ldc;
   int64_t* P;         // canonical digit planes [20][M][N] (det_gemm_partial), or null
 };
+
+// Wide residue path on (1, the default) or off (0); returns the previous setting.
+int set_wide_path(int enable);
 
 // Exact GEMM; writes C (if args.C) or the digit planes P (if args.P).
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);

@@ -16,11 +16,23 @@ namespace det {
 // 2^24, where fp32 accumulation is exact.  The product of all 14 moduli
 // exceeds 2^109, enough for |S| < 2^19 * 2^84 * 2 (1 + 2^-7) (f32 shallow
 // integers are below 2^(24+18)).
+//
+// The wide path (wide.cu) continues the list with 2^8 and 25 primes from 193
+// down to 71, all coprime to the first 14 and to one another: 40 moduli whose
+// product exceeds 2^292.  2^8 is even, but its reduction below rounds a/256
+// exactly (1/256 is exact in binary32), so its residues are the nearest
+// ones, |r| <= 128.
 constexpr int kNumModuli = 14;
+constexpr int kNumModuliWide = 40;
 __host__ __device__ constexpr int modulus(int i) {
   return i == 0 ? 255 : i == 1 ? 253 : i == 2 ? 251 : i == 3 ? 247 : i == 4 ? 241 : i == 5 ? 239
        : i == 6 ? 233 : i == 7 ? 229 : i == 8 ? 227 : i == 9 ? 223 : i == 10 ? 217 : i == 11 ? 211
-       : i == 12 ? 199 : 197;
+       : i == 12 ? 199 : i == 13 ? 197 : i == 14 ? 256 : i == 15 ? 193 : i == 16 ? 191
+       : i == 17 ? 181 : i == 18 ? 179 : i == 19 ? 173 : i == 20 ? 167 : i == 21 ? 163
+       : i == 22 ? 157 : i == 23 ? 151 : i == 24 ? 149 : i == 25 ? 139 : i == 26 ? 137
+       : i == 27 ? 131 : i == 28 ? 127 : i == 29 ? 113 : i == 30 ? 109 : i == 31 ? 107
+       : i == 32 ? 103 : i == 33 ? 101 : i == 34 ? 97 : i == 35 ? 89 : i == 36 ? 83
+       : i == 37 ? 79 : i == 38 ? 73 : 71;
 }
 // Balanced representatives, inverses and products modulo the moduli (compile
 // time).
@@ -88,6 +100,8 @@ struct ResidueOperand {
                               // sum_k X_int^2 / 2^norm_shift over the row's shallow elements
   unsigned* keymax;           // fused kernel: [rows], zeroed (row maxima of exponent keys)
   unsigned long long* norm_max;  // fused kernel: zeroed slot for the largest norm of these rows
+  unsigned* dmax;             // fused kernel: [rows/64], zeroed: largest deep count of each
+                              //   64-row block (or null)
 };
 
 // Thresholds of the moduli choice: P moduli suffice for a row band whose
@@ -147,6 +161,10 @@ void note_moduli_bands(int bands);
 // of the band's A rows and of B's rows (B's filled by band 0's launch, which
 // also covers B); done: a zeroed block counter per launch.
 constexpr int kFusedK = 4096;
+// A band whose every 64x64 tile goes to the general tiles (the smallest
+// 64-row-block maximum of deep counts of its rows of A plus that of B's rows
+// exceeds the lists' capacity) computes no modulus: its count is 0 and its
+// tensor-core GEMM returns at once; the routing sends all its tiles on.
 struct FusedBand {
   const unsigned long long* maxA;
   const unsigned long long* maxB;
@@ -154,6 +172,11 @@ struct FusedBand {
   int* used;
   int band, least, most;
   ModuliThresholds thr;
+  const unsigned* dmaxA;      // the band's 64-row blocks of A (null: never skip)
+  int64_t blocksA;
+  const unsigned* dmaxB;      // B's 64-row blocks
+  int64_t blocksB;
+  int cap;
 };
 bool fused_residues_ok(const ResidueOperand& o, int bf16);
 // Band 0 with B (o1 null: a band b >= 1 alone).
@@ -163,10 +186,12 @@ cudaError_t launch_residues_fused(const ResidueOperand& o0, const ResidueOperand
 // whose product exceeds 2 (1 + 2^-7) sqrt(max normA * max normB) 2^shift,
 // written to *used (a Cauchy-Schwarz bound of every |S| in the band).
 // maxima: two zeroed 8-byte slots of scratch per launch.
+// countA / countB (the rows' deep counts) and cap: as FusedBand, a band all of
+// whose tiles go to the general tiles gets the count 0 (null countA: never).
 cudaError_t launch_moduli(const unsigned long long* normA, int64_t rowsA,
                           const unsigned long long* normB, int64_t rowsB, int bf16, int least,
                           int most, int* used, int band, unsigned long long* maxima,
-                          cudaStream_t stream);
+                          const int* countA, const int* countB, int cap, cudaStream_t stream);
 cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cudaStream_t stream);
 // Two operands' planes in one launch (one grid covering both).
 cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1, int bf16, int nplanes,
@@ -189,14 +214,17 @@ struct ResGemmArgs {
   int64_t res_plane;          //   res + u * res_plane + m * N
   int* error;                 // per-call flag: a bounded wait ran out (outputs become NaN)
   unsigned* status;           // the library's sticky device status word, or null
-  const int* used;            // moduli to compute (device int, in [used_min, nplanes]), or
-  int used_min;               //   null for all nplanes; the grid is sized for used_min
+  const int* used;            // moduli to compute (device int, in [used_min, nplanes]; 0:
+  int used_min;               //   nothing), or null for all nplanes; the grid is sized for used_min
+  int grid_moduli;            // if > 0: size the grid for this many moduli instead
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
 // Moduli a GEMM launch computes (every CTA reads the same device int).
+// A count of 0 means the launch has nothing to compute (no work item).
 __device__ __forceinline__ int planes_used(const ResGemmArgs& a) {
   if (a.used == nullptr) return a.nplanes;
   const int u = *a.used;
+  if (u <= 0) return 0;
   return u < a.used_min ? a.used_min : (u > a.nplanes ? a.nplanes : u);
 }
 // The same GEMM with 256 x 256 tiles over CTA pairs (cta_group::2); returns

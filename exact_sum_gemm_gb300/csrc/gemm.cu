@@ -179,6 +179,7 @@ cudaError_t launch_band_path(const GemmArgs& g, cudaStream_t stream) {
 }
 
 constexpr int kMaxBands = 4;
+std::atomic<int> g_wide_path{1};                   // det_set_wide_path
 
 struct ResidueScratch {
   size_t bytes;
@@ -191,11 +192,14 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   size_t b = align_up(scratch_bytes(g, 0), 1024);
   // zeroed together: countA [M], countB [N], error, deep-row/col counters [2],
   // moduli per band [kMaxBands], fused-launch block counters [kMaxBands],
-  // exponent-key maxima keymaxA [M], keymaxB [N]; then the row-norm bounds
-  // normA [M], normB [N] and each band's two norm maxima [2 kMaxBands]
+  // exponent-key maxima keymaxA [M], keymaxB [N], the largest deep count of
+  // every 64-row block of A and of B [tiles_m + tiles_n]; then the row-norm
+  // bounds normA [M], normB [N] and four slots per band [4 kMaxBands] (norm
+  // maxima of A and B, and the moduli kernel's two block minima)
   r.off_counts = b;
-  r.off_norms = align_up(b + sizeof(int) * size_t(2 * (g.M + g.N) + 3 + 2 * kMaxBands), 8);
-  b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + g.N + 2 * kMaxBands);
+  r.off_norms = align_up(b + sizeof(int) * size_t(2 * (g.M + g.N) + 3 + 2 * kMaxBands +
+                                                  tiles_mn(g)), 8);
+  b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + g.N + 4 * kMaxBands);
   r.zero_bytes = b - r.off_counts;
   b = align_up(b, 1024);
   r.off_deep_idx = b;                    // deep rows [M], deep columns [N]
@@ -227,7 +231,9 @@ struct BandSync {
   cudaStream_t side = nullptr;                     // deep-output reconstruction
   cudaStream_t gen = nullptr;                      // general-tile kernel
   cudaStream_t fast2 = nullptr;                    // fast reconstruction of bands >= 1
+  cudaStream_t wide = nullptr;                     // general tiles: statistics and planes
   cudaEvent_t gen_fork = nullptr, gen_done = nullptr;   // after the routing; general kernel done
+  cudaEvent_t wide_planes = nullptr, wide_gemm = nullptr;  // gen -> tensor-core stream -> gen
   cudaEvent_t planes_done[kMaxBands] = {};         // caller's stream -> hi
   cudaEvent_t gemm_done[kMaxBands] = {};           // hi -> caller's stream
   cudaEvent_t deep_done[kMaxBands] = {};           // side -> caller's stream
@@ -256,10 +262,19 @@ cudaError_t band_sync(int dev, BandSync** out) {
     // crowd band 0's: measured slower)
     if (e == cudaSuccess && b.fast2 == nullptr)
       e = cudaStreamCreateWithPriority(&b.fast2, cudaStreamNonBlocking, least);
+    // small kernels that fit beside a tensor-core CTA (no shared memory but
+    // the planes kernel's, which prefers the largest carveout): dispatched
+    // ahead of the reconstruction's many blocks
+    if (e == cudaSuccess && b.wide == nullptr)
+      e = cudaStreamCreateWithPriority(&b.wide, cudaStreamNonBlocking, greatest);
     if (e == cudaSuccess && b.gen_fork == nullptr)
       e = cudaEventCreateWithFlags(&b.gen_fork, cudaEventDisableTiming);
     if (e == cudaSuccess && b.gen_done == nullptr)
       e = cudaEventCreateWithFlags(&b.gen_done, cudaEventDisableTiming);
+    if (e == cudaSuccess && b.wide_planes == nullptr)
+      e = cudaEventCreateWithFlags(&b.wide_planes, cudaEventDisableTiming);
+    if (e == cudaSuccess && b.wide_gemm == nullptr)
+      e = cudaEventCreateWithFlags(&b.wide_gemm, cudaEventDisableTiming);
     for (int i = 0; i < kMaxBands && e == cudaSuccess; ++i) {
       cudaEvent_t* ev[4] = {&b.planes_done[i], &b.gemm_done[i], &b.deep_done[i], &b.fast_done[i]};
       for (int k = 0; k < 4 && e == cudaSuccess; ++k)
@@ -324,8 +339,10 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   int* used = error + 3;                                             // moduli per band
   unsigned* done = reinterpret_cast<unsigned*>(used + kMaxBands);    // fused-launch counters
   unsigned* keymax = done + kMaxBands;                               // [M] then [N]
+  unsigned* dmax = keymax + g.M + g.N;                               // [tiles_m] then [tiles_n]
+  const int64_t tiles_m = (g.M + kTile - 1) / kTile, tiles_n = (g.N + kTile - 1) / kTile;
   unsigned long long* norms = reinterpret_cast<unsigned long long*>(base + L.off_norms);
-  unsigned long long* maxima = norms + g.M + g.N;                    // [2 b]: band b's A, [1]: B
+  unsigned long long* maxima = norms + g.M + g.N;                    // [4 b]: band b's A, [1]: B
   const int least = residue_planes_least(g.bf16);
   uint2* listA = reinterpret_cast<uint2*>(base + L.off_listA);
   uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
@@ -343,7 +360,7 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // exponent maxima, planes, norms and the moduli count in one launch per
   // band (no separate pre-pass over A and B)
   const ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
-                          norms + g.M, keymax + g.M, maxima + 1};
+                          norms + g.M, keymax + g.M, maxima + 1, dmax + tiles_m};
   const bool fused = fused_residues_ok(rb, g.bf16) &&
                      fused_residues_ok(ResidueOperand{g.A, g.lda, g.opA, g.M, g.K, Kp}, g.bf16);
   {
@@ -354,7 +371,10 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   if (e != cudaSuccess) return e;
   const ModuliThresholds thr = moduli_thresholds(g.bf16);
   auto fused_band = [&](int b) {
-    return FusedBand{maxima + 2 * b, maxima + 1, done + b, used + b, b, least, nplanes, thr};
+    const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
+    return FusedBand{maxima + 4 * b, maxima + 1, done + b, used + b, b, least, nplanes, thr,
+                     dmax + m0 / kTile, (rows + kTile - 1) / kTile, dmax + tiles_m, tiles_n,
+                     deep_list_cap(g.K)};
   };
   // the residue kernels' deep-list counters double as the rows' deep counts,
   // from which the tiles are routed
@@ -363,12 +383,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
     return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
                           planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
-                          counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0, maxima + 2 * b};
+                          counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0, maxima + 4 * b,
+                          dmax + m0 / kTile};
   };
   // the band's moduli count, once its rows' and B's norm bounds are complete
   auto moduli_of_band = [&](int b) {
     return launch_moduli(norms + edge[b], edge[b + 1] - edge[b], norms + g.M, g.N, g.bf16, least,
-                         nplanes, used + b, b, maxima + 2 * b, stream);
+                         nplanes, used + b, b, maxima + 4 * b, counts + edge[b], counts + g.M,
+                         deep_list_cap(g.K), stream);
   };
   auto planes_of_band = [&](int b) {
     const ResidueOperand oa = operand_of_band(b);
@@ -405,27 +427,29 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(0), bs->planes_done[0], 0);
   if (e == cudaSuccess) e = gemm_of_band(0);
   if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[0], hi_of(0));
+  // the later bands' planes, then the routing and the wide path's first
+  // half, and only then the later bands' GEMMs: a GEMM launch that is ready
+  // but waits for the SMs of band 0's GEMM would keep the routing and those
+  // small kernels from being dispatched until band 0's GEMM ended, and every
+  // band after the first starts only then anyway.  (With one band, its GEMM
+  // is enqueued at once and the wide path's kernels run beside it.)
   for (int b = 1; b < nb && e == cudaSuccess; ++b) {
     {
       StageScope t(kStageResiduePlanes, stream);
       e = planes_of_band(b);
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->planes_done[b], stream);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(hi_of(b), bs->planes_done[b], 0);
-    if (e == cudaSuccess) e = gemm_of_band(b);
-    if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[b], hi_of(b));
   }
   if (e == cudaSuccess) {
     StageScope t(kStageResiduePlanes, stream);
     e = launch_classify(g, counts, counts + g.M, s, deep_rows, deep_rows + g.M, error + 1, stream);
   }
   bool gen_forked = false;
-  if (e == cudaSuccess) {
-    // the general kernel's tiles need only the routing: it runs beside the
-    // tensor-core GEMMs (the reconstruction skips those tiles), on a stream of
-    // its own: it uses shared memory, so it cannot share an SM with a
-    // tensor-core CTA and may wait for the GEMMs, which must not hold up the
-    // reconstruction behind it
+  WidePlan plan{};
+  const bool wide_on = g_wide_path.load(std::memory_order_relaxed) != 0;
+  if (e == cudaSuccess && !wide_on) {
+    // the wide path switched off: the general kernel takes every general
+    // tile, beside the GEMMs on the lowest-priority stream
     e = cudaEventRecord(bs->gen_fork, stream);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->gen, bs->gen_fork, 0);
     if (e == cudaSuccess) {
@@ -434,6 +458,31 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
       e = launch_kulisch(g, s.general, true, bs->gen);
     }
     if (e == cudaSuccess) e = cudaEventRecord(bs->gen_done, bs->gen);
+  }
+  if (e == cudaSuccess && wide_on) {
+    // the general tiles need only the routing: the wide path's statistics,
+    // norms and planes run on a greatest-priority stream of their own (small
+    // kernels that fit beside a tensor-core CTA); its tensor-core GEMM, its
+    // reconstruction and the general kernel follow the last band's GEMM on
+    // that GEMM's stream: they need whole SMs, and a launch waiting for them
+    // any earlier at that priority would hold up the dispatch of the
+    // reconstruction.  With no general tile every one of them returns at once.
+    e = cudaEventRecord(bs->gen_fork, stream);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(bs->wide, bs->gen_fork, 0);
+    if (e == cudaSuccess) {
+      gen_forked = true;
+      e = wide_prepare(g, s, bs->wide, bs->wide_planes, &plan);
+    }
+  }
+  for (int b = 1; b < nb && e == cudaSuccess; ++b) {
+    e = cudaStreamWaitEvent(hi_of(b), bs->planes_done[b], 0);
+    if (e == cudaSuccess && wide_on) e = cudaStreamWaitEvent(hi_of(b), bs->wide_planes, 0);
+    if (e == cudaSuccess) e = gemm_of_band(b);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->gemm_done[b], hi_of(b));
+  }
+  if (e == cudaSuccess && gen_forked && wide_on) {
+    e = wide_finish(g, plan, hi_of(nb - 1), bs->wide_planes);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->gen_done, hi_of(nb - 1));
   }
   // Band b's reconstruction needs the routing (gen_fork, recorded on the
   // caller's stream after it) and band b's GEMM.  Its deep outputs go to the
@@ -481,11 +530,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     join = bs->fast_done[0];
     if (cudaEventRecord(join, bs->fast2) == cudaSuccess) cudaStreamWaitEvent(stream, join, 0);
     if (cudaEventRecord(bs->gen_done, bs->gen) == cudaSuccess) cudaStreamWaitEvent(stream, bs->gen_done, 0);
+    if (cudaEventRecord(bs->gen_done, bs->wide) == cudaSuccess) cudaStreamWaitEvent(stream, bs->gen_done, 0);
   }
   return e;
 }
 
 }  // namespace
+
+int set_wide_path(int enable) { return g_wide_path.exchange(enable ? 1 : 0); }
 
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;

@@ -94,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * tiles_n;
   const int64_t tile_pairs = (tiles + 1) / 2;
   const int64_t units = tile_pairs * planes_used(a);
+  if (units == 0) return;                  // nothing to compute: leave before any set-up
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -357,7 +358,8 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (sms <= 0) sms = 1;
   const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * ((a.N + kBlockN - 1) / kBlockN);
   // sized for the fewest moduli the launch may compute (every CTA has a unit)
-  const int64_t units = (tiles + 1) / 2 * (a.used != nullptr ? a.used_min : a.nplanes);
+  const int64_t units = (tiles + 1) / 2 *
+      (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
   residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   note_launch();

@@ -94,6 +94,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t tiles_n = (a.N + kTileN - 1) / kTileN;
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * tiles_n;
   const int64_t singles = tiles * planes_used(a);  // (modulus, tile), modulus-major
+  // a cluster with no item (a launch sized for more moduli than it computes)
+  // issues no MMA, so it neither commits nor waits for the final commit
+  const bool has_work = cluster < singles;
+  if (singles == 0) return;                // nothing for any cluster: leave before any set-up
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -233,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) report_timeout(a);
-      ptx::mma_commit_pair(fin);                   // every MMA of this CTA pair has completed
+      if (has_work) ptx::mma_commit_pair(fin);     // every MMA of this CTA pair has completed
     }
   } else {
     const int g = warp & 3;                // TMEM lanes 32g .. 32g+31 of this CTA
@@ -315,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // both CTAs meet before the columns are released
   ptx::tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 1 && has_work) {
     if (!wait_bounded(fin, 0) && lane == 0) report_timeout(a);
   }
   ptx::cluster_sync();
@@ -365,7 +369,8 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * ((a.N + kTileN - 1) / kTileN);
   // sized for the fewest moduli the launch may compute, so every cluster
   // has at least one item whatever count the device chooses
-  const int64_t singles = tiles * (a.used != nullptr ? a.used_min : a.nplanes);
+  const int64_t singles =
+      tiles * (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const int64_t clusters = singles < max_clusters[dev] ? singles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
   e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, tmA, tmB, a);

@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   const int em = kmax != 0 ? kmax - 150 : 0;
   const int64_t nkb = o.Kp / kStageK;
   float sum = 0.0f;                                 // this thread's X_int^2 / 2^norm_shift
+  int deep_seen = 0;                                // largest list slot + 1 this thread took
   constexpr float kHalfShift = kBf16 ? 0x1p-8f : 0x1p-26f;
 #pragma unroll
   for (int v = 0; v < kFusedRuns; ++v) {
@@ -347,6 +348,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       if (deep && k + h < o.K && live_row) {
         const int slot = atomicAdd(o.list_count + r, 1);
         if (slot < o.cap) o.list[r * o.cap + slot] = make_uint2(static_cast<uint32_t>(k + h), bits[v][h]);
+        deep_seen = max(deep_seen, slot + 1);
       }
       const float f = __fmul_rn(__fmul_rn(x[h], pw[h]), kHalfShift);   // exact
       sum = __fmaf_rn(f, f, sum);
@@ -363,15 +365,36 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   for (int w = 16; w >= 1; w /= 2) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, w));
   if (lane == 0 && live_row && sum > 0.0f)
     atomicAdd(o.norm + r, __float2ull_ru(__fmul_ru(sum, 1.0f + 0x1p-16f)));
-  __syncthreads();                                  // the row's norm is complete
-  if (tid != 0) return;
-  if (live_row) atomicMax(o.norm_max, __ldcg(o.norm + r));
+  // the row's deep count is the largest slot + 1 any thread took: one
+  // atomicMax per warp that found a deep element into its 64-row block
+  deep_seen = __reduce_max_sync(0xFFFFFFFFu, deep_seen);
+  if (lane == 0 && deep_seen > 0 && o.dmax != nullptr)
+    atomicMax(o.dmax + r / kTile, static_cast<unsigned>(deep_seen));
+  __syncthreads();                                  // the row's norm and deep count are complete
+  if (tid >= 32) return;
+  unsigned last = 0;
+  if (tid == 0) {
+    if (live_row) atomicMax(o.norm_max, __ldcg(o.norm + r));
+    __threadfence();
+    last = atomicAdd(fb.done, 1u) == gridDim.x - 1 ? 1u : 0u;
+  }
+  if (__shfl_sync(0xFFFFFFFFu, last, 0) == 0u) return;
+  // the launch's last block (its first warp): every row's maximum is in place
   __threadfence();
-  if (atomicAdd(fb.done, 1u) != gridDim.x - 1) return;
-  // the launch's last block: every row's maximum is in place
+  unsigned minA = ~0u, minB = ~0u;
+  if (fb.dmaxA != nullptr) {
+    for (int64_t i = lane; i < fb.blocksA; i += 32) minA = min(minA, __ldcg(fb.dmaxA + i));
+    for (int64_t i = lane; i < fb.blocksB; i += 32) minB = min(minB, __ldcg(fb.dmaxB + i));
+    minA = __reduce_min_sync(0xFFFFFFFFu, minA);
+    minB = __reduce_min_sync(0xFFFFFFFFu, minB);
+  }
+  if (lane != 0) return;
   const unsigned long long a = atomicAdd(const_cast<unsigned long long*>(fb.maxA), 0ull);
   const unsigned long long b = atomicAdd(const_cast<unsigned long long*>(fb.maxB), 0ull);
-  const int Pn = choose_moduli(a, b, fb.least, fb.most, fb.thr);
+  int Pn = choose_moduli(a, b, fb.least, fb.most, fb.thr);
+  if (fb.dmaxA != nullptr && fb.blocksA > 0 && fb.blocksB > 0 &&
+      static_cast<uint64_t>(minA) + minB > static_cast<uint64_t>(fb.cap))
+    Pn = 0;                                         // every tile of the band is general
   *fb.used = Pn;
   if (fb.band >= 0 && fb.band < kModuliRecord) g_moduli_record[fb.band] = Pn;
 }
@@ -1168,20 +1191,51 @@ __device__ __forceinline__ unsigned long long max_of_rows(const unsigned long lo
   return m[0];
 }
 
+// Smallest, over the 64-row blocks of `rows` rows, of the block's largest
+// deep count (one warp per block in turn; the warp's lanes hold the result).
+__device__ __forceinline__ unsigned min_block_max(const int* count, int64_t rows) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  unsigned mn = ~0u;
+  for (int64_t blk = warp; blk * kTile < rows; blk += kModuliThreads / 32) {
+    int mx = 0;
+#pragma unroll
+    for (int h = 0; h < kTile / 32; ++h) {
+      const int64_t i = blk * kTile + lane + 32 * h;
+      if (i < rows) mx = max(mx, __ldcg(count + i));
+    }
+    mn = min(mn, static_cast<unsigned>(__reduce_max_sync(0xFFFFFFFFu, mx)));
+  }
+  return mn;
+}
+
 __global__ void __launch_bounds__(kModuliThreads) moduli_kernel(
     const unsigned long long* normA, int64_t rowsA, const unsigned long long* normB, int64_t rowsB,
-    int least, int most, int* used, int band, unsigned long long* maxima, ModuliThresholds thr) {
+    int least, int most, int* used, int band, unsigned long long* maxima, ModuliThresholds thr,
+    const int* countA, const int* countB, int cap) {
   const unsigned long long a_w = max_of_rows(normA, rowsA);
   const unsigned long long b_w = max_of_rows(normB, rowsB);
+  unsigned mnA = ~0u, mnB = ~0u;
+  if (countA != nullptr) {
+    mnA = min_block_max(countA, rowsA);
+    mnB = min_block_max(countB, rowsB);
+  }
   if ((threadIdx.x & 31) == 0) {
     atomicMax(maxima, a_w);
     atomicMax(maxima + 1, b_w);
+    // minima through atomicMax of the complements on the zeroed slots 2, 3
+    atomicMax(maxima + 2, static_cast<unsigned long long>(~mnA));
+    atomicMax(maxima + 3, static_cast<unsigned long long>(~mnB));
   }
   __syncthreads();
   if (threadIdx.x != 0) return;
   const unsigned long long a = atomicAdd(maxima, 0ull);        // read at L2, after every warp
   const unsigned long long b = atomicAdd(maxima + 1, 0ull);
-  const int P = choose_moduli(a, b, least, most, thr);
+  int P = choose_moduli(a, b, least, most, thr);
+  if (countA != nullptr && rowsA > 0 && rowsB > 0) {
+    const unsigned minA = ~static_cast<unsigned>(atomicAdd(maxima + 2, 0ull));
+    const unsigned minB = ~static_cast<unsigned>(atomicAdd(maxima + 3, 0ull));
+    if (static_cast<uint64_t>(minA) + minB > static_cast<uint64_t>(cap)) P = 0;
+  }
   *used = P;
   if (band >= 0 && band < kModuliRecord) g_moduli_record[band] = P;
 }
@@ -1191,9 +1245,10 @@ __global__ void __launch_bounds__(kModuliThreads) moduli_kernel(
 cudaError_t launch_moduli(const unsigned long long* normA, int64_t rowsA,
                           const unsigned long long* normB, int64_t rowsB, int bf16, int least,
                           int most, int* used, int band, unsigned long long* maxima,
-                          cudaStream_t stream) {
+                          const int* countA, const int* countB, int cap, cudaStream_t stream) {
   moduli_kernel<<<1, kModuliThreads, 0, stream>>>(normA, rowsA, normB, rowsB, least, most, used,
-                                                  band, maxima, moduli_thresholds(bf16));
+                                                  band, maxima, moduli_thresholds(bf16), countA,
+                                                  countB, cap);
   note_launch();
   return cudaGetLastError();
 }

@@ -25,7 +25,9 @@ std::mutex g_mu;
 std::vector<Record> g_records;
 
 const char* const kStageNames[kNumStages] = {"prepass", "residue_planes", "residue_gemm",
-                                             "reconstruct", "general_kulisch", "band"};
+                                             "reconstruct", "general_kulisch", "band",
+                                             "wide_stats", "wide_planes", "wide_gemm",
+                                             "wide_reconstruct"};
 
 }  // namespace
 

@@ -168,6 +168,26 @@ det_status det_pipe_benchmark(int kind, int64_t iters, int64_t blocks, void* out
 int det_pipe_benchmark_ops_per_thread_iter(void);
 int det_pipe_benchmark_threads_per_block(void);
 
+/* The wide residue path (see det_tile_routes) on (enable != 0, the default)
+ * or off for the following calls from any thread; returns the previous
+ * setting.  Results are identical either way (every path computes the same
+ * exact sum); with the path off, tiles the narrow residue path leaves go to
+ * the general kernel on the CUDA cores, and a call enqueues about eight fewer
+ * kernels, which callers whose data is known to span few binades may prefer. */
+int det_set_wide_path(int enable);
+
+/* Diagnostic for tests and benchmarks: how the most recent residue-path
+ * det_gemm / det_gemm_partial call on the current device routed its 64x64
+ * output tiles.  out[0] = all tiles, out[1] = tiles the narrow residue path
+ * left ("general": more elements more than 18 binades below their row's
+ * largest than its lists take), out[2] = of those, tiles the wide residue
+ * path computed (every row of A and of B in the tile finite and spanning at
+ * most 88 binades for f32, 124 for bf16), out[3] = tiles left for the general
+ * Kulisch kernel.  Returns 0, or -1 (null out, CUDA error).  Reads device
+ * memory, so it synchronises with the device; calls that take the band path
+ * (K = 0, very large grids) do not update it. */
+int det_tile_routes(int64_t* out);
+
 /* Worst-case number of moduli (bf16 tensor-core GEMMs) of det_gemm's residue
  * path for this dtype and K: enough that their product exceeds twice the
  * largest possible |sum of shallow products|.  The residue planes are written

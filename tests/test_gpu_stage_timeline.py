@@ -19,7 +19,8 @@ from gpu_util import bits_of, dev_f32
 
 pytestmark = pytest.mark.gpu
 
-STAGES = {"prepass", "residue_planes", "residue_gemm", "reconstruct", "general_kulisch", "band"}
+STAGES = {"prepass", "residue_planes", "residue_gemm", "reconstruct", "general_kulisch", "band",
+          "wide_stats", "wide_planes", "wide_gemm", "wide_reconstruct"}
 
 
 def test_timeline_of_a_banded_call():

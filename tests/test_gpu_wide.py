@@ -1,0 +1,119 @@
+"""The wide residue path against the oracle, bit for bit.
+
+Tiles whose operand rows span more binades than the narrow residue path's
+18-binade grid (and its deep lists) covers go to the wide path: every row on
+its own integer grid from its smallest element, up to 40 moduli, the same
+tensor-core GEMM, a multi-limb CRT.  These tests draw such data (log-uniform
+magnitudes, bf16 with exponents over +-60, subnormals, zero rows, both operand
+layouts), compare every output and every digit with the oracle, and check
+through det_tile_routes that the wide path (not the general kernel) computed
+the tiles -- or, for rows it must not take (Inf/NaN, a spread beyond its
+window), that those tiles went to the general kernel.
+"""
+import numpy as np
+import pytest
+import torch
+
+import exact_sum_gemm_gb300 as dg
+from exact_sum_gemm_gb300 import _native
+from exact_sum_gemm_gb300 import workloads as wl
+from gpu_util import assert_bits_equal, bits_of, dev_bf16, dev_f32, np_bits
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(oracle_mod, A, B, dtype="f32", layouts=("NN",)):
+    to_dev = dev_f32 if dtype == "f32" else dev_bf16
+    want = np_bits(oracle_mod.gemm(A, B, dtype=dtype))
+    want_digits = oracle_mod.gemm_digits(A, B, dtype=dtype)
+    routes = []
+    for tag in layouts:
+        a = to_dev(A) if tag[0] == "N" else to_dev(np.ascontiguousarray(A.T)).t()
+        b = to_dev(B) if tag[1] == "N" else to_dev(np.ascontiguousarray(B.T)).t()
+        assert_bits_equal(bits_of(dg.det_gemm(a, b)), want, f"{dtype} {tag} det_gemm")
+        routes.append(_native.tile_routes())
+        np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), want_digits,
+                                      err_msg=f"{dtype} {tag} digits")
+        routes.append(_native.tile_routes())
+    return routes
+
+
+def _all_wide(routes):
+    for r in routes:
+        assert r["general"] == r["tiles"] and r["wide"] == r["tiles"] and r["kulisch"] == 0, r
+
+
+@pytest.mark.parametrize("M,N,K", [(300, 260, 777), (129, 257, 64), (64, 64, 4096), (1, 70, 33)])
+def test_wide_f32_loguniform(oracle_mod, M, N, K):
+    A = wl.loguniform_f32((M, K), 71, 0, lo=-40, hi=40)
+    B = wl.loguniform_f32((N, K), 71, 1, lo=-40, hi=40)
+    _all_wide(_check(oracle_mod, A, B, layouts=("NN", "TT", "NT")))
+
+
+def test_wide_bf16_exponents_60_with_cancellation(oracle_mod):
+    A, B, _ = wl.bf16_wide_with_cancellation(200, 130, 1000, seed=72)
+    _all_wide(_check(oracle_mod, A, B, dtype="bf16", layouts=("NN", "TN")))
+
+
+def test_wide_subnormals_and_zero_rows(oracle_mod):
+    # magnitudes 2^U[-149, -80]: a third of them subnormal; a zero row and a
+    # zero column
+    A = wl.loguniform_f32((150, 300), 73, 0, lo=-149, hi=-80)
+    B = wl.loguniform_f32((140, 300), 73, 1, lo=-149, hi=-80)
+    A[7] = 0.0
+    B[:, 11] = 0.0
+    B[100] = 0.0
+    routes = _check(oracle_mod, A, B)
+    for r in routes:
+        assert r["kulisch"] == 0 and r["wide"] > 0, r
+
+
+def test_rows_the_wide_path_must_not_take(oracle_mod):
+    # one row of A holds a NaN, one row of B spans 100 binades: their tiles go
+    # to the general kernel, every other tile to the wide path
+    A = wl.loguniform_f32((200, 500), 74, 0, lo=-30, hi=30)
+    B = wl.loguniform_f32((190, 500), 74, 1, lo=-30, hi=30)
+    A[70, 5] = np.nan
+    B[150, 9] = np.float32(2.0 ** 60)
+    B[150, 10] = np.float32(2.0 ** -40)
+    routes = _check(oracle_mod, A, B)
+    for r in routes:
+        assert r["wide"] > 0 and r["kulisch"] > 0 and r["wide"] + r["kulisch"] == r["general"], r
+
+
+def test_wide_headline_shape_sampled_rows(oracle_mod):
+    A = wl.loguniform_f32((4096, 4096), 0, 0, lo=-40, hi=40)
+    B = wl.loguniform_f32((4096, 4096), 0, 1, lo=-40, hi=40)
+    got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
+    _all_wide([_native.tile_routes()])
+    rows = np.array(sorted({0, 1, 127, 128, 255, 256, 2047, 2048, 2815, 2816, 4094, 4095} |
+                           set(wl.rng(75, 0).integers(0, 4096, size=52).tolist())))
+    assert_bits_equal(got[rows], np_bits(oracle_mod.gemm(A[rows], B)), "wide 4096^3 rows")
+
+
+def test_narrow_data_takes_no_wide_tile():
+    a = dev_f32(wl.normal_f32((512, 1024), 76, 0))
+    b = dev_f32(wl.normal_f32((384, 1024), 76, 1))
+    dg.det_gemm(a, b)
+    r = _native.tile_routes()
+    assert r["general"] == 0 and r["wide"] == 0 and r["kulisch"] == 0, r
+
+
+def test_wide_path_switch_gives_identical_results(oracle_mod):
+    # det_set_wide_path(0) sends the same tiles to the general kernel: the
+    # results are the same exact sums, bit for bit
+    A = wl.loguniform_f32((200, 300), 77, 0, lo=-40, hi=40)
+    B = wl.loguniform_f32((150, 300), 77, 1, lo=-40, hi=40)
+    a, b = dev_f32(A), dev_f32(B)
+    lib = dg.library()
+    on = bits_of(dg.det_gemm(a, b))
+    _all_wide([_native.tile_routes()])
+    assert lib.det_set_wide_path(0) == 1
+    try:
+        off = bits_of(dg.det_gemm(a, b))
+        off_digits = dg.det_gemm_partial(a, b).cpu().numpy()
+    finally:
+        assert lib.det_set_wide_path(1) == 0
+    assert np.array_equal(on, off)
+    assert_bits_equal(off, np_bits(oracle_mod.gemm(A, B)), "wide path off")
+    np.testing.assert_array_equal(off_digits, oracle_mod.gemm_digits(A, B))
