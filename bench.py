@@ -55,8 +55,10 @@ def parse_args():
     p.add_argument("--steps", type=int, default=10)
     p.add_argument("--warmup", type=int, default=3)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", choices=["normal", "wide"], default="normal",
-                   help="normal: N(0,1) (the headline); wide: |x| = 2^U[-40,40]")
+    p.add_argument("--workload", choices=["normal", "wide", "loguniform100"], default="normal",
+                   help="normal: N(0,1) (the headline); wide: |x| = 2^U[-40,40]; "
+                        "loguniform100: |x| = 2^U[-100,100] (beyond the wide path's window: "
+                        "the general kernel; with --mnk, for profiling)")
     p.add_argument("--cpu-rows", type=int, default=512,
                    help="rows of the 4096^3 problem the CPU baseline samples")
     p.add_argument("--no-extras", action="store_true",
@@ -97,13 +99,15 @@ def make_inputs(seed, workload):
     from exact_sum_gemm_gb300 import workloads as wl
     if workload == "normal":
         return wl.normal_f32((M, K), seed, 0), wl.normal_f32((N, K), seed, 1)
-    return (wl.loguniform_f32((M, K), seed, 0, lo=-40, hi=40),
-            wl.loguniform_f32((N, K), seed, 1, lo=-40, hi=40))
+    span = 40 if workload == "wide" else 100
+    return (wl.loguniform_f32((M, K), seed, 0, lo=-span, hi=span),
+            wl.loguniform_f32((N, K), seed, 1, lo=-span, hi=span))
 
 
 def workload_config(workload, extra=None):
-    cfg = {"workload": f"det_gemm f32 M=N=K=4096, A,B "
-                       f"{'iid N(0,1)' if workload == 'normal' else '|x|=2^U[-40,40]'}, seed 0",
+    dist = {"normal": "iid N(0,1)", "wide": "|x|=2^U[-40,40]",
+            "loguniform100": "|x|=2^U[-100,100]"}[workload]
+    cfg = {"workload": f"det_gemm f32 M={M} N={N} K={K}, A,B {dist}, seed 0",
            "M": M, "N": N, "K": K, "dtype_in": "f32", "dtype_out": "f32",
            "l2": "flushed: 256 MiB write between steps (outside the per-step events)",
            "inputs": "resident in HBM (e2e: copied from pinned host memory every step)"}

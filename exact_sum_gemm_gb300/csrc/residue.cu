@@ -979,6 +979,7 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
 // band's count (ReconArgs::used).
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
+  if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P,
                              [&](auto Q) { reconstruct_fast_body<kBf16, decltype(Q)::value>(g, ra); });
 }
@@ -1042,6 +1043,7 @@ __device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const R
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
     GemmArgs g, ReconArgs ra, const int* rows, const int* cols, const int* nrc) {
+  if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
     reconstruct_deep_body<kBf16, decltype(Q)::value>(g, ra, rows, cols, nrc);
   });
@@ -1093,6 +1095,7 @@ __device__ __forceinline__ void partial_fast_body(const GemmArgs& g, const Recon
 
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, ReconArgs ra) {
+  if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P,
                              [&](auto Q) { partial_fast_body<kBf16, decltype(Q)::value>(g, ra); });
 }

@@ -593,6 +593,61 @@ __device__ __forceinline__ void place_digits(const uint32_t (&x)[L], int E, uint
   top = static_cast<int64_t>(static_cast<int32_t>(d17));
 }
 
+// RNE_f32(S 2^E) from S's limbs: the leading 64 bits of |S|, with every bit
+// below them ORed into bit 0 (a sticky bit far below the rounding position),
+// round to binary32 exactly as |S| does; the scaling by a power of two is an
+// exponent add.  Returns false (the caller takes the digit route) where the
+// result is subnormal, zero or infinite.
+template <int L>
+__device__ __forceinline__ bool round_limbs_fast(const uint32_t (&x)[L], int E, uint32_t& bits) {
+  const bool neg = static_cast<int32_t>(x[L - 1]) < 0;
+  uint32_t a[L];
+  uint32_t carry = neg ? 1u : 0u;
+#pragma unroll
+  for (int l = 0; l < L; ++l) {                   // |S| (two's complement negation if negative)
+    const uint32_t v = neg ? ~x[l] : x[l];
+    a[l] = v + carry;
+    carry = (carry != 0u && a[l] == 0u) ? 1u : 0u;
+  }
+  int top = -1;
+#pragma unroll
+  for (int l = 0; l < L; ++l) top = a[l] != 0u ? l : top;
+  if (top < 0) {                                  // exact zero -> +0
+    bits = 0u;
+    return true;
+  }
+  // the three words from the leading one down, and the OR of the rest
+  uint32_t w2 = 0, w1 = 0, w0 = 0, rest = 0;
+#pragma unroll
+  for (int l = 0; l < L; ++l) {
+    if (l == top) w2 = a[l];
+    if (l == top - 1) w1 = a[l];
+    if (l == top - 2) w0 = a[l];
+    if (l < top - 2) rest |= a[l];
+  }
+  const int lz = __clz(w2);                       // 0 .. 31
+  const uint64_t hi64 = (static_cast<uint64_t>(w2) << 32) | w1;
+  uint64_t t = lz ? (hi64 << lz) | (w0 >> (32 - lz)) : hi64;
+  const uint32_t below = lz ? (w0 << lz) : w0;
+  t |= (below | rest) != 0u ? 1u : 0u;
+  const uint32_t f = f32_bits_of_top(t);          // |S| 2^-(32 top + 32 - lz - 64), rounded
+  const int shift = E + 32 * top + 32 - lz - 64;
+  const int ef = static_cast<int>(f >> 23) + shift;   // biased exponent of the result
+  if (ef < 1 || ef > 254) return false;
+  bits = (neg ? 0x80000000u : 0u) | (f + (static_cast<uint32_t>(shift) << 23));
+  return true;
+}
+
+// The digit route of one output: rare for det_gemm (subnormal, zero or
+// infinite results), kept out of line so the main loop keeps its registers.
+template <int L>
+__device__ __noinline__ uint32_t round_limbs_exact(const uint32_t (&x)[L], int E) {
+  uint32_t w[kDigits - 1];
+  int64_t top;
+  place_digits<L>(x, E, w, top);
+  return round_to_f32_bits(w, top);
+}
+
 template <int L>
 __device__ void wide_recon_body(const GemmArgs& g, const WideRecon& wr, int P,
                                 const int32_t (*C)[12], const int32_t* Wt, const int32_t* negM) {
@@ -630,12 +685,20 @@ __device__ void wide_recon_body(const GemmArgs& g, const WideRecon& wr, int P,
         for (int h = 0; h < 2; ++h)
           r[h] = live[h] ? static_cast<int32_t>(wr.res[q * wr.res_plane + m[h] * g.N + n]) : 0;
         const int32_t wq = Wt[q];
+        int32_t c[12];                              // the limbs, 16 bytes at a time
+#pragma unroll
+        for (int l4 = 0; l4 < (L + 3) / 4; ++l4) {
+          const int4 v = reinterpret_cast<const int4*>(C[q])[l4];
+          c[4 * l4] = v.x;
+          c[4 * l4 + 1] = v.y;
+          c[4 * l4 + 2] = v.z;
+          c[4 * l4 + 3] = v.w;
+        }
 #pragma unroll
         for (int l = 0; l < L; ++l) {
-          const int32_t c = C[q][l];
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[h][l]) : "r"(r[h]), "r"(c));
+            asm("mad.wide.s32 %0, %1, %2, %0;" : "+l"(acc[h][l]) : "r"(r[h]), "r"(c[l]));
         }
 #pragma unroll
         for (int h = 0; h < 2; ++h) Q[h] += r[h] * wq;
@@ -657,19 +720,26 @@ __device__ void wide_recon_body(const GemmArgs& g, const WideRecon& wr, int P,
         }
         const int bA = wr.loA[m[h]] != 0 ? kKeyBias - wr.loA[m[h]] : 0;
         const int E = bA + bB;
+        if (g.P == nullptr) {
+          uint32_t bits;
+          if (failed) {
+            bits = kNanBits;
+          } else if (!round_limbs_fast<L>(x, E, bits)) {   // subnormal, zero or infinite
+            bits = round_limbs_exact<L>(x, E);
+          }
+          reinterpret_cast<uint32_t*>(g.C)[m[h] * g.ldc + n] = bits;
+          continue;
+        }
         uint32_t w[kDigits - 1];
         int64_t top;
         place_digits<L>(x, E, w, top);
-        if (g.P != nullptr) {
+        {
           int64_t* out = g.P + m[h] * g.N + n;
 #pragma unroll
           for (int j = 0; j < kDigits - 1; ++j) out[j * MN] = failed ? 0 : static_cast<int64_t>(w[j]);
           out[(kDigits - 1) * MN] = failed ? 0 : top;
           out[kDigits * MN] = g.K;
           out[(kDigits + 1) * MN] = failed ? 1 : 0;
-        } else {
-          reinterpret_cast<uint32_t*>(g.C)[m[h] * g.ldc + n] =
-              failed ? kNanBits : round_to_f32_bits(w, top);
         }
       }
     }
