@@ -10,6 +10,10 @@ det_gemm), SGD with learning rate 1e-2, seed 7.  Initialisation N(0, 1/fan_in)
 with power-of-two scales.  The pages give no data set or initialisation: these
 are the readings stated in the design notes.
 """
+import hashlib
+import json
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -28,7 +32,20 @@ def _relu(x):
     return torch.clamp_min(x, 0.0)
 
 
-def train(k_shards, steps=STEPS, record_step0=False):
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "mlp_training_oracle.json")
+FULL_STEPS = (0, 1, 79, 159)
+
+
+def digest(t):
+    """SHA-256 (first 32 hex digits) of a tensor's float32 bytes in C order."""
+    a = t.detach().to(torch.float32).contiguous().cpu().numpy()
+    return hashlib.sha256(np.ascontiguousarray(a).tobytes()).hexdigest()[:32]
+
+
+def train(k_shards, steps=STEPS, record_step0=False, record=None):
+    """The 160-step run; with `record` (a dict) it also keeps the digests the
+    oracle's trajectory stores: targets and y every step, all six GEMM
+    outputs at FULL_STEPS, and the final weights."""
     dev = torch.device("cuda")
     w1, w2 = wl.mlp_init(stream=0)
     t1, t2 = wl.mlp_init(stream=1)
@@ -41,12 +58,22 @@ def train(k_shards, steps=STEPS, record_step0=False):
         x = torch.from_numpy(wl.mlp_batch(step)).to(dev)
         with torch.no_grad():
             target = dg.det_gemm(_relu(dg.det_gemm(x, t1d)), t2d)
-        h = _relu(l1(x))
+        h_pre = l1(x)
+        h = _relu(h_pre)
+        if record is not None:
+            h.retain_grad()                 # dgrad of layer 2: the gradient reaching h
         y = l2(h)
         loss = (y - target).square().mean()
         for p in (l1.weight, l2.weight):
             p.grad = None
         loss.backward()
+        if record is not None:
+            record.setdefault("per_step", []).append({"target": digest(target), "y": digest(y)})
+            if step in FULL_STEPS:
+                record.setdefault("full", {})[str(step)] = {
+                    "target": digest(target), "h_pre": digest(h_pre), "y": digest(y),
+                    "dh": digest(h.grad), "dw1": digest(l1.weight.grad),
+                    "dw2": digest(l2.weight.grad)}
         with torch.no_grad():
             for p in (l1.weight, l2.weight):
                 upd = p.grad * lr           # two separate roundings, no fused update
@@ -54,12 +81,27 @@ def train(k_shards, steps=STEPS, record_step0=False):
         losses.append(loss.detach().clone())
         if record_step0 and step == 0:
             step0 = y.detach().clone()
+    if record is not None:
+        record["final"] = {"w1": digest(l1.weight), "w2": digest(l2.weight)}
     return torch.stack(losses), l1.weight.detach().clone(), l2.weight.detach().clone(), step0
 
 
 def test_sharded_training_is_bitwise_identical(oracle_mod):
-    loss_a, w1_a, w2_a, y0 = train(k_shards=1, record_step0=True)
+    rec = {}
+    loss_a, w1_a, w2_a, y0 = train(k_shards=1, record_step0=True, record=rec)
     loss_b, w1_b, w2_b, _ = train(k_shards=4)
+    # every GEMM of every step against the oracle's own 160-step run (digests
+    # written by tests/golden/make_training_golden.py from the oracle alone)
+    with open(GOLDEN) as f:
+        gold = json.load(f)
+    assert gold["steps"] == STEPS
+    for step, (got, want) in enumerate(zip(rec["per_step"], gold["per_step"])):
+        for key in ("target", "y"):
+            assert got[key] == want[key], f"step {step}: {key} differs from the oracle's run"
+    for step, want in gold["full"].items():
+        for key, d in want.items():
+            assert rec["full"][step][key] == d, f"step {step}: {key} differs from the oracle's run"
+    assert rec["final"] == gold["final"], "final weights differ from the oracle's run"
     assert torch.equal(loss_a.view(torch.int32), loss_b.view(torch.int32)), \
         "per-step losses differ between unsharded and 4-way sharded runs"
     assert torch.equal(w1_a.view(torch.int32), w1_b.view(torch.int32))
