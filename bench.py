@@ -66,6 +66,9 @@ def parse_args():
     p.add_argument("--configs", action="store_true",
                    help="time each workload configuration (one JSON line each) instead of "
                         "the headline run")
+    p.add_argument("--op", choices=["gemm", "partial"], default="gemm",
+                   help="the timed call: det_gemm (the headline) or det_gemm_partial into a "
+                        "preallocated digit array (for profiling the digit write-out)")
     p.add_argument("--mnk", type=int, nargs=3, default=None, metavar=("M", "N", "K"),
                    help="override the problem size (profiling of small cases only)")
     args = p.parse_args()
@@ -444,6 +447,11 @@ def run_ours(args):
     c = torch.empty((M, N), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    if args.op == "partial":
+        digits = torch.empty((20, M, N), dtype=torch.int64, device=dev)
+        timed_call = lambda: dg.det_gemm_partial(a, b, out=digits)
+    else:
+        timed_call = lambda: dg.det_gemm(a, b, out=c)
 
     def barrier():
         if dist is not None:
@@ -451,7 +459,7 @@ def run_ours(args):
 
     for _ in range(args.warmup):
         flush.zero_()
-        dg.det_gemm(a, b, out=c)
+        timed_call()
     torch.cuda.synchronize(dev)
 
     props = torch.cuda.get_device_properties(dev)
@@ -473,7 +481,7 @@ def run_ours(args):
     for s in range(args.steps):
         flush.zero_()                  # L2 flush between steps, outside the step's events
         ev[s][0].record(stream)
-        dg.det_gemm(a, b, out=c)
+        timed_call()
         ev[s][1].record(stream)
     end.record(stream)
     torch.cuda.synchronize(dev)
@@ -492,18 +500,18 @@ def run_ours(args):
     lib.det_stage_timing(1)
     for _ in range(stage_calls):
         flush.zero_()
-        dg.det_gemm(a, b, out=c)
+        timed_call()
     torch.cuda.synchronize(dev)
     lib.det_stage_timing(0)
     stages = stage_spans(_native.stage_timeline(), stage_calls)
     flops = 2.0 * M * N * K
     value = flops * world / (ms_per_step * 1e-3) / 1e9
 
-    extras = {}
-    if rank == 0 and not args.no_extras:
+    extras = {"op": "det_gemm_partial"} if args.op == "partial" else {}
+    if rank == 0 and not args.no_extras and args.op == "gemm":
         extras = measure_extras(args, dg, a, b, c, A, B, dev, stream)
     pipes = measure_pipe_peaks(lib, dev, uuid) if rank == 0 and not args.no_extras else None
-    if rank == 0 and not args.no_extras and args.workload == "normal":
+    if rank == 0 and not args.no_extras and args.workload == "normal" and args.op == "gemm":
         del a, b, c
         torch.cuda.empty_cache()
         extras["workloads"] = measure_workloads(args, dev, pipes, with_cpu=True)

@@ -1100,6 +1100,77 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
                              [&](auto Q) { partial_fast_body<kBf16, decltype(Q)::value>(g, ra); });
 }
 
+// The same outputs with the residues staged through shared memory: the
+// block's 256 columns of one row, every modulus, arrive by 16-byte cp.async
+// copies (one per 16 columns and modulus, 0.06 per output instead of one byte
+// load per output and modulus), double-buffered so that the next row's
+// copies are in flight while this row is rebuilt.  Needs N to be a multiple
+// of 16 (every copy 16-byte aligned); 7 KB of shared memory.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_one() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+template <int kBf16, int P>
+__device__ __forceinline__ void partial_staged_body(const GemmArgs& g, const ReconArgs& ra,
+                                                    int8_t (*buf)[kNumModuli][kThreads]) {
+  const int64_t MN = g.M * g.N;
+  const int64_t tiles_n = (g.N + kTile - 1) / kTile;
+  const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
+  const int64_t n0 = int64_t(blockIdx.x) * kThreads;
+  const int64_t n = n0 + threadIdx.x;
+  bool col_live = n < g.N && ra.countB[n] == 0;                 // deep column: deep kernel
+  int colE = 0;
+  if (col_live) {
+    int emB = ra.emaxB[n];
+    emB = emB == kEmaxEmpty ? 0 : emB;
+    colE = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+  }
+  const int t = threadIdx.x, cu = t >> 4, cc = (t & 15) * 16;
+  const bool copier = cu < P && n0 + cc < g.N;
+  auto issue = [&](int64_t m, int slot) {
+    if (copier) cp_async16(&buf[slot][cu][cc], ra.res + cu * MN + m * g.N + n0 + cc);
+    cp_async_commit();                            // every thread: one group per row
+  };
+  const int64_t step = gridDim.y;
+  int64_t m = ra.m_begin + blockIdx.y;
+  if (m >= ra.m_end) return;
+  issue(m, 0);
+  for (int slot = 0; m < ra.m_end; m += step, slot ^= 1) {
+    if (m + step < ra.m_end) issue(m + step, slot ^ 1);
+    else cp_async_commit();                       // an empty group keeps the count uniform
+    cp_async_wait_one();                          // this row's copies have landed
+    __syncthreads();
+    if (col_live && !ra.route[(m / kTile) * tiles_n + n / kTile] && ra.countA[m] == 0) {
+      int emA = ra.emaxA[m];
+      emA = emA == kEmaxEmpty ? 0 : emA;
+      int32_t r[kNumModuli];
+#pragma unroll
+      for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(buf[slot][i][t]) : 0;
+      uint64_t slo, shi;
+      crt_s128<P>(r, slo, shi);
+      const DigitWindow d = digit_window(slo, shi, emA + colE);
+      write_window(g.P + m * g.N + n, MN, d, g.K, nf);
+    }
+    __syncthreads();                              // the slot is free for the row after next
+  }
+}
+
+template <int kBf16, int P>
+__global__ void __launch_bounds__(kThreads, 4) partial_staged_kernel(GemmArgs g, ReconArgs ra) {
+  if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
+  __shared__ __align__(16) int8_t buf[2][kNumModuli][kThreads];
+  with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
+    partial_staged_body<kBf16, decltype(Q)::value>(g, ra, buf);
+  });
+}
+
 // Moduli counts with compiled kernels: f32 operands need 12 to 14 moduli
 // (K from 1 to 2^19), bf16 operands 8 to 10.  A call uses the smallest
 // compiled count that covers its bound (more moduli never change the result).
@@ -1354,8 +1425,23 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
     // 512 blocks per column of blocks beat one row per block by 3 %)
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
                static_cast<unsigned>(band < 512 ? band : 512));
+    // staged copies where every row of residues starts 16-byte aligned
+    const bool staged = (g.N % 16) == 0 && (reinterpret_cast<uintptr_t>(ra.res) % 16) == 0;
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
-      partial_fast_kernel<decltype(B)::value, decltype(P)::value><<<pgrid, kThreads, 0, stream>>>(g, ra);
+      constexpr int kB = decltype(B)::value, kP = decltype(P)::value;
+      if (staged) {
+        static PerDeviceOnce carveout;            // room beside a running tensor-core CTA
+        carveout.run([](int) {
+          cudaFuncSetAttribute(partial_staged_kernel<kB, kP>,
+                               cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
+          cudaGetLastError();
+          return cudaSuccess;
+        });
+        partial_staged_kernel<kB, kP><<<pgrid, kThreads, 0, stream>>>(g, ra);
+      } else {
+        partial_fast_kernel<kB, kP><<<pgrid, kThreads, 0, stream>>>(g, ra);
+      }
       return cudaSuccess;
     });
   } else {
