@@ -197,13 +197,22 @@ cudaError_t launch_residues(const ResidueOperand& o, int bf16, int nplanes, cuda
 cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1, int bf16, int nplanes,
                              cudaStream_t stream);
 // The outputs of a band whose row of A and column of B hold no deep element.
+// For det_gemm_partial (g.P set) the launch may write whole row segments of
+// digit planes, placeholder zeros in the deep columns included: the band's
+// deep kernel must then run after it (it does not touch deep rows or the
+// general tiles).
 cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream);
-// The band's other outputs (independent of the fast kernel: both may run at
-// once).  deep_lists: the rows of A then the columns of C that hold deep
+// The band's other outputs: those of its deep rows (kDeepRows) and of its
+// deep columns outside deep rows (kDeepCols).  For det_gemm both kernels may
+// run at once; for det_gemm_partial the deep-column part follows the fast
+// kernel.  deep_lists: the rows of A then the columns of C that hold deep
 // elements (M + N ints), with their two counts in deep_counters, as the
-// routing step lists them.
+// routing step lists them.  blocks_per_sm: 1, or 2 where nothing else is
+// meant to run beside it.
+constexpr int kDeepRows = 1, kDeepCols = 2;
 cudaError_t launch_reconstruct_deep(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
-                                    int* deep_counters, cudaStream_t stream);
+                                    int* deep_counters, int parts, int blocks_per_sm,
+                                    cudaStream_t stream);
 
 struct ResGemmArgs {
   const __nv_bfloat16* A;     // [M/32][Kp/64][nplanes][32][64] (ResidueOperand::planes)

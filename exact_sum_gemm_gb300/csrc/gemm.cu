@@ -488,7 +488,21 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // caller's stream after it) and band b's GEMM.  Its deep outputs go to the
   // side stream; its other outputs to the caller's stream for band 0 and to
   // fast2 for later bands, so that the last band's starts when its GEMM ends
-  // even while band 0's is still running.
+  // even while band 0's is still running.  For det_gemm_partial the fast
+  // kernel writes whole row segments (placeholders in the deep columns), so
+  // the deep kernel's deep-column part follows it (its deep-row part, which
+  // the fast kernel leaves alone, runs beside it).
+  const bool cols_after = g.P != nullptr;
+  auto recon_args = [&](int b) {
+    return ReconArgs{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB,
+                     cap, error, edge[b], edge[b + 1], used + b};
+  };
+  auto deep = [&](int b, int parts, int blocks_per_sm) {
+    // deep-row/column lists, and their two counters right after the error flag
+    StageScope t(kStageReconstruct, bs->side);
+    return launch_reconstruct_deep(g, recon_args(b), deep_rows, error + 1, parts, blocks_per_sm,
+                                   bs->side);
+  };
   int forked = 0, fast_forked = 0;
   for (int b = 0; b < nb && e == cudaSuccess; ++b) {
     e = cudaStreamWaitEvent(bs->side, bs->gen_fork, 0);
@@ -498,23 +512,23 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     if (e == cudaSuccess) e = cudaStreamWaitEvent(fs, bs->gemm_done[b], 0);
     if (e != cudaSuccess) break;
     forked = b + 1;
-    const int64_t m0 = edge[b], m1 = edge[b + 1];
-    ReconArgs rc{res, nplanes, s.emaxA, s.emaxB, s.route, counts, listA, counts + g.M, listB, cap,
-                 error, m0, m1, used + b};
-    {
-      // deep-row/column lists, and their two counters right after the error flag
-      StageScope t(kStageReconstruct, bs->side);
-      e = launch_reconstruct_deep(g, rc, deep_rows, error + 1, bs->side);
-    }
-    if (e == cudaSuccess) e = cudaEventRecord(bs->deep_done[b], bs->side);
+    e = deep(b, cols_after ? kDeepRows : kDeepRows | kDeepCols, 1);
+    if (e == cudaSuccess && !cols_after) e = cudaEventRecord(bs->deep_done[b], bs->side);
     if (e == cudaSuccess) {
       StageScope t(kStageReconstruct, fs);
-      e = launch_reconstruct_fast(g, rc, fs);
+      e = launch_reconstruct_fast(g, recon_args(b), fs);
     }
-    if (e == cudaSuccess && b > 0) {
+    if (e == cudaSuccess && (b > 0 || cols_after)) {
       e = cudaEventRecord(bs->fast_done[b], fs);
-      if (e == cudaSuccess) fast_forked = b + 1;
+      if (e == cudaSuccess && b > 0) fast_forked = b + 1;
     }
+  }
+  // det_gemm_partial: every band's deep-row part is enqueued ahead of the
+  // deep-column parts, which wait for their band's fast kernel
+  for (int b = 0; cols_after && b < forked && e == cudaSuccess; ++b) {
+    e = cudaStreamWaitEvent(bs->side, bs->fast_done[b], 0);
+    if (e == cudaSuccess) e = deep(b, kDeepCols, 2);
+    if (e == cudaSuccess) e = cudaEventRecord(bs->deep_done[b], bs->side);
   }
   for (int b = 0; b < forked && e == cudaSuccess; ++b) e = cudaStreamWaitEvent(stream, bs->deep_done[b], 0);
   for (int b = 1; b < fast_forked && e == cudaSuccess; ++b)

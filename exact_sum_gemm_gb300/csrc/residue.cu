@@ -35,6 +35,7 @@
 #include "det_gemm_internal.cuh"
 #include "det_kernels.h"
 #include "det_residue.cuh"
+#include "tc_ptx.cuh"
 
 #include <atomic>
 #include <type_traits>
@@ -631,10 +632,17 @@ __device__ __forceinline__ uint32_t window_word(const DigitWindow& d) {
 
 // One output's 20 planes; the window's start J0 is a compile-time constant, so
 // every plane is one store of a known word.
+// Digit planes are written once and read only by a later call: streaming
+// stores, so that they do not evict what a running tensor-core GEMM shares
+// through L2.
+__device__ __forceinline__ void put_digit(int64_t* p, int64_t v) {
+  __stcs(reinterpret_cast<long long*>(p), static_cast<long long>(v));
+}
+
 template <int J0, int j>
 __device__ __forceinline__ void write_window_planes(int64_t* out, int64_t MN, const DigitWindow& d) {
   if constexpr (j < kDigits) {
-    out[j * MN] = digit_of(window_word<J0, j>(d), j);
+    put_digit(out + j * MN, digit_of(window_word<J0, j>(d), j));
     write_window_planes<J0, j + 1>(out, MN, d);
   }
 }
@@ -643,8 +651,8 @@ template <int J0>
 __device__ __forceinline__ void write_window_at(int64_t* out, int64_t MN, const DigitWindow& d, int64_t K,
                                                 int64_t nf) {
   write_window_planes<J0, 0>(out, MN, d);
-  out[kDigits * MN] = K;
-  out[(kDigits + 1) * MN] = nf;
+  put_digit(out + kDigits * MN, K);
+  put_digit(out + (kDigits + 1) * MN, nf);
 }
 
 // The same for any start, in the general form (words selected at run time).
@@ -656,10 +664,10 @@ __device__ __forceinline__ void write_window_any(int64_t* out, int64_t MN, const
     const uint32_t w = k < 0 ? 0u
                      : k == 0 ? d.x[0] : k == 1 ? d.x[1] : k == 2 ? d.x[2] : k == 3 ? d.x[3]
                      : k == 4 ? d.x[4] : d.sx;
-    out[j * MN] = digit_of(w, j);
+    put_digit(out + j * MN, digit_of(w, j));
   }
-  out[kDigits * MN] = K;
-  out[(kDigits + 1) * MN] = nf;
+  put_digit(out + kDigits * MN, K);
+  put_digit(out + (kDigits + 1) * MN, nf);
 }
 
 // Dispatch on the window's start.  For finite operands it is at most 14
@@ -991,11 +999,12 @@ __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs 
 template <int kBf16, int P>
 __device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const ReconArgs& ra,
                                                       const int* rows, const int* cols,
-                                                      const int* nrc) {
+                                                      const int* nrc, int parts) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
   const bool failed = ra.error != nullptr && *ra.error != 0;
-  const int64_t n_rows = nrc[0], n_cols = nrc[1];
+  const int64_t n_rows = (parts & kDeepRows) ? nrc[0] : 0;
+  const int64_t n_cols = (parts & kDeepCols) ? nrc[1] : 0;
   const int64_t band = ra.m_end - ra.m_begin;
   const int64_t part1 = n_rows * g.N, total = part1 + band * n_cols;
   for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
@@ -1042,10 +1051,10 @@ __device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const R
 
 template <int kBf16, int P>
 __global__ void __launch_bounds__(kThreads, 1) reconstruct_deep_kernel(
-    GemmArgs g, ReconArgs ra, const int* rows, const int* cols, const int* nrc) {
+    GemmArgs g, ReconArgs ra, const int* rows, const int* cols, const int* nrc, int parts) {
   if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
-    reconstruct_deep_body<kBf16, decltype(Q)::value>(g, ra, rows, cols, nrc);
+    reconstruct_deep_body<kBf16, decltype(Q)::value>(g, ra, rows, cols, nrc, parts);
   });
 }
 
@@ -1100,74 +1109,183 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
                              [&](auto Q) { partial_fast_body<kBf16, decltype(Q)::value>(g, ra); });
 }
 
-// The same outputs with the residues staged through shared memory: the
-// block's 256 columns of one row, every modulus, arrive by 16-byte cp.async
-// copies (one per 16 columns and modulus, 0.06 per output instead of one byte
-// load per output and modulus), double-buffered so that the next row's
-// copies are in flight while this row is rebuilt.  Needs N to be a multiple
-// of 16 (every copy 16-byte aligned); 7 KB of shared memory.
+// The same outputs written by bulk copies.  A block owns 128 columns of a
+// contiguous chunk of the band's rows.  The rows' residues, every modulus,
+// arrive by 16-byte cp.async copies into a ring of kRing row buffers,
+// kRing - 1 rows ahead (one thread of the block also copies the row's deep
+// count and exponent maximum); each thread rebuilds its output's 20 digit
+// words into shared memory, and 20 threads send the row segment's 20 planes
+// (1 KB each) to global memory as bulk copies, double-buffered so that the
+// next row is rebuilt while they drain.  The SMs issue 0.16 store
+// instructions per output instead of 20.
+//
+// A bulk copy writes the whole segment, so deep columns get placeholder
+// zeros: the band's deep kernel, ordered after this one, writes them.  Deep
+// rows are skipped whole (the deep kernel's), and a row segment that touches
+// a general tile (the general or wide kernel's outputs) is written output by
+// output instead.  Needs N a multiple of 16 and 16-byte aligned residues and
+// digit planes (every copy 16-byte aligned, every size a multiple of 128
+// bytes); 45 KB of shared memory, four blocks per SM.
+constexpr int kRing = 3;
+constexpr int kBulkCols = 128;
+constexpr int kPlanesOut = kDigits + 2;
+
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
                    static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
                "l"(gmem)
                : "memory");
 }
+__device__ __forceinline__ void cp_async4(void* smem, const void* gmem) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                   static_cast<uint32_t>(__cvta_generic_to_shared(smem))),
+               "l"(gmem)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_one() {
-  asm volatile("cp.async.wait_group 1;" ::: "memory");
+template <int kPending>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(kPending) : "memory");
 }
 
+// One output's 20 plane words into column t of a shared segment buffer.
+template <int J0, int j>
+__device__ __forceinline__ void window_to_smem(int64_t (*seg)[kBulkCols], int t, const DigitWindow& d) {
+  if constexpr (j < kDigits) {
+    seg[j][t] = digit_of(window_word<J0, j>(d), j);
+    window_to_smem<J0, j + 1>(seg, t, d);
+  }
+}
+__device__ __forceinline__ void window_to_smem_any(int64_t (*seg)[kBulkCols], int t, const DigitWindow& d) {
+#pragma unroll
+  for (int j = 0; j < kDigits; ++j) {
+    const int k = j - d.j0;
+    const uint32_t w = k < 0 ? 0u
+                     : k == 0 ? d.x[0] : k == 1 ? d.x[1] : k == 2 ? d.x[2] : k == 3 ? d.x[3]
+                     : k == 4 ? d.x[4] : d.sx;
+    seg[j][t] = digit_of(w, j);
+  }
+}
+__device__ __forceinline__ void window_to_smem_at(int64_t (*seg)[kBulkCols], int t, const DigitWindow& d) {
+  switch (d.j0) {
+#define DET_SEG_CASE(J) \
+  case J: window_to_smem<J, 0>(seg, t, d); break;
+    DET_SEG_CASE(0) DET_SEG_CASE(1) DET_SEG_CASE(2) DET_SEG_CASE(3) DET_SEG_CASE(4)
+    DET_SEG_CASE(5) DET_SEG_CASE(6) DET_SEG_CASE(7) DET_SEG_CASE(8) DET_SEG_CASE(9)
+    DET_SEG_CASE(10) DET_SEG_CASE(11) DET_SEG_CASE(12) DET_SEG_CASE(13) DET_SEG_CASE(14)
+#undef DET_SEG_CASE
+    default: window_to_smem_any(seg, t, d);
+  }
+}
+
+struct BulkSmem {
+  int64_t seg[2][kPlanesOut][kBulkCols];      // 40 KB: two row segments of digit planes
+  int8_t res[kRing][kNumModuli][kBulkCols];   // 5.25 KB: residue rows
+  int meta[kRing][2];                         // deep count, exponent maximum of the row
+};
+
 template <int kBf16, int P>
-__device__ __forceinline__ void partial_staged_body(const GemmArgs& g, const ReconArgs& ra,
-                                                    int8_t (*buf)[kNumModuli][kThreads]) {
+__device__ __forceinline__ void partial_bulk_body(const GemmArgs& g, const ReconArgs& ra, BulkSmem& sm) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
+  const int64_t band = ra.m_end - ra.m_begin;
+  const int64_t chunk = (band + gridDim.y - 1) / gridDim.y;
+  const int64_t r0 = ra.m_begin + int64_t(blockIdx.y) * chunk;
+  const int64_t r1 = r0 + chunk < ra.m_end ? r0 + chunk : ra.m_end;
+  if (r0 >= r1) return;                                         // the same for the whole block
   const int64_t nf = ra.error != nullptr && *ra.error != 0 ? 1 : 0;   // tensor-core kernel gave up
-  const int64_t n0 = int64_t(blockIdx.x) * kThreads;
-  const int64_t n = n0 + threadIdx.x;
-  bool col_live = n < g.N && ra.countB[n] == 0;                 // deep column: deep kernel
+  const int t = threadIdx.x;
+  const int64_t n0 = int64_t(blockIdx.x) * kBulkCols;
+  const int64_t n = n0 + t;
+  const int ncols = g.N - n0 < kBulkCols ? static_cast<int>(g.N - n0) : kBulkCols;
+  const bool in_range = t < ncols;
+  const bool col_live = in_range && ra.countB[n] == 0;          // deep column: deep kernel
   int colE = 0;
   if (col_live) {
     int emB = ra.emaxB[n];
     emB = emB == kEmaxEmpty ? 0 : emB;
     colE = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
   }
-  const int t = threadIdx.x, cu = t >> 4, cc = (t & 15) * 16;
-  const bool copier = cu < P && n0 + cc < g.N;
+  // residue copies: 8 threads per modulus row of 128 bytes; two more threads
+  // copy the row's metadata
+  const int cu = t >> 3, cc = (t & 7) * 16;
+  const bool copier = cu < P && cc < ncols;
+  const int8_t* src = ra.res + cu * MN + n0 + cc;
   auto issue = [&](int64_t m, int slot) {
-    if (copier) cp_async16(&buf[slot][cu][cc], ra.res + cu * MN + m * g.N + n0 + cc);
-    cp_async_commit();                            // every thread: one group per row
-  };
-  const int64_t step = gridDim.y;
-  int64_t m = ra.m_begin + blockIdx.y;
-  if (m >= ra.m_end) return;
-  issue(m, 0);
-  for (int slot = 0; m < ra.m_end; m += step, slot ^= 1) {
-    if (m + step < ra.m_end) issue(m + step, slot ^ 1);
-    else cp_async_commit();                       // an empty group keeps the count uniform
-    cp_async_wait_one();                          // this row's copies have landed
-    __syncthreads();
-    if (col_live && !ra.route[(m / kTile) * tiles_n + n / kTile] && ra.countA[m] == 0) {
-      int emA = ra.emaxA[m];
-      emA = emA == kEmaxEmpty ? 0 : emA;
-      int32_t r[kNumModuli];
-#pragma unroll
-      for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(buf[slot][i][t]) : 0;
-      uint64_t slo, shi;
-      crt_s128<P>(r, slo, shi);
-      const DigitWindow d = digit_window(slo, shi, emA + colE);
-      write_window(g.P + m * g.N + n, MN, d, g.K, nf);
+    if (m < r1) {
+      if (copier) cp_async16(&sm.res[slot][cu][cc], src + m * g.N);
+      if (t == kBulkCols - 1) cp_async4(&sm.meta[slot][0], ra.countA + m);
+      if (t == kBulkCols - 2) cp_async4(&sm.meta[slot][1], ra.emaxA + m);
     }
-    __syncthreads();                              // the slot is free for the row after next
+    cp_async_commit();                                          // one group per row, empty or not
+  };
+#pragma unroll
+  for (int i = 0; i < kRing - 1; ++i) issue(r0 + i, i);
+  // this thread's route byte, for the current 64-row tile and the next
+  const int64_t tn = (in_range ? n : n0) / kTile;
+  int64_t tile_row = r0 / kTile;
+  uint8_t rt = ra.route[tile_row * tiles_n + tn];
+  uint8_t rt_next = (tile_row + 1) * kTile < g.M ? ra.route[(tile_row + 1) * tiles_n + tn] : 0;
+  int slot = 0, oslot = 0;
+  for (int64_t m = r0; m < r1; ++m) {
+    if (m / kTile != tile_row) {
+      ++tile_row;
+      rt = rt_next;
+      rt_next = (tile_row + 1) * kTile < g.M ? ra.route[(tile_row + 1) * tiles_n + tn] : 0;
+    }
+    // the buffers alternate by send and every send is one bulk group per
+    // issuing thread: the send before last, which used the buffer this row
+    // may fill, must have read it (the last one may still be reading)
+    if (t < kPlanesOut) ptx::bulk_wait_read<1>();
+    cp_async_wait<kRing - 2>();                   // this thread's copies of row m have landed
+    const bool general = __syncthreads_or(in_range && rt != 0) != 0;   // and everyone's
+    issue(m + kRing - 1, slot == 0 ? kRing - 1 : slot - 1);   // row m - 1's slot is free
+    const int cA = sm.meta[slot][0];
+    const int emA = sm.meta[slot][1] == kEmaxEmpty ? 0 : sm.meta[slot][1];
+    if (cA == 0) {                                              // deep rows: the deep kernel's
+      DigitWindow d;
+      if (col_live && (!general || !rt)) {
+        int32_t r[kNumModuli];
+#pragma unroll
+        for (int i = 0; i < kNumModuli; ++i) r[i] = i < P ? static_cast<int32_t>(sm.res[slot][i][t]) : 0;
+        uint64_t slo, shi;
+        crt_s128<P>(r, slo, shi);
+        d = digit_window(slo, shi, emA + colE);
+      } else {
+        d.j0 = 0;                                   // placeholder zeros (a deep column)
+        d.x[0] = d.x[1] = d.x[2] = d.x[3] = d.x[4] = 0u;
+        d.sx = 0u;
+      }
+      if (!general) {
+        if (in_range) {
+          window_to_smem_at(sm.seg[oslot], t, d);
+          sm.seg[oslot][kDigits][t] = g.K;
+          sm.seg[oslot][kDigits + 1][t] = nf;
+          ptx::fence_proxy_async_smem();          // visible to the bulk copies
+        }
+        __syncthreads();
+        if (t < kPlanesOut) {
+          ptx::bulk_store(g.P + t * MN + m * g.N + n0, &sm.seg[oslot][t][0],
+                          static_cast<uint32_t>(ncols) * 8u);
+          ptx::bulk_commit();
+        }
+        oslot ^= 1;
+      } else if (col_live && !rt) {
+        write_window(g.P + m * g.N + n, MN, d, g.K, nf);        // beside a general tile
+      }
+    }
+    slot = slot == kRing - 1 ? 0 : slot + 1;
   }
+  cp_async_wait<0>();                             // nothing left in flight at exit
+  if (t < kPlanesOut) ptx::bulk_wait_all();       // the copies have read shared memory
 }
 
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kThreads, 4) partial_staged_kernel(GemmArgs g, ReconArgs ra) {
+__global__ void __launch_bounds__(kBulkCols, 4) partial_bulk_kernel(GemmArgs g, ReconArgs ra) {
   if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
-  __shared__ __align__(16) int8_t buf[2][kNumModuli][kThreads];
+  __shared__ __align__(128) BulkSmem sm;
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
-    partial_staged_body<kBf16, decltype(Q)::value>(g, ra, buf);
+    partial_bulk_body<kBf16, decltype(Q)::value>(g, ra, sm);
   });
 }
 
@@ -1416,6 +1534,13 @@ cudaError_t launch_residues2(const ResidueOperand& o0, const ResidueOperand& o1,
                          (o1.rows + kTileRows - 1) / kTileRows, r0, bf16, nplanes, stream);
 }
 
+// Every copy of the bulk write-out starts 16-byte aligned: residue rows and
+// digit rows (N a multiple of 16) and both bases.
+bool partial_bulk_ok(const GemmArgs& g, const ReconArgs& ra) {
+  return g.P != nullptr && (g.N % 16) == 0 && (reinterpret_cast<uintptr_t>(ra.res) % 16) == 0 &&
+         (reinterpret_cast<uintptr_t>(g.P) % 16) == 0;
+}
+
 cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cudaStream_t stream) {
   const int64_t band = ra.m_end - ra.m_begin;
   if (g.M * g.N == 0 || band <= 0) return cudaSuccess;
@@ -1425,20 +1550,28 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
     // 512 blocks per column of blocks beat one row per block by 3 %)
     dim3 pgrid(static_cast<unsigned>((g.N + kThreads - 1) / kThreads),
                static_cast<unsigned>(band < 512 ? band : 512));
-    // staged copies where every row of residues starts 16-byte aligned
-    const bool staged = (g.N % 16) == 0 && (reinterpret_cast<uintptr_t>(ra.res) % 16) == 0;
+    // bulk copies where every row of residues and of digits starts 16-byte aligned
+    const bool bulk = partial_bulk_ok(g, ra);
+    if (bulk) {                                   // four blocks per SM, each a chunk of rows
+      int dev = 0, sms = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+      pgrid.x = static_cast<unsigned>((g.N + kBulkCols - 1) / kBulkCols);
+      const int64_t per_col = (int64_t(sms > 0 ? sms : 1) * 4 + pgrid.x - 1) / pgrid.x;
+      pgrid.y = static_cast<unsigned>(band < per_col ? band : per_col);
+    }
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
       constexpr int kB = decltype(B)::value, kP = decltype(P)::value;
-      if (staged) {
-        static PerDeviceOnce carveout;            // room beside a running tensor-core CTA
+      if (bulk) {
+        static PerDeviceOnce carveout;            // four 45 KB blocks per SM
         carveout.run([](int) {
-          cudaFuncSetAttribute(partial_staged_kernel<kB, kP>,
+          cudaFuncSetAttribute(partial_bulk_kernel<kB, kP>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
                                cudaSharedmemCarveoutMaxShared);
           cudaGetLastError();
           return cudaSuccess;
         });
-        partial_staged_kernel<kB, kP><<<pgrid, kThreads, 0, stream>>>(g, ra);
+        partial_bulk_kernel<kB, kP><<<pgrid, kBulkCols, 0, stream>>>(g, ra);
       } else {
         partial_fast_kernel<kB, kP><<<pgrid, kThreads, 0, stream>>>(g, ra);
       }
@@ -1460,21 +1593,22 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
 }
 
 cudaError_t launch_reconstruct_deep(const GemmArgs& g, const ReconArgs& ra, int* deep_lists,
-                                    int* deep_counters, cudaStream_t stream) {
+                                    int* deep_counters, int parts, int blocks_per_sm,
+                                    cudaStream_t stream) {
   const int64_t band = ra.m_end - ra.m_begin;
-  if (g.M * g.N == 0 || band <= 0) return cudaSuccess;
+  if (g.M * g.N == 0 || band <= 0 || (parts & (kDeepRows | kDeepCols)) == 0) return cudaSuccess;
   // deep rows and columns: index lists [M] and [N] and their two counters,
-  // filled by the routing step.  One block per SM: the kernel waits on
-  // memory most of the time, and leaves room for the fast kernel beside it.
+  // filled by the routing step.  The kernel waits on memory most of the
+  // time; one block per SM leaves room for the fast kernel beside it.
   const int* rows = deep_lists;
   const int* cols = deep_lists + g.M;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const unsigned dgrid = static_cast<unsigned>(sms > 0 ? sms : 1);
+  const unsigned dgrid = static_cast<unsigned>((sms > 0 ? sms : 1) * (blocks_per_sm > 1 ? 2 : 1));
   const cudaError_t e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
     reconstruct_deep_kernel<decltype(B)::value, decltype(P)::value>
-        <<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, deep_counters);
+        <<<dgrid, kThreads, 0, stream>>>(g, ra, rows, cols, deep_counters, parts);
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;

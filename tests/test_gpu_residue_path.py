@@ -169,6 +169,34 @@ def test_many_deep_columns_and_rows(oracle_mod):
     np.testing.assert_array_equal(dg.det_gemm_partial(a, b).cpu().numpy(), oracle_mod.gemm_digits(A, B))
 
 
+@pytest.mark.parametrize("N", [400, 512])
+def test_partial_row_segments_with_deep_and_general_outputs(oracle_mod, N):
+    # N a multiple of 16: det_gemm_partial writes row segments of 128 columns
+    # by bulk copies.  Deep columns inside a segment get placeholders that the
+    # deep kernel rewrites after it, deep rows are left to the deep kernel,
+    # and a segment touching a general tile is written output by output.
+    # N = 400 ends in a 16-column segment; M = 2048 makes two row bands.
+    g = np.random.default_rng(43)
+    M, K = 2048, 1024
+    A = g.standard_normal((M, K)).astype(np.float32)
+    B = g.standard_normal((N, K)).astype(np.float32)
+    for i, n in enumerate(range(1, N, 37)):                 # deep columns
+        B[n, (5 * i) % K] = np.float32(3e-9) * (1 if i % 2 else -1)
+    for i, m in enumerate(range(2, M, 53)):                 # deep rows
+        A[m, (13 * i + 1) % K] = np.float32(-2e-9)
+    # general tiles: rows 64..127 of C, and columns 256..319 (half of the
+    # third segment, so that segment mixes general and residue-path tiles)
+    A[64:128] = wl.loguniform_f32((64, K), 43, 0, lo=-60, hi=60)
+    B[256:320] = wl.loguniform_f32((64, K), 43, 1, lo=-60, hi=60)
+    A[300, 10] = np.float32(np.inf)
+    A[1900:1964] = wl.loguniform_f32((64, K), 44, 0, lo=-60, hi=60)   # and in the second band
+    B[N - 3, 20] = np.float32(1e-40)                        # the digit route, last segment
+    a, b = dev_f32(A), dev_f32(B)
+    P = torch.full((20, M, N), -5, dtype=torch.int64, device="cuda")   # every plane written?
+    dg.det_gemm_partial(a, b, out=P)
+    np.testing.assert_array_equal(P.cpu().numpy(), oracle_mod.gemm_digits(A, B))
+
+
 def test_vector_rows_with_ragged_k_tail(oracle_mod):
     # rows padded to a 16-byte multiple (the vector-load residue kernel) with
     # K = 1001, so the last run of four k crosses the end of the row
