@@ -295,8 +295,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const int64_t n_left = a.N - (n0 + cb * 32);
             if (n_left >= 32 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
-              reinterpret_cast<uint4*>(out)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-              reinterpret_cast<uint4*>(out)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+              // evict-first: read once, by the reconstruction after the launch
+              __stcs(reinterpret_cast<uint4*>(out), make_uint4(packed[0], packed[1], packed[2], packed[3]));
+              __stcs(reinterpret_cast<uint4*>(out) + 1, make_uint4(packed[4], packed[5], packed[6], packed[7]));
             } else {
 #pragma unroll
               for (int j = 0; j < 32; ++j)

@@ -192,9 +192,11 @@ __device__ __forceinline__ void write_residue_quads(uint2* dst, const float (&x)
                                                     const float (&pw)[4]) {
   if constexpr (i < P) {
     constexpr int p = modulus(i);
-    dst[i * (kPlaneRows * kStageK / 4)] =
-        make_uint2(bf16_pair(residue_f32<p>(x[0], pw[0]), residue_f32<p>(x[1], pw[1])),
-                   bf16_pair(residue_f32<p>(x[2], pw[2]), residue_f32<p>(x[3], pw[3])));
+    // evict-first: the planes are read back by a later launch, and a later
+    // band's are written while a GEMM's own planes need L2
+    __stcs(&dst[i * (kPlaneRows * kStageK / 4)],
+           make_uint2(bf16_pair(residue_f32<p>(x[0], pw[0]), residue_f32<p>(x[1], pw[1])),
+                      bf16_pair(residue_f32<p>(x[2], pw[2]), residue_f32<p>(x[3], pw[3]))));
     write_residue_quads<i + 1, P>(dst, x, pw);
   }
 }
@@ -935,7 +937,7 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
       if (i < P) {
         const int8_t* plane = ra.res + i * MN + base;
         if (vec) {
-          packed[i] = *reinterpret_cast<const uint32_t*>(plane);
+          packed[i] = __ldcs(reinterpret_cast<const unsigned int*>(plane));   // read once
         } else {
 #pragma unroll
           for (int j = 0; j < kReconCols; ++j)
@@ -963,7 +965,7 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
     }
     uint32_t* dst = reinterpret_cast<uint32_t*>(g.C) + m * g.ldc + n0;
     if (store4) {
-      *reinterpret_cast<uint4*>(dst) = make_uint4(out[0], out[1], out[2], out[3]);
+      __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
     } else {
 #pragma unroll
       for (int j = 0; j < kReconCols; ++j)
