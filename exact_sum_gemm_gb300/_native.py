@@ -33,6 +33,7 @@ SIGNATURES = {
     "det_kernel_launches": (ctypes.c_uint64, []),
     "det_tile_routes": (_i32, [ctypes.POINTER(_i64)]),
     "det_set_wide_path": (_i32, [_i32]),
+    "det_set_batched_pipeline": (_i32, [_i32]),
     "det_stage_timing": (_i32, [_i32]),
     "det_residue_moduli": (_i32, [_i32, _i64]),
     "det_moduli_used": (_i32, [ctypes.POINTER(_i32), _i32]),

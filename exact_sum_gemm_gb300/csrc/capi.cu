@@ -51,6 +51,8 @@ det_status validate_gemm(det_dtype dtype, int64_t M, int64_t N, int64_t K, const
   return DET_OK;
 }
 
+std::atomic<int> g_batched_pipeline{1};          // det_set_batched_pipeline
+
 det::GemmArgs make_args(det_dtype dtype, int64_t M, int64_t N, int64_t K, const void* A,
                         int64_t lda, int opA, const void* B, int64_t ldb, int opB) {
   det::GemmArgs a{};
@@ -88,6 +90,8 @@ int det_moduli_used(int* out, int max) {
 }
 
 int det_set_wide_path(int enable) { return det::set_wide_path(enable); }
+
+int det_set_batched_pipeline(int enable) { return g_batched_pipeline.exchange(enable ? 1 : 0); }
 
 int det_tile_routes(int64_t* out) {
   if (out == nullptr) return -1;
@@ -234,6 +238,20 @@ det_status det_gemm_strided_batched(det_dtype dtype, int64_t batch, int64_t M, i
     return DET_ERR_SHAPE;
   const int64_t es = dtype == DET_F32 ? 4 : 2;
   const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // every entry in one residue-path pipeline where the shapes allow
+  const int64_t kBig = int64_t(1) << 30;
+  if (batch > 1 && g_batched_pipeline.load(std::memory_order_relaxed) != 0 && M <= kBig / batch &&
+      N <= kBig / batch && strideA <= INT32_MAX && strideB <= INT32_MAX && strideC <= INT32_MAX) {
+    det::GemmArgs g = make_args(dtype, batch * M, N, K, A, lda, opA, B, ldb, opB);
+    g.C = C;
+    g.ldc = ldc;
+    g.batch = static_cast<int32_t>(batch);
+    g.Me = static_cast<int32_t>(M);
+    g.strideA = static_cast<int32_t>(strideA);
+    g.strideB = static_cast<int32_t>(strideB);
+    g.strideC = static_cast<int32_t>(strideC);
+    if (det::batched_residue_ok(g)) return from_cuda(det::launch_gemm(g, st));
+  }
   for (int64_t b = 0; b < batch; ++b) {
     const void* Ab = static_cast<const char*>(A) + b * strideA * es;
     const void* Bb = static_cast<const char*>(B) + b * strideB * es;

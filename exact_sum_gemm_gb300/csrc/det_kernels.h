@@ -77,13 +77,66 @@ struct GemmArgs {
   float* C;           // fused-finalize output (det_gemm), or null
   int64_t ldc;
   int64_t* P;         // canonical digit planes [20][M][N] (det_gemm_partial), or null
+  // A strided batch computed as one problem (det_gemm_strided_batched, C
+  // output only): `batch` entries of Me rows each are stacked as the
+  // M = batch * Me rows of A and C; output row m belongs to entry
+  // e = m / Me, whose A, B and C start e * strideA, e * strideB elements and
+  // e * strideC floats after entry 0's.  Per-row arrays of B hold every
+  // entry's N rows, stacked: row n of entry e at e * N + n.  batch = 1: a
+  // plain GEMM (Me and the strides unused).  32-bit fields (the batched path
+  // takes stacked row counts below 2^30 and strides below 2^31): the kernels
+  // that take GemmArgs by value keep their register allocation.
+  int32_t batch = 1;
+  int32_t Me = 0;
+  int32_t strideA = 0, strideB = 0, strideC = 0;
 };
+
+// Quotient of row indices of a strided batch (below 2^30: a 32-bit division).
+__host__ __device__ inline int64_t entry_div(int64_t r, int64_t rows) {
+  return static_cast<int64_t>(static_cast<uint32_t>(r) / static_cast<uint32_t>(rows));
+}
+// Rows of B's per-row arrays (every entry's N rows).
+__host__ __device__ inline int64_t rows_of_b(const GemmArgs& g) {
+  return g.batch > 1 ? g.batch * g.N : g.N;
+}
+// B's stacked row for output row m, column n.
+__host__ __device__ inline int64_t brow_of(const GemmArgs& g, int64_t m, int64_t n) {
+  return g.batch > 1 ? entry_div(m, g.Me) * g.N + n : n;
+}
+// Element offsets of A's (m, k) and of B's stacked row s at k.
+__host__ __device__ inline int64_t a_offset(const GemmArgs& g, int64_t m, int64_t k) {
+  int64_t e = 0;
+  if (g.batch > 1) {
+    e = entry_div(m, g.Me);
+    m -= e * g.Me;
+  }
+  return e * int64_t(g.strideA) + (g.opA ? k * g.lda + m : m * g.lda + k);
+}
+__host__ __device__ inline int64_t b_offset(const GemmArgs& g, int64_t s, int64_t k) {
+  int64_t e = 0;
+  if (g.batch > 1) {
+    e = entry_div(s, g.N);
+    s -= e * g.N;
+  }
+  return e * int64_t(g.strideB) + (g.opB ? k * g.ldb + s : s * g.ldb + k);
+}
+// Offset (in floats) of C's output row m.
+__host__ __device__ inline int64_t c_row_offset(const GemmArgs& g, int64_t m) {
+  if (g.batch <= 1) return m * g.ldc;
+  const int64_t e = entry_div(m, g.Me);
+  return e * int64_t(g.strideC) + (m - e * g.Me) * g.ldc;
+}
 
 // Wide residue path on (1, the default) or off (0); returns the previous setting.
 int set_wide_path(int enable);
 
-// Exact GEMM; writes C (if args.C) or the digit planes P (if args.P).
+// Exact GEMM; writes C (if args.C) or the digit planes P (if args.P).  A
+// strided batch (batch > 1) must pass batched_residue_ok.
 cudaError_t launch_gemm(const GemmArgs& args, cudaStream_t stream);
+// Whether a strided batch can run as one residue-path problem: C output,
+// K-contiguous operands whose rows suit the fused planes kernel, N and the
+// entries' rows multiples of 64.
+bool batched_residue_ok(const GemmArgs& args);
 
 // Stream-ordered scratch from the library's memory pool (one per device, kept
 // reserved between calls); release with cudaFreeAsync on the same stream.

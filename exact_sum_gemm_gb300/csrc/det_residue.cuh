@@ -102,7 +102,16 @@ struct ResidueOperand {
   unsigned long long* norm_max;  // fused kernel: zeroed slot for the largest norm of these rows
   unsigned* dmax;             // fused kernel: [rows/64], zeroed: largest deep count of each
                               //   64-row block (or null)
+  int64_t group_rows = 0;     // > 0: the rows are groups of group_rows (a strided batch's
+  int64_t group_stride = 0;   //   entries), group g starting g * group_stride elements on
 };
+
+// Element offset of an operand's row r (K-contiguous or not).
+__host__ __device__ inline int64_t operand_row_offset(const ResidueOperand& o, int64_t r) {
+  if (o.group_rows <= 0) return r * o.ld;
+  const int64_t g = entry_div(r, o.group_rows);      // grouped rows stay below 2^30
+  return g * o.group_stride + (r - g * o.group_rows) * o.ld;
+}
 
 // Thresholds of the moduli choice: P moduli suffice for a row band whose
 // largest row-norm bounds are a (A) and b (B) when the 128-bit a * b is below
@@ -226,8 +235,48 @@ struct ResGemmArgs {
   const int* used;            // moduli to compute (device int, in [used_min, nplanes]; 0:
   int used_min;               //   nothing), or null for all nplanes; the grid is sized for used_min
   int grid_moduli;            // if > 0: size the grid for this many moduli instead
+  // A strided batch's band (entry_rows > 0): M = whole entries of entry_rows
+  // rows, the first being entry entry0; output rows of local entry e take
+  // B's planes rows (entry0 + e) * N + n.  Only each entry's own tiles are
+  // computed; rows and columns past the entry's are not written.
+  int64_t entry_rows = 0;
+  int64_t entry0 = 0;
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
+
+// Rows of B's planes a launch reads (every entry's up to its band's last).
+__host__ __device__ inline int64_t gemm_b_rows(const ResGemmArgs& a) {
+  return a.entry_rows > 0 ? (a.entry0 + a.M / a.entry_rows) * a.N : a.N;
+}
+// Output tiles of TM x TN of a launch: the whole M x N, or each entry's own.
+template <int TM, int TN>
+__host__ __device__ inline int64_t gemm_tiles(const ResGemmArgs& a) {
+  const int64_t tn = (a.N + TN - 1) / TN;
+  if (a.entry_rows > 0) return (a.M / a.entry_rows) * ((a.entry_rows + TM - 1) / TM) * tn;
+  return ((a.M + TM - 1) / TM) * tn;
+}
+// Tile t: its first row of A (in the launch), first row of B's planes, first
+// output column, and the end of its rows' entry (rows from there on are
+// another entry's, or past M: computed but not written).
+template <int TM, int TN>
+__host__ __device__ inline void gemm_tile(const ResGemmArgs& a, int64_t t, int64_t& m0, int64_t& nb0,
+                                          int64_t& n0, int64_t& m_end) {
+  const int64_t tn = (a.N + TN - 1) / TN;
+  if (a.entry_rows > 0) {
+    const int64_t tm = (a.entry_rows + TM - 1) / TM;
+    const int64_t e = t / (tm * tn), r = t - e * (tm * tn);
+    const int64_t i = r / tn;
+    m0 = e * a.entry_rows + i * TM;
+    n0 = (r - i * tn) * TN;
+    nb0 = (a.entry0 + e) * a.N + n0;
+    m_end = (e + 1) * a.entry_rows;
+  } else {
+    m0 = (t / tn) * TM;
+    n0 = (t - (t / tn) * tn) * TN;
+    nb0 = n0;
+    m_end = a.M;
+  }
+}
 // Moduli a GEMM launch computes (every CTA reads the same device int).
 // A count of 0 means the launch has nothing to compute (no work item).
 __device__ __forceinline__ int planes_used(const ResGemmArgs& a) {

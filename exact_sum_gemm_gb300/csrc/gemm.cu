@@ -58,14 +58,19 @@ cudaError_t device_pool(cudaMemPool_t* out) {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-int64_t tiles_mn(const GemmArgs& g) { return (g.M + kTile - 1) / kTile + (g.N + kTile - 1) / kTile; }
+// 64-row blocks of A plus 64-row blocks of B's per-row arrays (a strided
+// batch's entries have N a multiple of 64, so no block spans two entries)
+int64_t tiles_mn(const GemmArgs& g) {
+  return (g.M + kTile - 1) / kTile + (rows_of_b(g) + kTile - 1) / kTile;
+}
 
 }  // namespace
 
 size_t scratch_bytes(const GemmArgs& g, int64_t slots) {
   const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
-  size_t b = align_up(sizeof(int) * size_t(g.M + g.N), 256);        // emax
-  b += align_up(sizeof(int) * size_t(g.M + g.N), 256);              // deep
+  const int64_t nb = rows_of_b(g);
+  size_t b = align_up(sizeof(int) * size_t(g.M + nb), 256);         // emax
+  b += align_up(sizeof(int) * size_t(g.M + nb), 256);               // deep
   b += align_up(size_t(tiles), 256);                                 // route
   b += align_up(sizeof(int) * size_t(tiles + 1), 256);              // general-tile list
   b += align_up(sizeof(int) * size_t(tiles_mn(g)), 256);            // block maxima
@@ -77,12 +82,13 @@ Scratch carve_scratch(void* base, const GemmArgs& g, int64_t slots) {
   const int64_t tiles = ((g.M + kTile - 1) / kTile) * ((g.N + kTile - 1) / kTile);
   char* p = static_cast<char*>(base);
   Scratch s{};
+  const int64_t nb = rows_of_b(g);
   s.emaxA = reinterpret_cast<int*>(p);
   s.emaxB = s.emaxA + g.M;
-  p += align_up(sizeof(int) * size_t(g.M + g.N), 256);
+  p += align_up(sizeof(int) * size_t(g.M + nb), 256);
   s.deepA = reinterpret_cast<int*>(p);
   s.deepB = s.deepA + g.M;
-  p += align_up(sizeof(int) * size_t(g.M + g.N), 256);
+  p += align_up(sizeof(int) * size_t(g.M + nb), 256);
   s.route = reinterpret_cast<uint8_t*>(p);
   p += align_up(size_t(tiles), 256);
   s.general = reinterpret_cast<int*>(p);
@@ -196,22 +202,24 @@ ResidueScratch residue_layout(const GemmArgs& g, int nplanes, int64_t Kp, int ca
   // every 64-row block of A and of B [tiles_m + tiles_n]; then the row-norm
   // bounds normA [M], normB [N] and four slots per band [4 kMaxBands] (norm
   // maxima of A and B, and the moduli kernel's two block minima)
+  // (B's per-row arrays have rows_of_b rows: every entry's of a strided batch)
+  const int64_t nb = rows_of_b(g);
   r.off_counts = b;
-  r.off_norms = align_up(b + sizeof(int) * size_t(2 * (g.M + g.N) + 3 + 2 * kMaxBands +
+  r.off_norms = align_up(b + sizeof(int) * size_t(2 * (g.M + nb) + 3 + 2 * kMaxBands +
                                                   tiles_mn(g)), 8);
-  b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + g.N + 4 * kMaxBands);
+  b = r.off_norms + sizeof(unsigned long long) * size_t(g.M + nb + 4 * kMaxBands);
   r.zero_bytes = b - r.off_counts;
   b = align_up(b, 1024);
   r.off_deep_idx = b;                    // deep rows [M], deep columns [N]
-  b = align_up(b + sizeof(int) * size_t(g.M + g.N), 1024);
+  b = align_up(b + sizeof(int) * size_t(g.M + nb), 1024);
   r.off_listA = b;
   b = align_up(b + sizeof(uint2) * size_t(g.M) * cap, 1024);
   r.off_listB = b;
-  b = align_up(b + sizeof(uint2) * size_t(g.N) * cap, 1024);
+  b = align_up(b + sizeof(uint2) * size_t(nb) * cap, 1024);
   r.off_planesA = b;
   b = align_up(b + size_t(2) * nplanes * size_t(plane_rows(g.M)) * size_t(Kp), 1024);
   r.off_planesB = b;
-  b = align_up(b + size_t(2) * nplanes * size_t(plane_rows(g.N)) * size_t(Kp), 1024);
+  b = align_up(b + size_t(2) * nplanes * size_t(plane_rows(nb)) * size_t(Kp), 1024);
   r.off_res = b;
   b = align_up(b + size_t(nplanes) * size_t(g.M) * size_t(g.N), 1024);
   r.bytes = b;
@@ -303,12 +311,19 @@ int band_bounds(const GemmArgs& g, int64_t (&edge)[kMaxBands + 1]) {
     edge[1] = g.M;
     return 1;
   }
-  const int64_t tiles = (g.M + 255) / 256;
+  // a strided batch is cut between entries (each band's GEMM takes whole
+  // entries); one entry of 2048 rows or more stays one band
+  const int64_t unit = g.batch > 1 ? g.Me : 256;
+  const int64_t tiles = (g.M + unit - 1) / unit;
+  if (tiles < 2) {
+    edge[1] = g.M;
+    return 1;
+  }
   double f = 0.5 + 0.19 * log2(static_cast<double>(g.K) / 2048.0);
   f = f < 0.5 ? 0.5 : (f > 0.69 ? 0.69 : f);
   int64_t t0 = static_cast<int64_t>(static_cast<double>(tiles) * f);
   t0 = t0 < 1 ? 1 : (t0 > tiles - 1 ? tiles - 1 : t0);
-  edge[1] = t0 * 256;
+  edge[1] = t0 * unit;
   edge[2] = g.M;
   return 2;
 }
@@ -335,14 +350,15 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   if (e != cudaSuccess) return e;
   const Scratch s = carve_scratch(base, g, 0);
   int* counts = reinterpret_cast<int*>(base + L.off_counts);
-  int* error = counts + g.M + g.N;
+  const int64_t nbr = rows_of_b(g);                                  // B's per-row arrays
+  int* error = counts + g.M + nbr;
   int* used = error + 3;                                             // moduli per band
   unsigned* done = reinterpret_cast<unsigned*>(used + kMaxBands);    // fused-launch counters
   unsigned* keymax = done + kMaxBands;                               // [M] then [N]
-  unsigned* dmax = keymax + g.M + g.N;                               // [tiles_m] then [tiles_n]
-  const int64_t tiles_m = (g.M + kTile - 1) / kTile, tiles_n = (g.N + kTile - 1) / kTile;
+  unsigned* dmax = keymax + g.M + nbr;                               // [tiles_m] then B's blocks
+  const int64_t tiles_m = (g.M + kTile - 1) / kTile, blocks_b = (nbr + kTile - 1) / kTile;
   unsigned long long* norms = reinterpret_cast<unsigned long long*>(base + L.off_norms);
-  unsigned long long* maxima = norms + g.M + g.N;                    // [4 b]: band b's A, [1]: B
+  unsigned long long* maxima = norms + g.M + nbr;                    // [4 b]: band b's A, [1]: B
   const int least = residue_planes_least(g.bf16);
   uint2* listA = reinterpret_cast<uint2*>(base + L.off_listA);
   uint2* listB = reinterpret_cast<uint2*>(base + L.off_listB);
@@ -359,10 +375,16 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // K-contiguous, aligned operands with K <= kFusedK take the fused kernel:
   // exponent maxima, planes, norms and the moduli count in one launch per
   // band (no separate pre-pass over A and B)
-  const ResidueOperand rb{g.B, g.ldb, g.opB, g.N, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
-                          norms + g.M, keymax + g.M, maxima + 1, dmax + tiles_m};
-  const bool fused = fused_residues_ok(rb, g.bf16) &&
-                     fused_residues_ok(ResidueOperand{g.A, g.lda, g.opA, g.M, g.K, Kp}, g.bf16);
+  // (a strided batch: B's operand is every entry's rows, stacked)
+  const bool grouped = g.batch > 1;
+  const ResidueOperand rb{g.B, g.ldb, g.opB, nbr, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
+                          norms + g.M, keymax + g.M, maxima + 1, dmax + tiles_m,
+                          grouped ? g.N : 0, grouped ? g.strideB : 0};
+  ResidueOperand whole_a{g.A, g.lda, g.opA, g.M, g.K, Kp};
+  whole_a.group_rows = grouped ? g.Me : 0;
+  whole_a.group_stride = grouped ? g.strideA : 0;
+  const bool fused = fused_residues_ok(rb, g.bf16) && fused_residues_ok(whole_a, g.bf16);
+  if (grouped && !fused) return cudaErrorInvalidValue;   // the caller checks batched_residue_ok
   {
     StageScope t(kStagePrepass, stream);
     e = fused ? cudaSuccess : launch_emax(g, s, stream);
@@ -373,22 +395,24 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   auto fused_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
     return FusedBand{maxima + 4 * b, maxima + 1, done + b, used + b, b, least, nplanes, thr,
-                     dmax + m0 / kTile, (rows + kTile - 1) / kTile, dmax + tiles_m, tiles_n,
+                     dmax + m0 / kTile, (rows + kTile - 1) / kTile, dmax + tiles_m, blocks_b,
                      deep_list_cap(g.K)};
   };
   // the residue kernels' deep-list counters double as the rows' deep counts,
   // from which the tiles are routed
   auto operand_of_band = [&](int b) {
     const int64_t m0 = edge[b], rows = edge[b + 1] - edge[b];
-    const void* X = static_cast<const char*>(g.A) + (g.opA ? m0 : m0 * g.lda) * es;
+    // (a strided batch's bands start on an entry: rows m0.. are entry m0 / Me's)
+    const void* X = static_cast<const char*>(g.A) +
+                    (grouped ? (m0 / g.Me) * g.strideA : (g.opA ? m0 : m0 * g.lda)) * es;
     return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
                           planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
                           counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0, maxima + 4 * b,
-                          dmax + m0 / kTile};
+                          dmax + m0 / kTile, grouped ? g.Me : 0, grouped ? g.strideA : 0};
   };
   // the band's moduli count, once its rows' and B's norm bounds are complete
   auto moduli_of_band = [&](int b) {
-    return launch_moduli(norms + edge[b], edge[b + 1] - edge[b], norms + g.M, g.N, g.bf16, least,
+    return launch_moduli(norms + edge[b], edge[b + 1] - edge[b], norms + g.M, nbr, g.bf16, least,
                          nplanes, used + b, b, maxima + 4 * b, counts + edge[b], counts + g.M,
                          deep_list_cap(g.K), stream);
   };
@@ -404,6 +428,10 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     StageScope t(kStageResidueGemm, hs);
     ResGemmArgs rg{planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK, planesB,
                    rows, g.N, Kp, nplanes, res + m0 * g.N, g.M * g.N, error, status, used + b, least};
+    if (grouped) {                         // the band's entries: only their own tiles
+      rg.entry_rows = g.Me;
+      rg.entry0 = m0 / g.Me;
+    }
     // 256 x 256 tiles on CTA pairs, unless a single 128-row tile covers M or
     // the device cannot run clusters of two
     if (rows > 128) {
@@ -446,7 +474,8 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   }
   bool gen_forked = false;
   WidePlan plan{};
-  const bool wide_on = g_wide_path.load(std::memory_order_relaxed) != 0;
+  // (a strided batch's general tiles go to the general kernel)
+  const bool wide_on = g_wide_path.load(std::memory_order_relaxed) != 0 && !grouped;
   if (e == cudaSuccess && !wide_on) {
     // the wide path switched off: the general kernel takes every general
     // tile, beside the GEMMs on the lowest-priority stream
@@ -553,8 +582,28 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
 
 int set_wide_path(int enable) { return g_wide_path.exchange(enable ? 1 : 0); }
 
+bool batched_residue_ok(const GemmArgs& g) {
+  if (g.batch <= 1 || g.Me <= 0 || g.M != int64_t(g.batch) * g.Me || g.P != nullptr || g.C == nullptr)
+    return false;
+  // whole 64-row blocks per entry (routing, tiles), K-contiguous rows for the
+  // fused planes kernel, every stacked row index an int
+  if (g.Me % kTile != 0 || g.N % kTile != 0 || g.opA != 0 || g.opB != 0 || g.K <= 0) return false;
+  if (g.M > (int64_t(1) << 30) || rows_of_b(g) > (int64_t(1) << 30)) return false;
+  if (g.strideA < 0 || g.strideB < 0 || g.strideC < 0) return false;
+  if (residue_planes_needed(g) <= 0) return false;
+  ResidueOperand a{g.A, g.lda, g.opA, g.M, g.K, 0};
+  a.group_rows = g.Me;
+  a.group_stride = g.strideA;
+  ResidueOperand b{g.B, g.ldb, g.opB, rows_of_b(g), g.K, 0};
+  b.group_rows = g.N;
+  b.group_stride = g.strideB;
+  return fused_residues_ok(a, g.bf16) && fused_residues_ok(b, g.bf16);
+}
+
 cudaError_t launch_gemm(const GemmArgs& g, cudaStream_t stream) {
   if (g.M == 0 || g.N == 0) return cudaSuccess;
+  // a strided batch as one problem only where every stage handles it
+  if (g.batch > 1 && !batched_residue_ok(g)) return cudaErrorInvalidValue;
   const int nplanes = residue_planes_needed(g);
   // grid limits: the residue kernel puts 32-row blocks, the tensor-core
   // kernel 128-row tiles, in gridDim.y (at most 65535)

@@ -126,18 +126,16 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p, c
         const int r = p.opA ? (idx & 31) : (idx >> 5);
         const int k = p.opA ? (idx >> 5) : (idx & 31);
         const int64_t gm = m0 + r, gk = k0 + k;
-        st.a[u] = (gm < p.M && gk < p.K)
-                      ? load_bits<kBf16>(p.A, p.opA ? gk * p.lda + gm : gm * p.lda + gk)
-                      : 0u;
+        st.a[u] = (gm < p.M && gk < p.K) ? load_bits<kBf16>(p.A, a_offset(p, gm, gk)) : 0u;
       }
       // B
       {
         const int r = p.opB ? (idx & 31) : (idx >> 5);
         const int k = p.opB ? (idx >> 5) : (idx & 31);
         const int64_t gn = n0 + r, gk = k0 + k;
-        st.b[u] = (gn < p.N && gk < p.K)
-                      ? load_bits<kBf16>(p.B, p.opB ? gk * p.ldb + gn : gn * p.ldb + gk)
-                      : 0u;
+        // (a strided batch: B's rows of the tile's entry)
+        st.b[u] = (gn < p.N && gk < p.K) ? load_bits<kBf16>(p.B, b_offset(p, brow_of(p, m0, gn), gk))
+                                         : 0u;
       }
     }
   };
@@ -272,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) kulisch_smem_kernel(GemmArgs p, c
       out[(kDigits + 1) * MN] = nf_count[s];
     } else {
       const uint32_t bits = nf_count[s] ? kNanBits : round_to_f32_bits(w, top);
-      reinterpret_cast<uint32_t*>(p.C)[m * p.ldc + n] = bits;
+      reinterpret_cast<uint32_t*>(p.C)[c_row_offset(p, m) + n] = bits;
     }
   }
   }  // tile loop

@@ -194,15 +194,18 @@ __global__ void __launch_bounds__(kThreads) block_max_kernel(const int* deepA, i
 
 // Routing, step 2, one thread per 64x64 tile: 1 = general kernel, 0 = residue
 // path / band kernel.  The general kernel's tiles are also listed after a
-// count, general[0].
+// count, general[0].  A strided batch (tm_entry > 0 row blocks per entry):
+// tile row tm belongs to entry tm / tm_entry, whose column blocks are B's
+// blocks from entry * tiles_n on.
 __global__ void __launch_bounds__(kThreads) route_kernel(const int* bmax, int64_t tiles_m,
-                                                          int64_t tiles_n, int cap, uint8_t* route,
-                                                          int* general) {
+                                                          int64_t tiles_n, int64_t tm_entry, int cap,
+                                                          uint8_t* route, int* general) {
   const int64_t tiles = tiles_m * tiles_n;
   for (int64_t t = int64_t(blockIdx.x) * kThreads + threadIdx.x; t < tiles;
        t += int64_t(gridDim.x) * kThreads) {
     const int64_t tm = t / tiles_n, tn = t - (t / tiles_n) * tiles_n;
-    const bool gen = static_cast<int64_t>(bmax[tm]) + bmax[tiles_m + tn] > cap;
+    const int64_t bn = tm_entry > 0 ? (tm / tm_entry) * tiles_n + tn : tn;
+    const bool gen = static_cast<int64_t>(bmax[tm]) + bmax[tiles_m + bn] > cap;
     route[t] = gen ? 1 : 0;
     if (gen) general[1 + atomicAdd(general, 1)] = static_cast<int>(t);
   }
@@ -243,15 +246,18 @@ int deep_list_cap(int64_t K) {
 cudaError_t launch_classify(const GemmArgs& g, const int* deepA, const int* deepB, const Scratch& s,
                             int* deep_rows, int* deep_cols, int* deep_counters,
                             cudaStream_t stream) {
+  // (a strided batch: B's blocks are every entry's, N and Me multiples of 64)
+  const int64_t nb = rows_of_b(g);
   const int64_t tiles_m = (g.M + kTile - 1) / kTile, tiles_n = (g.N + kTile - 1) / kTile;
-  const int64_t warps = tiles_m + tiles_n;
+  const int64_t warps = tiles_m + (nb + kTile - 1) / kTile;
   const int64_t grid1 = (warps * 32 + kThreads - 1) / kThreads;
   block_max_kernel<<<static_cast<unsigned>(grid1 > 0 ? grid1 : 1), kThreads, 0, stream>>>(
-      deepA, g.M, deepB, g.N, s.bmax, deep_rows, deep_cols, deep_counters, s.general);
+      deepA, g.M, deepB, nb, s.bmax, deep_rows, deep_cols, deep_counters, s.general);
   const int64_t tiles = tiles_m * tiles_n;
   const int64_t grid2 = (tiles + kThreads - 1) / kThreads;
   route_kernel<<<static_cast<unsigned>(grid2 < 1024 ? (grid2 > 0 ? grid2 : 1) : 1024), kThreads, 0,
-                 stream>>>(s.bmax, tiles_m, tiles_n, deep_list_cap(g.K), s.route, s.general);
+                 stream>>>(s.bmax, tiles_m, tiles_n, g.batch > 1 ? g.Me / kTile : 0,
+                           deep_list_cap(g.K), s.route, s.general);
   note_launch(2);
   return cudaGetLastError();
 }

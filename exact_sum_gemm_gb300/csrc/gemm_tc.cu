@@ -90,8 +90,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   // work units: (modulus, pair of neighbouring output tiles), modulus-major so
   // that the CTAs in flight share one plane of A and one of B in L2
-  const int64_t tiles_n = (a.N + kBlockN - 1) / kBlockN;
-  const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * tiles_n;
+  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a);   // (a strided batch: each entry's own)
   const int64_t tile_pairs = (tiles + 1) / 2;
   const int64_t units = tile_pairs * planes_used(a);
   if (units == 0) return;                  // nothing to compute: leave before any set-up
@@ -125,10 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     t0 = 2 * (unit - static_cast<int64_t>(u) * tile_pairs);
     T = t0 + 1 < tiles ? 2 : 1;
   };
-  auto tile_origin = [&](int64_t t, int64_t& m0, int64_t& n0) {
-    m0 = (t / tiles_n) * kBlockM;
-    n0 = (t - (t / tiles_n) * tiles_n) * kBlockN;
-  };
+
 
   if (warp == 0) {
     if (lane == 0) {
@@ -141,8 +137,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int J = 0; J < T * nch && ok; ++J) {
         int tt, c;
         job_at(J, T, tt, c);
-        int64_t m0, n0;
-        tile_origin(t0 + tt, m0, n0);
+        int64_t m0, nb0, n0, m_end;
+        gemm_tile<kBlockM, kBlockN>(a, t0 + tt, m0, nb0, n0, m_end);
         const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
         for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -154,7 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           unsigned char* st = smem + s * kStageBytes;
           ptx::tma_load_5d(st, &tmA, &full[s], 0, 0, u, kb, static_cast<int>(m0 / kPlaneRows));
           ptx::tma_load_5d(st + kABytes, &tmB, &full[s], 0, 0, u, kb,
-                           static_cast<int>(n0 / kPlaneRows));
+                           static_cast<int>(nb0 / kPlaneRows));
           ++it;
         }
       }
@@ -229,8 +225,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int J = 0; J < T * nch; ++J) {
       int tt, c;
       job_at(J, T, tt, c);
-      int64_t m0, n0;
-      tile_origin(t0 + tt, m0, n0);
+      int64_t m0, nb0, n0, m_end;
+      gemm_tile<kBlockM, kBlockN>(a, t0 + tt, m0, nb0, n0, m_end);
       const int64_t row = m0 + 32 * g + lane;
       const int acc = tt;
       if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
@@ -254,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[j] = __float_as_uint(near_mod_f32(__uint_as_float(v[j]), p, inv_p));
         if (!last) {
           ptx::tmem_st32(taddr, v);
-        } else if (row < a.M) {
+        } else if (row < m_end) {
           // a second reduction makes the residue balanced (|r| <= 127); its
           // byte is the low byte of the pattern of r + 1.5*2^23
           int8_t* out = a.res + u * a.res_plane + row * a.N + n0 + cb * 32;
@@ -349,14 +345,14 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (ce != cudaSuccess) return ce;
   CUtensorMap tmA, tmB;
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kBlockM) ||
-      !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kBlockN))
+      !make_plane_map(&tmB, a.B, gemm_b_rows(a), a.Kp, a.nplanes, kBlockN))
     return cudaErrorInvalidValue;
   // persistent: one CTA per SM (the shared memory and TMEM footprint allow no more)
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int64_t tiles = ((a.M + kBlockM - 1) / kBlockM) * ((a.N + kBlockN - 1) / kBlockN);
+  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a);
   // sized for the fewest moduli the launch may compute (every CTA has a unit)
   const int64_t units = (tiles + 1) / 2 *
       (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));

@@ -91,8 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
-  const int64_t tiles_n = (a.N + kTileN - 1) / kTileN;
-  const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * tiles_n;
+  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a);   // (a strided batch: each entry's own)
   const int64_t singles = tiles * planes_used(a);  // (modulus, tile), modulus-major
   // a cluster with no item (a launch sized for more moduli than it computes)
   // issues no MMA, so it neither commits nor waits for the final commit
@@ -139,10 +138,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     u = static_cast<int>(sgl / tiles);
     t = sgl - static_cast<int64_t>(u) * tiles;
   };
-  auto tile_origin = [&](int64_t t, int64_t& m0, int64_t& n0) {
-    m0 = (t / tiles_n) * kPairM;
-    n0 = (t - (t / tiles_n) * tiles_n) * kTileN;
-  };
+
 
   if (warp == 0) {
     if (lane == 0) {
@@ -156,11 +152,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int J = 0; J < T * nch && ok; ++J) {
           int tt, c, u;
           job_at(J, T, tt, c);
-          int64_t t, m0, n0;
+          int64_t t, m0, nb0, n0, m_end;
           single_at(sg[tt], u, t);
-          tile_origin(t, m0, n0);
+          gemm_tile<kPairM, kTileN>(a, t, m0, nb0, n0, m_end);
           const int ga = static_cast<int>((m0 + kHalfM * rank) / kPlaneRows);
-          const int gb = static_cast<int>((n0 + (kTileN / 2) * rank) / kPlaneRows);
+          const int gb = static_cast<int>((nb0 + (kTileN / 2) * rank) / kPlaneRows);
           const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
           for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
             const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -251,9 +247,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int J = 0; J < T * nch; ++J) {
         int tt, c, u;
         job_at(J, T, tt, c);
-        int64_t t, m0, n0;
+        int64_t t, m0, nb0, n0, m_end;
         single_at(sg[tt], u, t);
-        tile_origin(t, m0, n0);
+        gemm_tile<kPairM, kTileN>(a, t, m0, nb0, n0, m_end);
         const int64_t row = m0 + kHalfM * rank + 32 * g + lane;
         const int acc = tt;
         if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
@@ -277,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[j] = __float_as_uint(near_mod_f32(__uint_as_float(v[j]), p, inv_p));
           if (!last) {
             ptx::tmem_st32(taddr, v);
-          } else if (row < a.M) {
+          } else if (row < m_end) {
             // a second reduction makes the residue balanced; its byte is the
             // low byte of the pattern of r + 1.5*2^23
             int8_t* out = a.res + u * a.res_plane + row * a.N + n0 + cb * 32;
@@ -365,9 +361,9 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   if (max_clusters[dev] < 0) return cudaErrorNotSupported;
   CUtensorMap tmA, tmB;
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kHalfM) ||
-      !make_plane_map(&tmB, a.B, a.N, a.Kp, a.nplanes, kTileN / 2))
+      !make_plane_map(&tmB, a.B, gemm_b_rows(a), a.Kp, a.nplanes, kTileN / 2))
     return cudaErrorInvalidValue;
-  const int64_t tiles = ((a.M + kPairM - 1) / kPairM) * ((a.N + kTileN - 1) / kTileN);
+  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a);
   // sized for the fewest moduli the launch may compute, so every cluster
   // has at least one item whatever count the device chooses
   const int64_t singles =

@@ -54,7 +54,8 @@ bool rows_layout(const ResidueOperand& o, int bf16) {
   // 8-byte (bf16) aligned
   const uintptr_t vec = bf16 ? 8 : 16;
   return o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
-         (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0;
+         (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0 &&
+         (o.group_rows <= 0 || (o.group_stride * (bf16 ? 2 : 4)) % int64_t(vec) == 0);
 }
 
 constexpr int kThreads = 256;
@@ -284,7 +285,7 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
 // zero residues.
 constexpr int kFusedRuns = kFusedK / (4 * kThreads);
 
-template <int kBf16, int P>
+template <int kBf16, int P, bool kGrouped>
 __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand o0, ResidueOperand o1,
                                                                   unsigned split, FusedBand fb) {
   const bool second = blockIdx.x >= split;
@@ -292,6 +293,8 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   const int64_t r = second ? blockIdx.x - split : blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31;
   const bool live_row = r < o.rows;
+  // (a strided batch's rows: groups of group_rows at group_stride)
+  const int64_t row0 = kGrouped ? (live_row ? operand_row_offset(o, r) : 0) : r * o.ld;
   uint32_t bits[kFusedRuns][4];
   int key = 0;
 #pragma unroll
@@ -303,14 +306,14 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       if (k + 4 <= o.K) {
         if (kBf16) {
           const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(o.X) +
-                                                               r * o.ld + k));
+                                                               row0 + k));
           bits[v][0] = w.x << 16;
           bits[v][1] = w.x & 0xFFFF0000u;
           bits[v][2] = w.y << 16;
           bits[v][3] = w.y & 0xFFFF0000u;
         } else {
           const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(o.X) +
-                                                               r * o.ld + k));
+                                                               row0 + k));
           bits[v][0] = w.x;
           bits[v][1] = w.y;
           bits[v][2] = w.z;
@@ -319,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       } else {
 #pragma unroll
         for (int h = 0; h < 4; ++h)
-          if (k + h < o.K) bits[v][h] = load_bits<kBf16>(o.X, r * o.ld + k + h);
+          if (k + h < o.K) bits[v][h] = load_bits<kBf16>(o.X, row0 + k + h);
       }
     }
 #pragma unroll
@@ -694,8 +697,8 @@ __device__ __forceinline__ void write_window(int64_t* out, int64_t MN, const Dig
 // window; rebuilds the exact value as 18 int64 digits and writes it.
 template <int kBf16>
 __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArgs& ra, int64_t m,
-                                               int64_t n, W192 t, int E, bool wide, __int128 S,
-                                               int emA, int64_t nf) {
+                                               int64_t n, int64_t sb, W192 t, int E, bool wide,
+                                               __int128 S, int emA, int64_t nf) {
   const int64_t MN = g.M * g.N;
   int64_t d[kDigits];
 #pragma unroll
@@ -709,19 +712,19 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
     s0.w[2] = static_cast<uint64_t>(S >> 64);
     add_w192_to_digits(d, s0, E + kLsbBias);
     const int na = min(ra.countA[m], ra.cap);
-    const int nb = min(ra.countB[n], ra.cap);
+    const int nb = min(ra.countB[sb], ra.cap);
     for (int q = 0; q < na; ++q) {
       const uint2 ent = ra.listA[m * ra.cap + q];
       const int64_t k = ent.x;
       const Decoded a = decode_f32_bits(ent.y);
-      const Decoded b = decode_f32_bits(load_bits<kBf16>(g.B, g.opB ? k * g.ldb + n : n * g.ldb + k));
+      const Decoded b = decode_f32_bits(load_bits<kBf16>(g.B, b_offset(g, sb, k)));
       if (!a.nonfinite && !b.nonfinite) add_product(d, a.m, a.e, b.m, b.e);
     }
     for (int q = 0; q < nb; ++q) {
-      const uint2 ent = ra.listB[n * ra.cap + q];
+      const uint2 ent = ra.listB[sb * ra.cap + q];
       const int64_t k = ent.x;
       const Decoded b = decode_f32_bits(ent.y);
-      const Decoded a = decode_f32_bits(load_bits<kBf16>(g.A, g.opA ? k * g.lda + m : m * g.lda + k));
+      const Decoded a = decode_f32_bits(load_bits<kBf16>(g.A, a_offset(g, m, k)));
       if (a.nonfinite || (a.m != 0 && a.e - emA + kDeepGap < 0)) continue;
       if (!b.nonfinite) add_product(d, a.m, a.e, b.m, b.e);
     }
@@ -737,7 +740,7 @@ __device__ __noinline__ void output_via_digits(const GemmArgs& g, const ReconArg
     out[kDigits * MN] = g.K;
     out[(kDigits + 1) * MN] = nf;
   } else {
-    reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_to_f32_bits(w, top);
+    reinterpret_cast<uint32_t*>(g.C)[c_row_offset(g, m) + n] = nf ? kNanBits : round_to_f32_bits(w, top);
   }
 }
 
@@ -847,15 +850,16 @@ __device__ __forceinline__ uint32_t round_s128(uint64_t lo, uint64_t hi, int E) 
 // digit route).  nf counts products with a non-finite operand.
 template <int kBf16>
 __device__ __noinline__ bool add_deep_products(const GemmArgs& g, const ReconArgs& ra, int64_t m,
-                                               int64_t n, int emA, int E, W192& t, int64_t& nf) {
+                                               int64_t sb, int emA, int E, W192& t, int64_t& nf) {
+  // sb: B's row of the output's column (its stacked row in a strided batch)
   bool fits = true;
   const int na = min(ra.countA[m], ra.cap);
-  const int nb = min(ra.countB[n], ra.cap);
+  const int nb = min(ra.countB[sb], ra.cap);
   for (int q = 0; q < na; ++q) {                 // row m of A's deep elements x column n of B
     const uint2 ent = ra.listA[m * ra.cap + q];
     const int64_t k = ent.x;
     const Decoded a = decode_f32_bits(ent.y);
-    const Decoded b = decode_f32_bits(load_bits<kBf16>(g.B, g.opB ? k * g.ldb + n : n * g.ldb + k));
+    const Decoded b = decode_f32_bits(load_bits<kBf16>(g.B, b_offset(g, sb, k)));
     if (a.nonfinite || b.nonfinite) {
       ++nf;
     } else if (a.m != 0 && b.m != 0) {
@@ -865,10 +869,10 @@ __device__ __noinline__ bool add_deep_products(const GemmArgs& g, const ReconArg
     }
   }
   for (int q = 0; q < nb; ++q) {                 // column n of B's deep elements x shallow row m
-    const uint2 ent = ra.listB[n * ra.cap + q];
+    const uint2 ent = ra.listB[sb * ra.cap + q];
     const int64_t k = ent.x;
     const Decoded b = decode_f32_bits(ent.y);
-    const Decoded a = decode_f32_bits(load_bits<kBf16>(g.A, g.opA ? k * g.lda + m : m * g.lda + k));
+    const Decoded a = decode_f32_bits(load_bits<kBf16>(g.A, a_offset(g, m, k)));
     if (a.nonfinite || (a.m != 0 && a.e - emA + kDeepGap < 0)) continue;   // row m's list had it
     if (b.nonfinite) {
       ++nf;
@@ -899,7 +903,7 @@ constexpr int kReconCols = 4;                       // outputs per thread (one r
 
 // Fast path: det_gemm outputs whose row of A and column of B hold no deep
 // element -- CRT, then one rounding.  Nothing else, to keep registers low.
-template <int kBf16, int P>
+template <int kBf16, int P, bool kGrouped>
 __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const ReconArgs& ra) {
   const int64_t MN = g.M * g.N;
   const int64_t tiles_n = (g.N + kTile - 1) / kTile;
@@ -909,25 +913,33 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
   const int ncols = g.N - n0 < kReconCols ? static_cast<int>(g.N - n0) : kReconCols;
   const bool vec_ok = ((MN & 3) == 0) && ((g.N & 3) == 0) &&
                       (reinterpret_cast<uintptr_t>(ra.res) & 3u) == 0;
-  // the thread's columns stay fixed: their deep flags and exponents once
+  // the thread's columns' deep flags and exponents: once, or (a strided
+  // batch) once per entry its rows reach
   uint32_t live = 0;                     // bit j: column n0 + j is reconstructed here
   int colE[kReconCols];
+  auto columns_of = [&](int64_t e) {
+    live = 0;
 #pragma unroll
-  for (int j = 0; j < kReconCols; ++j) {
-    colE[j] = 0;
-    if (j < ncols) {
-      const int64_t n = n0 + j;
-      if (ra.countB[n] == 0) live |= 1u << j;                     // else: deep kernel
-      int emB = ra.emaxB[n];
-      emB = emB == kEmaxEmpty ? 0 : emB;
-      colE[j] = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+    for (int j = 0; j < kReconCols; ++j) {
+      colE[j] = 0;
+      if (j < ncols) {
+        const int64_t n = e * g.N + n0 + j;                       // B's stacked row
+        if (ra.countB[n] == 0) live |= 1u << j;                   // else: deep kernel
+        int emB = ra.emaxB[n];
+        emB = emB == kEmaxEmpty ? 0 : emB;
+        colE[j] = emB - 2 * kDeepGap + (kBf16 ? 32 : 0);
+      }
     }
-  }
-  if (live == 0) return;
+  };
+  int64_t entry = 0;
+  if constexpr (kGrouped) entry = entry_div(ra.m_begin + int64_t(blockIdx.y), g.Me);
+  columns_of(entry);
+  if (!kGrouped && live == 0) return;
   // all four outputs of a row in one 16-byte store where the layout allows
   static_assert(kReconCols == 4, "one uint4 of outputs per row");
-  const bool store4 = live == (1u << kReconCols) - 1 && (g.ldc & 3) == 0 &&
-                      (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0;
+  const bool store4_ok = (g.ldc & 3) == 0 && (reinterpret_cast<uintptr_t>(g.C) & 15u) == 0 &&
+                         (!kGrouped || (g.strideC & 3) == 0);
+  const bool store4 = store4_ok && live == (1u << kReconCols) - 1;   // (fixed columns)
   const bool vec = vec_ok && ncols == kReconCols;
   auto load_row = [&](int64_t m, uint32_t (&packed)[kNumModuli]) {
     const int64_t base = m * g.N + n0;
@@ -947,6 +959,14 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
     }
   };
   auto finish_row = [&](int64_t m, const uint32_t (&packed)[kNumModuli]) {
+    if constexpr (kGrouped) {
+      const int64_t e = entry_div(m, g.Me);
+      if (e != entry) {
+        entry = e;
+        columns_of(e);
+      }
+      if (live == 0) return;
+    }
     if (ra.route[(m / kTile) * tiles_n + n0 / kTile]) return;     // general kernel's outputs
     if (ra.countA[m] != 0) return;                                // deep row: deep kernel
     int emA = ra.emaxA[m];
@@ -963,8 +983,8 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
       crt_s128<P>(r, slo, shi);
       if (!failed) out[j] = round_s128(slo, shi, emA + colE[j]);
     }
-    uint32_t* dst = reinterpret_cast<uint32_t*>(g.C) + m * g.ldc + n0;
-    if (store4) {
+    uint32_t* dst = reinterpret_cast<uint32_t*>(g.C) + (kGrouped ? c_row_offset(g, m) : m * g.ldc) + n0;
+    if (kGrouped ? store4_ok && live == (1u << kReconCols) - 1 : store4) {
       __stcs(reinterpret_cast<uint4*>(dst), make_uint4(out[0], out[1], out[2], out[3]));
     } else {
 #pragma unroll
@@ -987,11 +1007,12 @@ __device__ __forceinline__ void reconstruct_fast_body(const GemmArgs& g, const R
 
 // The launch is compiled for the planes' count P and runs the body for the
 // band's count (ReconArgs::used).
-template <int kBf16, int P>
+template <int kBf16, int P, bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 4) reconstruct_fast_kernel(GemmArgs g, ReconArgs ra) {
   if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
-  with_used_planes<kBf16, P>(ra.used ? *ra.used : P,
-                             [&](auto Q) { reconstruct_fast_body<kBf16, decltype(Q)::value>(g, ra); });
+  with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
+    reconstruct_fast_body<kBf16, decltype(Q)::value, kGrouped>(g, ra);
+  });
 }
 
 // Outputs with deep entries: every output of a deep row, then every output of
@@ -1008,23 +1029,37 @@ __device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const R
   const int64_t n_rows = (parts & kDeepRows) ? nrc[0] : 0;
   const int64_t n_cols = (parts & kDeepCols) ? nrc[1] : 0;
   const int64_t band = ra.m_end - ra.m_begin;
-  const int64_t part1 = n_rows * g.N, total = part1 + band * n_cols;
+  // the deep-column part walks, per listed column, the band's rows; in a
+  // strided batch the listed columns are B's stacked rows e * N + n, and
+  // only entry e's rows (those in the band) take them
+  const bool grouped = g.batch > 1;
+  const int64_t col_rows = grouped ? g.Me : band;
+  const int64_t part1 = n_rows * g.N, total = part1 + col_rows * n_cols;
   for (int64_t idx = int64_t(blockIdx.x) * kThreads + threadIdx.x; idx < total;
        idx += int64_t(gridDim.x) * kThreads) {
-    int64_t m, n;
+    int64_t m, n, sb;
     if (idx < part1) {
       m = rows[idx / g.N];
       if (m < ra.m_begin || m >= ra.m_end) continue;              // another band's row
       n = idx - (idx / g.N) * g.N;
+      sb = brow_of(g, m, n);
     } else {
       const int64_t j = idx - part1;
       const int64_t mb = j / n_cols;
-      m = ra.m_begin + mb;
-      n = cols[j - mb * n_cols];
+      sb = cols[j - mb * n_cols];
+      if (grouped) {
+        const int64_t e = entry_div(sb, g.N);
+        n = sb - e * g.N;
+        m = e * g.Me + mb;
+        if (m < ra.m_begin || m >= ra.m_end) continue;            // another band's entry
+      } else {
+        m = ra.m_begin + mb;
+        n = sb;
+      }
       if (ra.countA[m] != 0) continue;                          // done with its deep row
     }
     if (ra.route[(m / kTile) * tiles_n + n / kTile]) continue;  // general kernel's output
-    int emA = ra.emaxA[m], emB = ra.emaxB[n];
+    int emA = ra.emaxA[m], emB = ra.emaxB[sb];
     emA = emA == kEmaxEmpty ? 0 : emA;
     emB = emB == kEmaxEmpty ? 0 : emB;
     int32_t r[kNumModuli];
@@ -1038,15 +1073,15 @@ __device__ __forceinline__ void reconstruct_deep_body(const GemmArgs& g, const R
     t.w[1] = slo;
     t.w[2] = shi;
     int64_t nf = 0;
-    const bool fits = add_deep_products<kBf16>(g, ra, m, n, emA, E, t, nf);
+    const bool fits = add_deep_products<kBf16>(g, ra, m, sb, emA, E, t, nf);
     if (failed) nf = 1;
     if (fits && g.P != nullptr) {
       write_canonical_digits(g.P + m * g.N + n, MN, t, E, g.K, nf);
     } else if (fits) {
-      reinterpret_cast<uint32_t*>(g.C)[m * g.ldc + n] = nf ? kNanBits : round_w192(t, E);
+      reinterpret_cast<uint32_t*>(g.C)[c_row_offset(g, m) + n] = nf ? kNanBits : round_w192(t, E);
     } else {
       const __int128 S = static_cast<__int128>((static_cast<unsigned __int128>(shi) << 64) | slo);
-      output_via_digits<kBf16>(g, ra, m, n, t, E, true, S, emA, nf);
+      output_via_digits<kBf16>(g, ra, m, n, sb, t, E, true, S, emA, nf);
     }
   }
 }
@@ -1457,9 +1492,13 @@ cudaError_t launch_residues_fused(const ResidueOperand& o0, const ResidueOperand
   if (b0 + b1 == 0 || b0 + b1 > 0x7FFFFFFF) return cudaErrorInvalidValue;
   const dim3 grid(static_cast<unsigned>(b0 + b1));
   const ResidueOperand& second = o1 != nullptr ? *o1 : o0;
+  const bool grouped = o0.group_rows > 0 || second.group_rows > 0;
   const cudaError_t e = with_planes(bf16, nplanes, [&](auto B, auto P) {
-    residue_fused_kernel<decltype(B)::value, decltype(P)::value>
-        <<<grid, kThreads, 0, stream>>>(o0, second, static_cast<unsigned>(b0), fb);
+    constexpr int kB = decltype(B)::value, kP = decltype(P)::value;
+    if (grouped)
+      residue_fused_kernel<kB, kP, true><<<grid, kThreads, 0, stream>>>(o0, second, static_cast<unsigned>(b0), fb);
+    else
+      residue_fused_kernel<kB, kP, false><<<grid, kThreads, 0, stream>>>(o0, second, static_cast<unsigned>(b0), fb);
     return cudaSuccess;
   });
   if (e != cudaSuccess) return e;
@@ -1585,7 +1624,9 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
     dim3 grid(static_cast<unsigned>((g.N + cols_per_block - 1) / cols_per_block),
               static_cast<unsigned>(band < 1024 ? band : 1024));
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
-      reconstruct_fast_kernel<decltype(B)::value, decltype(P)::value><<<grid, kThreads, 0, stream>>>(g, ra);
+      constexpr int kB = decltype(B)::value, kP = decltype(P)::value;
+      if (g.batch > 1) reconstruct_fast_kernel<kB, kP, true><<<grid, kThreads, 0, stream>>>(g, ra);
+      else reconstruct_fast_kernel<kB, kP, false><<<grid, kThreads, 0, stream>>>(g, ra);
       return cudaSuccess;
     });
   }

@@ -176,6 +176,12 @@ int det_pipe_benchmark_threads_per_block(void);
  * kernels, which callers whose data is known to span few binades may prefer. */
 int det_set_wide_path(int enable);
 
+/* Strided batches (det_gemm_strided_batched) as one pipeline where their
+ * shapes allow (1, the default) or entry by entry (0); returns the previous
+ * setting.  The results are the same bytes; the switch exists so that the
+ * two can be timed against each other. */
+int det_set_batched_pipeline(int enable);
+
 /* Diagnostic for tests and benchmarks: how the most recent residue-path
  * det_gemm / det_gemm_partial call on the current device routed its 64x64
  * output tiles.  out[0] = all tiles, out[1] = tiles the narrow residue path
@@ -336,7 +342,17 @@ det_status det_linear_bias_grad(int64_t batch, int64_t out_features, const float
  * references (section "References"), whose per-head attention products are
  * batches of small independent GEMMs.  Each C_b is bitwise the det_gemm of
  * its operands.  The C_b must not overlap.  Negative strides return
- * DET_ERR_SHAPE.  Entries are enqueued one after another on `stream`.
+ * DET_ERR_SHAPE.
+ *
+ * Where M and N are multiples of 64 and both operands are K-contiguous
+ * (opA = opB = 0) with rows the fused residue kernel reads by vector loads
+ * (K <= 4096; A, B, lda, ldb, strideA and strideB 16-byte multiples for f32,
+ * 8-byte for bf16), every entry runs in ONE residue-path pipeline: the
+ * entries' rows are stacked, each output tile is computed from its own
+ * entry's operands only, and one set of launches serves the batch (scratch
+ * from the memory pool grows with batch * (M + N) rows).  Other shapes, or
+ * det_set_batched_pipeline(0), enqueue the entries one after another on
+ * `stream`.  Either way each C_b is bitwise the same.
  */
 det_status det_gemm_strided_batched(det_dtype dtype, int64_t batch, int64_t M, int64_t N,
                                     int64_t K, const void* A, int64_t lda, int opA,
