@@ -841,6 +841,34 @@ def measure_workloads(args, dev, pipes=None, with_cpu=True):
         entry(f"c5_step_shards{shards}", f"MLP 1024->4096->1024 training step, batch 256, "
               f"k_shards={shards}, seed 7", timed(step), 7 * 2.0 * 256 * 1024 * 4096,
               cpu if shards == 1 else None)
+    del l1, l2, t1d, t2d, xb
+    # strided batch: 64 attention-like heads of 128 x 128 x 4096, one pipeline
+    # against the same entries enqueued one after another
+    lib = dg.library()
+    nb, mb, kb = 64, 128, 4096
+    Ab, Bb = wl.normal_f32((nb, mb, kb), 61, 0), wl.normal_f32((nb, mb, kb), 61, 1)
+    xb3, wb3 = f32(Ab), f32(Bb)
+    outb = torch.empty((nb, mb, mb), dtype=torch.float32, device=dev)
+    call = lambda: dg.det_gemm_batched(xb3, wb3, out=outb)
+    fl = 2.0 * nb * mb * mb * kb
+
+    def launches(fn):
+        torch.cuda.synchronize(dev)
+        n0 = lib.det_kernel_launches()
+        fn()
+        torch.cuda.synchronize(dev)
+        return int(lib.det_kernel_launches() - n0)
+    n_pipe, t_pipe = launches(call), timed(call)
+    prev = lib.det_set_batched_pipeline(0)
+    n_loop, t_loop = launches(call), timed(call)
+    lib.det_set_batched_pipeline(prev)
+    cpu = oracle_time(lambda: oracle.gemm(Ab[0], Bb[0], nthreads=cores), mb * mb * kb, cores,
+                      "one of the 64 entries (each costs the same)") if with_cpu else None
+    entry("batched_64x128x128x4096", "det_gemm_strided_batched f32, 64 entries of 128x128x4096 "
+          "N(0,1), seed 61", t_pipe, fl, cpu, launches=n_pipe,
+          entry_by_entry={"ms": round(t_loop, 4), "exact_gflops": round(fl / (t_loop * 1e-3) / 1e9, 2),
+                          "launches": n_loop},
+          speedup=round(t_loop / t_pipe, 2))
     return out
 
 

@@ -87,6 +87,9 @@ struct ResidueOperand {
   const void* X;
   int64_t ld;
   int op;
+  int32_t group_rows = 0;     // > 0: the rows are groups of group_rows (a strided batch's
+                              //   entries), group g starting g * group_stride elements on
+                              //   (both 32-bit and in padding: the operand keeps its size)
   int64_t rows;
   int64_t K;
   int64_t Kp;                 // K rounded up to kStageK (zero padded)
@@ -96,21 +99,21 @@ struct ResidueOperand {
   int* list_count;            // [rows], zeroed before the launch
   uint2* list;                // [rows][cap]: (k, raw bits) of deep / non-finite elements
   int cap;
+  int32_t group_stride = 0;
   unsigned long long* norm;   // [rows], zeroed before the launch: an upper bound of
                               // sum_k X_int^2 / 2^norm_shift over the row's shallow elements
   unsigned* keymax;           // fused kernel: [rows], zeroed (row maxima of exponent keys)
   unsigned long long* norm_max;  // fused kernel: zeroed slot for the largest norm of these rows
   unsigned* dmax;             // fused kernel: [rows/64], zeroed: largest deep count of each
                               //   64-row block (or null)
-  int64_t group_rows = 0;     // > 0: the rows are groups of group_rows (a strided batch's
-  int64_t group_stride = 0;   //   entries), group g starting g * group_stride elements on
 };
+static_assert(sizeof(ResidueOperand) == 15 * 8, "the group fields sit in padding");
 
 // Element offset of an operand's row r (K-contiguous or not).
 __host__ __device__ inline int64_t operand_row_offset(const ResidueOperand& o, int64_t r) {
   if (o.group_rows <= 0) return r * o.ld;
   const int64_t g = entry_div(r, o.group_rows);      // grouped rows stay below 2^30
-  return g * o.group_stride + (r - g * o.group_rows) * o.ld;
+  return g * int64_t(o.group_stride) + (r - g * o.group_rows) * o.ld;
 }
 
 // Thresholds of the moduli choice: P moduli suffice for a row band whose
@@ -248,21 +251,44 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
 __host__ __device__ inline int64_t gemm_b_rows(const ResGemmArgs& a) {
   return a.entry_rows > 0 ? (a.entry0 + a.M / a.entry_rows) * a.N : a.N;
 }
-// Output tiles of TM x TN of a launch: the whole M x N, or each entry's own.
-template <int TM, int TN>
-__host__ __device__ inline int64_t gemm_tiles(const ResGemmArgs& a) {
+// Entries a TM x TN tile packs (a strided batch whose entries' rows and
+// columns both divide the tile's): tile k takes entries kG .. kG + G - 1, A's
+// rows and B's rows of those entries side by side, and only the diagonal
+// blocks (an entry's rows with its own columns) are outputs.  1: one entry
+// per tile.
+template <int TM, int TN, bool kGrouped = true>
+__host__ __device__ inline int64_t gemm_pack(const ResGemmArgs& a) {
+  if (!kGrouped || a.entry_rows <= 0 || a.entry_rows > TM || a.N > TN || TM % a.entry_rows != 0 ||
+      TN % a.N != 0)
+    return 1;
+  const int64_t gm = TM / a.entry_rows, gn = TN / a.N;
+  return gm < gn ? gm : gn;
+}
+// Output tiles of TM x TN of a launch: the whole M x N, or each entry's own
+// (pack entries per tile where they fit).
+template <int TM, int TN, bool kGrouped = true>
+__host__ __device__ inline int64_t gemm_tiles(const ResGemmArgs& a, int64_t pack) {
   const int64_t tn = (a.N + TN - 1) / TN;
-  if (a.entry_rows > 0) return (a.M / a.entry_rows) * ((a.entry_rows + TM - 1) / TM) * tn;
-  return ((a.M + TM - 1) / TM) * tn;
+  if (!kGrouped || a.entry_rows <= 0) return ((a.M + TM - 1) / TM) * tn;
+  const int64_t entries = a.M / a.entry_rows;
+  if (pack > 1) return (entries + pack - 1) / pack;
+  return entries * ((a.entry_rows + TM - 1) / TM) * tn;
 }
 // Tile t: its first row of A (in the launch), first row of B's planes, first
 // output column, and the end of its rows' entry (rows from there on are
-// another entry's, or past M: computed but not written).
-template <int TM, int TN>
-__host__ __device__ inline void gemm_tile(const ResGemmArgs& a, int64_t t, int64_t& m0, int64_t& nb0,
-                                          int64_t& n0, int64_t& m_end) {
+// another entry's, or past M: computed but not written).  A packed tile's
+// first column is 0 and m_end the end of its last entry.
+// (kGrouped false: the plain tiling, whatever the arguments hold)
+template <int TM, int TN, bool kGrouped = true>
+__host__ __device__ inline void gemm_tile(const ResGemmArgs& a, int64_t pack, int64_t t, int64_t& m0,
+                                          int64_t& nb0, int64_t& n0, int64_t& m_end) {
   const int64_t tn = (a.N + TN - 1) / TN;
-  if (a.entry_rows > 0) {
+  if (kGrouped && a.entry_rows > 0 && pack > 1) {
+    m0 = t * pack * a.entry_rows;
+    n0 = 0;
+    nb0 = (a.entry0 + t * pack) * a.N;
+    m_end = m0 + pack * a.entry_rows < a.M ? m0 + pack * a.entry_rows : a.M;
+  } else if (kGrouped && a.entry_rows > 0) {
     const int64_t tm = (a.entry_rows + TM - 1) / TM;
     const int64_t e = t / (tm * tn), r = t - e * (tm * tn);
     const int64_t i = r / tn;

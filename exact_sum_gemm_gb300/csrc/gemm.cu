@@ -58,6 +58,32 @@ cudaError_t device_pool(cudaMemPool_t* out) {
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+ResidueOperand residue_operand(const void* X, int64_t ld, int op, int64_t rows, int64_t K, int64_t Kp,
+                               int* emax, __nv_bfloat16* planes, int* list_count, uint2* list,
+                               int cap, unsigned long long* norm, unsigned* keymax,
+                               unsigned long long* norm_max, unsigned* dmax, int64_t group_rows,
+                               int64_t group_stride) {
+  ResidueOperand o{};
+  o.X = X;
+  o.ld = ld;
+  o.op = op;
+  o.rows = rows;
+  o.K = K;
+  o.Kp = Kp;
+  o.emax = emax;
+  o.planes = planes;
+  o.list_count = list_count;
+  o.list = list;
+  o.cap = cap;
+  o.norm = norm;
+  o.keymax = keymax;
+  o.norm_max = norm_max;
+  o.dmax = dmax;
+  o.group_rows = static_cast<int32_t>(group_rows);      // (below 2^30 where grouped)
+  o.group_stride = static_cast<int32_t>(group_stride);  // (below 2^31 where grouped)
+  return o;
+}
 // 64-row blocks of A plus 64-row blocks of B's per-row arrays (a strided
 // batch's entries have N a multiple of 64, so no block spans two entries)
 int64_t tiles_mn(const GemmArgs& g) {
@@ -377,12 +403,14 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
   // band (no separate pre-pass over A and B)
   // (a strided batch: B's operand is every entry's rows, stacked)
   const bool grouped = g.batch > 1;
-  const ResidueOperand rb{g.B, g.ldb, g.opB, nbr, g.K, Kp, s.emaxB, planesB, counts + g.M, listB, cap,
-                          norms + g.M, keymax + g.M, maxima + 1, dmax + tiles_m,
-                          grouped ? g.N : 0, grouped ? g.strideB : 0};
-  ResidueOperand whole_a{g.A, g.lda, g.opA, g.M, g.K, Kp};
-  whole_a.group_rows = grouped ? g.Me : 0;
-  whole_a.group_stride = grouped ? g.strideA : 0;
+  const ResidueOperand rb = residue_operand(g.B, g.ldb, g.opB, nbr, g.K, Kp, s.emaxB, planesB,
+                                             counts + g.M, listB, cap, norms + g.M, keymax + g.M,
+                                             maxima + 1, dmax + tiles_m, grouped ? g.N : 0,
+                                             grouped ? g.strideB : 0);
+  const ResidueOperand whole_a = residue_operand(g.A, g.lda, g.opA, g.M, g.K, Kp, nullptr, nullptr,
+                                                 nullptr, nullptr, 0, nullptr, nullptr, nullptr,
+                                                 nullptr, grouped ? g.Me : 0,
+                                                 grouped ? g.strideA : 0);
   const bool fused = fused_residues_ok(rb, g.bf16) && fused_residues_ok(whole_a, g.bf16);
   if (grouped && !fused) return cudaErrorInvalidValue;   // the caller checks batched_residue_ok
   {
@@ -405,10 +433,11 @@ cudaError_t run_residue_path(const GemmArgs& g, char* base, const ResidueScratch
     // (a strided batch's bands start on an entry: rows m0.. are entry m0 / Me's)
     const void* X = static_cast<const char*>(g.A) +
                     (grouped ? (m0 / g.Me) * g.strideA : (g.opA ? m0 : m0 * g.lda)) * es;
-    return ResidueOperand{X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
-                          planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
-                          counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0, maxima + 4 * b,
-                          dmax + m0 / kTile, grouped ? g.Me : 0, grouped ? g.strideA : 0};
+    return residue_operand(X, g.lda, g.opA, rows, g.K, Kp, s.emaxA + m0,
+                           planesA + (m0 / kPlaneRows) * nkb * nplanes * kPlaneRows * kStageK,
+                           counts + m0, listA + m0 * cap, cap, norms + m0, keymax + m0,
+                           maxima + 4 * b, dmax + m0 / kTile, grouped ? g.Me : 0,
+                           grouped ? g.strideA : 0);
   };
   // the band's moduli count, once its rows' and B's norm bounds are complete
   auto moduli_of_band = [&](int b) {
@@ -591,12 +620,12 @@ bool batched_residue_ok(const GemmArgs& g) {
   if (g.M > (int64_t(1) << 30) || rows_of_b(g) > (int64_t(1) << 30)) return false;
   if (g.strideA < 0 || g.strideB < 0 || g.strideC < 0) return false;
   if (residue_planes_needed(g) <= 0) return false;
-  ResidueOperand a{g.A, g.lda, g.opA, g.M, g.K, 0};
-  a.group_rows = g.Me;
-  a.group_stride = g.strideA;
-  ResidueOperand b{g.B, g.ldb, g.opB, rows_of_b(g), g.K, 0};
-  b.group_rows = g.N;
-  b.group_stride = g.strideB;
+  const ResidueOperand a = residue_operand(g.A, g.lda, g.opA, g.M, g.K, 0, nullptr, nullptr, nullptr,
+                                           nullptr, 0, nullptr, nullptr, nullptr, nullptr, g.Me,
+                                           g.strideA);
+  const ResidueOperand b = residue_operand(g.B, g.ldb, g.opB, rows_of_b(g), g.K, 0, nullptr, nullptr,
+                                           nullptr, nullptr, 0, nullptr, nullptr, nullptr, nullptr,
+                                           static_cast<int32_t>(g.N), g.strideB);
   return fused_residues_ok(a, g.bf16) && fused_residues_ok(b, g.bf16);
 }
 

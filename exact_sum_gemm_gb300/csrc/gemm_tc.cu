@@ -73,6 +73,7 @@ __device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
   tt = J - c * T;
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, ResGemmArgs a) {
@@ -90,7 +91,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   // work units: (modulus, pair of neighbouring output tiles), modulus-major so
   // that the CTAs in flight share one plane of A and one of B in L2
-  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a);   // (a strided batch: each entry's own)
+  // (a strided batch: each entry's own tiles, or several entries per tile)
+  const int64_t pack = gemm_pack<kBlockM, kBlockN, kGrouped>(a);
+  const int64_t tiles = gemm_tiles<kBlockM, kBlockN, kGrouped>(a, pack);
   const int64_t tile_pairs = (tiles + 1) / 2;
   const int64_t units = tile_pairs * planes_used(a);
   if (units == 0) return;                  // nothing to compute: leave before any set-up
@@ -138,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tt, c;
         job_at(J, T, tt, c);
         int64_t m0, nb0, n0, m_end;
-        gemm_tile<kBlockM, kBlockN>(a, t0 + tt, m0, nb0, n0, m_end);
+        gemm_tile<kBlockM, kBlockN, kGrouped>(a, pack, t0 + tt, m0, nb0, n0, m_end);
         const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
         for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -226,8 +229,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tt, c;
       job_at(J, T, tt, c);
       int64_t m0, nb0, n0, m_end;
-      gemm_tile<kBlockM, kBlockN>(a, t0 + tt, m0, nb0, n0, m_end);
+      gemm_tile<kBlockM, kBlockN, kGrouped>(a, pack, t0 + tt, m0, nb0, n0, m_end);
       const int64_t row = m0 + 32 * g + lane;
+      // a packed tile: this row's entry within the tile (only its own columns)
+      const int64_t row_entry = pack > 1 ? entry_div(row - m0, a.entry_rows) : 0;
       const int acc = tt;
       if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
         ok = false;
@@ -250,10 +255,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           v[j] = __float_as_uint(near_mod_f32(__uint_as_float(v[j]), p, inv_p));
         if (!last) {
           ptx::tmem_st32(taddr, v);
-        } else if (row < m_end) {
+        } else if (row < m_end &&
+                     (pack <= 1 || entry_div(n0 + cb * 32, a.N) == row_entry)) {
           // a second reduction makes the residue balanced (|r| <= 127); its
           // byte is the low byte of the pattern of r + 1.5*2^23
-          int8_t* out = a.res + u * a.res_plane + row * a.N + n0 + cb * 32;
+          const int64_t col = n0 + cb * 32 - row_entry * a.N;   // (0 unless packed)
+            int8_t* out = a.res + u * a.res_plane + row * a.N + col;
           uint32_t packed[8];
 #pragma unroll
           for (int j4 = 0; j4 < 8; ++j4) {
@@ -266,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             packed[j4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040),
                                      0x5410);
           }
-          const int64_t n_left = a.N - (n0 + cb * 32);
+          const int64_t n_left = a.N - col;
           if (n_left >= 32 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
             reinterpret_cast<uint4*>(out)[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             reinterpret_cast<uint4*>(out)[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
@@ -339,8 +346,12 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
   static PerDeviceOnce configured;                 // the attribute is per device
   cudaError_t ce = configured.run([](int) {
-    return cudaFuncSetAttribute(residue_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(kSmemBytes));
+    cudaError_t r = cudaFuncSetAttribute(residue_gemm_kernel<false>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kSmemBytes));
+    return r != cudaSuccess ? r : cudaFuncSetAttribute(residue_gemm_kernel<true>,
+                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                       static_cast<int>(kSmemBytes));
   });
   if (ce != cudaSuccess) return ce;
   CUtensorMap tmA, tmB;
@@ -352,12 +363,13 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a);
+  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a, gemm_pack<kBlockM, kBlockN>(a));
   // sized for the fewest moduli the launch may compute (every CTA has a unit)
   const int64_t units = (tiles + 1) / 2 *
       (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  residue_gemm_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  if (a.entry_rows > 0) residue_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  else residue_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
   note_launch();
   return cudaGetLastError();
 }

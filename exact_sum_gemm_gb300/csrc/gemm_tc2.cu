@@ -73,6 +73,7 @@ __device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
   tt = J - c * T;
 }
 
+template <bool kGrouped>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, ResGemmArgs a) {
@@ -91,7 +92,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t cluster = blockIdx.x >> 1, clusters = gridDim.x >> 1;
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
-  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a);   // (a strided batch: each entry's own)
+  // (a strided batch: each entry's own tiles, or several entries per tile)
+  const int64_t pack = gemm_pack<kPairM, kTileN, kGrouped>(a);
+  const int64_t tiles = gemm_tiles<kPairM, kTileN, kGrouped>(a, pack);
   const int64_t singles = tiles * planes_used(a);  // (modulus, tile), modulus-major
   // a cluster with no item (a launch sized for more moduli than it computes)
   // issues no MMA, so it neither commits nor waits for the final commit
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           job_at(J, T, tt, c);
           int64_t t, m0, nb0, n0, m_end;
           single_at(sg[tt], u, t);
-          gemm_tile<kPairM, kTileN>(a, t, m0, nb0, n0, m_end);
+          gemm_tile<kPairM, kTileN, kGrouped>(a, pack, t, m0, nb0, n0, m_end);
           const int ga = static_cast<int>((m0 + kHalfM * rank) / kPlaneRows);
           const int gb = static_cast<int>((nb0 + (kTileN / 2) * rank) / kPlaneRows);
           const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
@@ -249,8 +252,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         job_at(J, T, tt, c);
         int64_t t, m0, nb0, n0, m_end;
         single_at(sg[tt], u, t);
-        gemm_tile<kPairM, kTileN>(a, t, m0, nb0, n0, m_end);
+        gemm_tile<kPairM, kTileN, kGrouped>(a, pack, t, m0, nb0, n0, m_end);
         const int64_t row = m0 + kHalfM * rank + 32 * g + lane;
+        // a packed tile: this row's entry within the tile (only its own columns)
+        const int64_t row_entry = pack > 1 ? entry_div(row - m0, a.entry_rows) : 0;
         const int acc = tt;
         if (!wait_bounded(&acc_ready[acc], uses[acc] & 1u)) {
           ok = false;
@@ -273,10 +278,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             v[j] = __float_as_uint(near_mod_f32(__uint_as_float(v[j]), p, inv_p));
           if (!last) {
             ptx::tmem_st32(taddr, v);
-          } else if (row < m_end) {
+          } else if (row < m_end &&
+                     (pack <= 1 || entry_div(n0 + cb * 32, a.N) == row_entry)) {
             // a second reduction makes the residue balanced; its byte is the
             // low byte of the pattern of r + 1.5*2^23
-            int8_t* out = a.res + u * a.res_plane + row * a.N + n0 + cb * 32;
+            const int64_t col = n0 + cb * 32 - row_entry * a.N;   // (0 unless packed)
+            int8_t* out = a.res + u * a.res_plane + row * a.N + col;
             uint32_t packed[8];
 #pragma unroll
             for (int j4 = 0; j4 < 8; ++j4) {
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               packed[j4] = __byte_perm(__byte_perm(b[0], b[1], 0x0040),
                                        __byte_perm(b[2], b[3], 0x0040), 0x5410);
             }
-            const int64_t n_left = a.N - (n0 + cb * 32);
+            const int64_t n_left = a.N - col;
             if (n_left >= 32 && (reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
               // evict-first: read once, by the reconstruction after the launch
               __stcs(reinterpret_cast<uint4*>(out), make_uint4(packed[0], packed[1], packed[2], packed[3]));
@@ -344,12 +351,16 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   cudaError_t e = queried.run([&](int d) {
     int n = 0, sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
-    cudaError_t r = cudaFuncSetAttribute(residue_gemm_pair_kernel,
+    cudaError_t r = cudaFuncSetAttribute(residue_gemm_pair_kernel<false>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
+    if (r == cudaSuccess)
+      r = cudaFuncSetAttribute(residue_gemm_pair_kernel<true>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(kSmemBytes));
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(static_cast<unsigned>(sms > 1 ? sms / 2 * 2 : 2), 1, 1);
-    if (r == cudaSuccess) r = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel, &q);
+    if (r == cudaSuccess) r = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<false>, &q);
     max_clusters[d] = (r == cudaSuccess && n > 0) ? n : -1;
     cudaGetLastError();                                 // a failed query is not the caller's error
     return cudaSuccess;
@@ -363,14 +374,17 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kHalfM) ||
       !make_plane_map(&tmB, a.B, gemm_b_rows(a), a.Kp, a.nplanes, kTileN / 2))
     return cudaErrorInvalidValue;
-  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a);
+  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a, gemm_pack<kPairM, kTileN>(a));
   // sized for the fewest moduli the launch may compute, so every cluster
   // has at least one item whatever count the device chooses
   const int64_t singles =
       tiles * (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const int64_t clusters = singles < max_clusters[dev] ? singles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel, tmA, tmB, a);
+  // (a strided batch's band: the entry-aware tiling, compiled apart so that
+  // plain launches keep their own register allocation)
+  e = a.entry_rows > 0 ? cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<true>, tmA, tmB, a)
+                       : cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<false>, tmA, tmB, a);
   note_launch();
   return e;
 }

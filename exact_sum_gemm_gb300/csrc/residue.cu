@@ -55,7 +55,7 @@ bool rows_layout(const ResidueOperand& o, int bf16) {
   const uintptr_t vec = bf16 ? 8 : 16;
   return o.op == 0 && (reinterpret_cast<uintptr_t>(o.X) % vec) == 0 &&
          (o.ld * (bf16 ? 2 : 4)) % int64_t(vec) == 0 &&
-         (o.group_rows <= 0 || (o.group_stride * (bf16 ? 2 : 4)) % int64_t(vec) == 0);
+         (o.group_rows <= 0 || (int64_t(o.group_stride) * (bf16 ? 2 : 4)) % int64_t(vec) == 0);
 }
 
 constexpr int kThreads = 256;
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   const int tid = threadIdx.x, lane = tid & 31;
   const bool live_row = r < o.rows;
   // (a strided batch's rows: groups of group_rows at group_stride)
-  const int64_t row0 = kGrouped ? (live_row ? operand_row_offset(o, r) : 0) : r * o.ld;
+  const int64_t row0 = kGrouped && live_row ? operand_row_offset(o, r) : 0;
   uint32_t bits[kFusedRuns][4];
   int key = 0;
 #pragma unroll
@@ -306,14 +306,14 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       if (k + 4 <= o.K) {
         if (kBf16) {
           const uint2 w = __ldg(reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(o.X) +
-                                                               row0 + k));
+                                                               (kGrouped ? row0 : r * o.ld) + k));
           bits[v][0] = w.x << 16;
           bits[v][1] = w.x & 0xFFFF0000u;
           bits[v][2] = w.y << 16;
           bits[v][3] = w.y & 0xFFFF0000u;
         } else {
           const uint4 w = __ldg(reinterpret_cast<const uint4*>(static_cast<const uint32_t*>(o.X) +
-                                                               row0 + k));
+                                                               (kGrouped ? row0 : r * o.ld) + k));
           bits[v][0] = w.x;
           bits[v][1] = w.y;
           bits[v][2] = w.z;
@@ -322,7 +322,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       } else {
 #pragma unroll
         for (int h = 0; h < 4; ++h)
-          if (k + h < o.K) bits[v][h] = load_bits<kBf16>(o.X, row0 + k + h);
+          if (k + h < o.K) bits[v][h] = load_bits<kBf16>(o.X, (kGrouped ? row0 : r * o.ld) + k + h);
       }
     }
 #pragma unroll

@@ -126,6 +126,24 @@ def test_two_small_entries_on_the_single_cta_kernel(oracle_mod):
         assert_bits_equal(bits_of(got[i]), np_bits(oracle_mod.gemm(A[i], B[i])), f"entry {i}")
 
 
+@pytest.mark.parametrize("batch,M,N,K", [(16, 64, 64, 512), (7, 128, 128, 1000), (5, 64, 128, 256)])
+def test_entries_packed_into_shared_tiles(oracle_mod, batch, M, N, K):
+    # entries smaller than a tile share it: four 64 x 64 entries per
+    # 256 x 256 tile, two 128 x 128 ones (seven entries: the last tile holds
+    # one), two 64 x 128 ones; only each entry's own block is an output
+    A = wl.normal_f32((batch, M, K), 67, 0)
+    B = wl.normal_f32((batch, N, K), 67, 1)
+    A[batch - 1, 0, 3] = np.float32(2e-9)                 # a deep row in the last entry
+    B[0, N - 1, 5] = np.float32(-3e-9)                    # a deep column in the first
+    a, b = dev_f32(A), dev_f32(B)
+    got, n = _launches(lambda: dg.det_gemm_batched(a, b))
+    assert n < 40, n
+    for i in range(batch):
+        assert_bits_equal(bits_of(got[i]), np_bits(oracle_mod.gemm(A[i], B[i])), f"entry {i}")
+    assert_bits_equal(bits_of(got), bits_of(_per_entry(lambda: dg.det_gemm_batched(a, b))),
+                      "against entry by entry")
+
+
 def test_switch_returns_the_previous_setting():
     lib = dg.library()
     assert lib.det_set_batched_pipeline(0) == 1
