@@ -1162,7 +1162,7 @@ __global__ void __launch_bounds__(kThreads, 4) partial_fast_kernel(GemmArgs g, R
 // a general tile (the general or wide kernel's outputs) is written output by
 // output instead.  Needs N a multiple of 16 and 16-byte aligned residues and
 // digit planes (every copy 16-byte aligned, every size a multiple of 128
-// bytes); 45 KB of shared memory, four blocks per SM.
+// bytes); 43 KB of shared memory, five blocks per SM.
 constexpr int kRing = 3;
 constexpr int kBulkCols = 128;
 constexpr int kPlanesOut = kDigits + 2;
@@ -1216,10 +1216,13 @@ __device__ __forceinline__ void window_to_smem_at(int64_t (*seg)[kBulkCols], int
 }
 
 struct BulkSmem {
-  int64_t seg[2][kPlanesOut][kBulkCols];      // 40 KB: two row segments of digit planes
+  int64_t seg[2][kDigits][kBulkCols];         // 36 KB: two row segments of digit planes
+  int64_t fixed[2][kBulkCols];                // planes 18 and 19 (K, the non-finite count):
+                                              //   the same in every segment of the call
   int8_t res[kRing][kNumModuli][kBulkCols];   // 5.25 KB: residue rows
   int meta[kRing][2];                         // deep count, exponent maximum of the row
 };
+constexpr int kBulkBlocksPerSm = 5;           // 43.3 KB each
 
 template <int kBf16, int P>
 __device__ __forceinline__ void partial_bulk_body(const GemmArgs& g, const ReconArgs& ra, BulkSmem& sm) {
@@ -1248,6 +1251,9 @@ __device__ __forceinline__ void partial_bulk_body(const GemmArgs& g, const Recon
   const int cu = t >> 3, cc = (t & 7) * 16;
   const bool copier = cu < P && cc < ncols;
   const int8_t* src = ra.res + cu * MN + n0 + cc;
+  sm.fixed[0][t] = g.K;
+  sm.fixed[1][t] = nf;
+  ptx::fence_proxy_async_smem();                // read by the bulk copies (after a barrier)
   auto issue = [&](int64_t m, int slot) {
     if (m < r1) {
       if (copier) cp_async16(&sm.res[slot][cu][cc], src + m * g.N);
@@ -1296,14 +1302,12 @@ __device__ __forceinline__ void partial_bulk_body(const GemmArgs& g, const Recon
       if (!general) {
         if (in_range) {
           window_to_smem_at(sm.seg[oslot], t, d);
-          sm.seg[oslot][kDigits][t] = g.K;
-          sm.seg[oslot][kDigits + 1][t] = nf;
           ptx::fence_proxy_async_smem();          // visible to the bulk copies
         }
         __syncthreads();
         if (t < kPlanesOut) {
-          ptx::bulk_store(g.P + t * MN + m * g.N + n0, &sm.seg[oslot][t][0],
-                          static_cast<uint32_t>(ncols) * 8u);
+          const int64_t* from = t < kDigits ? &sm.seg[oslot][t][0] : &sm.fixed[t - kDigits][0];
+          ptx::bulk_store(g.P + t * MN + m * g.N + n0, from, static_cast<uint32_t>(ncols) * 8u);
           ptx::bulk_commit();
         }
         oslot ^= 1;
@@ -1318,7 +1322,7 @@ __device__ __forceinline__ void partial_bulk_body(const GemmArgs& g, const Recon
 }
 
 template <int kBf16, int P>
-__global__ void __launch_bounds__(kBulkCols, 4) partial_bulk_kernel(GemmArgs g, ReconArgs ra) {
+__global__ void __launch_bounds__(kBulkCols, kBulkBlocksPerSm) partial_bulk_kernel(GemmArgs g, ReconArgs ra) {
   if (ra.used != nullptr && *ra.used == 0) return;   // every tile of the band is general
   __shared__ __align__(128) BulkSmem sm;
   with_used_planes<kBf16, P>(ra.used ? *ra.used : P, [&](auto Q) {
@@ -1593,18 +1597,19 @@ cudaError_t launch_reconstruct_fast(const GemmArgs& g, const ReconArgs& ra, cuda
                static_cast<unsigned>(band < 512 ? band : 512));
     // bulk copies where every row of residues and of digits starts 16-byte aligned
     const bool bulk = partial_bulk_ok(g, ra);
-    if (bulk) {                                   // four blocks per SM, each a chunk of rows
+    if (bulk) {                                   // five blocks per SM, each a chunk of rows
       int dev = 0, sms = 0;
       cudaGetDevice(&dev);
       cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
       pgrid.x = static_cast<unsigned>((g.N + kBulkCols - 1) / kBulkCols);
-      const int64_t per_col = (int64_t(sms > 0 ? sms : 1) * 4 + pgrid.x - 1) / pgrid.x;
+      const int64_t per_col =
+          (int64_t(sms > 0 ? sms : 1) * kBulkBlocksPerSm + pgrid.x - 1) / pgrid.x;
       pgrid.y = static_cast<unsigned>(band < per_col ? band : per_col);
     }
     e = with_planes(g.bf16, ra.nplanes, [&](auto B, auto P) {
       constexpr int kB = decltype(B)::value, kP = decltype(P)::value;
       if (bulk) {
-        static PerDeviceOnce carveout;            // four 45 KB blocks per SM
+        static PerDeviceOnce carveout;            // five 43 KB blocks per SM
         carveout.run([](int) {
           cudaFuncSetAttribute(partial_bulk_kernel<kB, kP>,
                                cudaFuncAttributePreferredSharedMemoryCarveout,
