@@ -60,6 +60,20 @@ bool rows_layout(const ResidueOperand& o, int bf16) {
 
 constexpr int kThreads = 256;
 constexpr int kTileRows = 32;
+
+// A row's deep-element list slot.  The count saturates a little past the
+// list's capacity: once a row holds more deep elements than its list takes,
+// every tile of the row goes to the general tiles, and every reader of the
+// count only asks whether it exceeds the capacity (or is nonzero), so further
+// increments are skipped.  Without this, data whose elements are nearly all
+// deep (exponents spread over hundreds of binades) piled millions of atomic
+// increments onto a few hundred counters.  Returns the slot taken, or a value
+// past the capacity when none was taken.
+__device__ __forceinline__ int take_deep_slot(int* count, int cap) {
+  if (__ldcg(count) > cap) return cap + 1;
+  return atomicAdd(count, 1);
+}
+
 constexpr int kTileK = 64;
 
 // Reduction modulo a compile-time modulus (near_mod_f32 states the bounds).
@@ -174,7 +188,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, Re
       x[h] = static_cast<float>(deep ? 0 : mi);                        // exact: |mi| < 2^24
       pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);  // 2^s, s in [0, 18]
       if (deep && gk + h < o.K && gr < o.rows) {
-        const int slot = atomicAdd(o.list_count + gr, 1);
+        const int slot = take_deep_slot(o.list_count + gr, o.cap);
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits);
       }
     }
@@ -259,7 +273,7 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
       x[h] = static_cast<float>(deep ? 0 : mi);
       pw[h] = __int_as_float((deep || d.m == 0 ? 127 : s + 127) << 23);
       if (deep && gk + h < o.K && gr < o.rows) {
-        const int slot = atomicAdd(o.list_count + gr, 1);
+        const int slot = take_deep_slot(o.list_count + gr, o.cap);
         if (slot < o.cap) o.list[gr * o.cap + slot] = make_uint2(static_cast<uint32_t>(gk + h), bits[h]);
       }
     }
@@ -352,7 +366,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       x[h] = static_cast<float>(deep ? 0 : mi);
       pw[h] = __int_as_float((deep || d.m == 0 ? 127 : sh + 127) << 23);
       if (deep && k + h < o.K && live_row) {
-        const int slot = atomicAdd(o.list_count + r, 1);
+        const int slot = take_deep_slot(o.list_count + r, o.cap);
         if (slot < o.cap) o.list[r * o.cap + slot] = make_uint2(static_cast<uint32_t>(k + h), bits[v][h]);
         deep_seen = max(deep_seen, slot + 1);
       }
