@@ -74,6 +74,19 @@ __device__ __forceinline__ int take_deep_slot(int* count, int cap) {
   return atomicAdd(count, 1);
 }
 
+// Whether every row of a block's 32 is past its deep list's capacity: such a
+// row is general on every tile (the routing sends each tile holding it to the
+// general tiles), so nothing the planes kernels would write for it -- its
+// residues, list entries, norm -- is read again; padding rows are read only
+// for outputs past M or N.  The two-pass kernels, whose blocks each take one
+// 64-k stage of 32 rows, skip such blocks (data whose rows are nearly all
+// deep elements, such as exponents spread over hundreds of binades).
+__device__ __forceinline__ bool rows_past_capacity(const ResidueOperand& o, int64_t r0) {
+  const int64_t gr = r0 + threadIdx.x;
+  const int past = threadIdx.x >= kTileRows || gr >= o.rows || __ldcg(o.list_count + gr) > o.cap;
+  return __syncthreads_and(past) != 0;
+}
+
 constexpr int kTileK = 64;
 
 // Reduction modulo a compile-time modulus (near_mod_f32 states the bounds).
@@ -153,6 +166,7 @@ __global__ void __launch_bounds__(kThreads) residue_kernel(ResidueOperand o0, Re
   const int tid = threadIdx.x;
   const int64_t r0 = by * kTileRows;
   const int64_t k0 = int64_t(blockIdx.x) * kTileK;
+  if (rows_past_capacity(o, r0)) return;
 #pragma unroll
   for (int u = 0; u < kTileRows * kTileK / kThreads; ++u) {
     const int idx = tid + u * kThreads;
@@ -231,6 +245,7 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
   const int64_t r0 = by * kTileRows;
   const int64_t k0 = int64_t(blockIdx.x) * kTileK;
   const int64_t nkb = o.Kp / kStageK;
+  if (rows_past_capacity(o, r0)) return;
 #pragma unroll 1
   for (int u = 0; u < kTileRows * kTileK / (4 * kThreads); ++u) {
     const int idx = tid + u * kThreads;
