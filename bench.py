@@ -66,15 +66,20 @@ def parse_args():
     p.add_argument("--configs", action="store_true",
                    help="time each workload configuration (one JSON line each) instead of "
                         "the headline run")
-    p.add_argument("--op", choices=["gemm", "partial"], default="gemm",
-                   help="the timed call: det_gemm (the headline) or det_gemm_partial into a "
-                        "preallocated digit array (for profiling the digit write-out)")
+    p.add_argument("--op", choices=["gemm", "partial", "batched"], default="gemm",
+                   help="the timed call: det_gemm (the headline), det_gemm_partial into a "
+                        "preallocated digit array (for profiling the digit write-out), or "
+                        "det_gemm_strided_batched over --batch entries of M x N x K (default "
+                        "128 x 128 x 4096; for profiling the batched pipeline)")
+    p.add_argument("--batch", type=int, default=64, help="entries of --op batched")
     p.add_argument("--mnk", type=int, nargs=3, default=None, metavar=("M", "N", "K"),
                    help="override the problem size (profiling of small cases only)")
     args = p.parse_args()
+    global M, N, K
     if args.mnk:
-        global M, N, K
         M, N, K = args.mnk
+    elif args.op == "batched":
+        M, N, K = 128, 128, 4096
     return args
 
 
@@ -441,13 +446,21 @@ def run_ours(args):
     from exact_sum_gemm_gb300 import _native
     lib = dg.library()
 
-    A, B = make_inputs(rank_seed(rank), args.workload)
+    nbatch = args.batch if args.op == "batched" else 1
+    if args.op == "batched":                   # entries stacked along a leading axis
+        from exact_sum_gemm_gb300 import workloads as wl
+        A = wl.normal_f32((nbatch, M, K), rank_seed(rank), 0)
+        B = wl.normal_f32((nbatch, N, K), rank_seed(rank), 1)
+    else:
+        A, B = make_inputs(rank_seed(rank), args.workload)
     a = torch.from_numpy(A).to(dev)
     b = torch.from_numpy(B).to(dev)
-    c = torch.empty((M, N), dtype=torch.float32, device=dev)
+    c = torch.empty((nbatch, M, N) if nbatch > 1 else (M, N), dtype=torch.float32, device=dev)
     flush = torch.empty(FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    if args.op == "partial":
+    if args.op == "batched":
+        timed_call = lambda: dg.det_gemm_batched(a, b, out=c)
+    elif args.op == "partial":
         digits = torch.empty((20, M, N), dtype=torch.int64, device=dev)
         timed_call = lambda: dg.det_gemm_partial(a, b, out=digits)
     else:
@@ -504,10 +517,12 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     lib.det_stage_timing(0)
     stages = stage_spans(_native.stage_timeline(), stage_calls)
-    flops = 2.0 * M * N * K
+    flops = 2.0 * M * N * K * nbatch
     value = flops * world / (ms_per_step * 1e-3) / 1e9
 
     extras = {"op": "det_gemm_partial"} if args.op == "partial" else {}
+    if args.op == "batched":
+        extras = {"op": "det_gemm_strided_batched", "batch": nbatch}
     if rank == 0 and not args.no_extras and args.op == "gemm":
         extras = measure_extras(args, dg, a, b, c, A, B, dev, stream)
     pipes = measure_pipe_peaks(lib, dev, uuid) if rank == 0 and not args.no_extras else None
@@ -527,7 +542,9 @@ def run_ours(args):
     # run once per row band, on several streams at once), so the stages need
     # not add up to the step
     stage_ms = {k: v[0] for k, v in stages.items()}
-    roofline = roofline_for(stage_ms, stages, props, peaks, lib, args.workload, pipes)
+    # (the batched profiling mode has no per-entry roofline: its planes bound it)
+    roofline = roofline_for(stage_ms, stages, props, peaks, lib, args.workload, pipes) \
+        if args.op != "batched" else None
     line = {
         "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
