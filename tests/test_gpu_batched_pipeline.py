@@ -144,6 +144,24 @@ def test_entries_packed_into_shared_tiles(oracle_mod, batch, M, N, K):
                       "against entry by entry")
 
 
+def test_many_tiny_entries_and_a_shared_left_operand(oracle_mod):
+    # 1000 entries of 64 x 64 x 64: 64 000 stacked rows through the planes,
+    # the routing and two bands; x is one [M, K] matrix every entry shares
+    # (an expanded view: entry stride 0)
+    batch, M, N, K = 1000, 64, 64, 64
+    x = wl.normal_f32((M, K), 68, 0)
+    W = wl.normal_f32((batch, N, K), 68, 1)
+    W[999, 5, 7] = np.float32(-4e-9)                      # a deep column in the last entry
+    xb = dev_f32(x).unsqueeze(0).expand(batch, M, K)
+    wd = dev_f32(W)
+    got, n = _launches(lambda: dg.det_gemm_batched(xb, wd))
+    assert n < 40, n
+    for i in (0, 1, 500, 998, 999):
+        assert_bits_equal(bits_of(got[i]), np_bits(oracle_mod.gemm(x, W[i])), f"entry {i}")
+    assert_bits_equal(bits_of(got), bits_of(_per_entry(lambda: dg.det_gemm_batched(xb, wd))),
+                      "against entry by entry")
+
+
 def test_switch_returns_the_previous_setting():
     lib = dg.library()
     assert lib.det_set_batched_pipeline(0) == 1
