@@ -422,7 +422,9 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
             "data": "synthetic", "impl": "reference",
-            "config": workload_config(args.workload, {"parallelism": "host cores"}),
+            # our arm's config (the oracle runs on the host cores: cpu_baseline)
+            "config": workload_config(args.workload, {"parallelism": f"{world} independent replicas"
+                                                      if world > 1 else "single GPU"}),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores,
                              "kind": "oracle",
                              "sample": f"each step: {rows} random rows of the 4096^3 problem"},
