@@ -62,6 +62,7 @@ struct WidePlan {
   void* mem;                  // scratch, released on the tail stream
   int* wide;                  // wide tiles (count first)
   int* rest;                  // tiles left for the general kernel (count first)
+  int* glist;                 // the wide GEMM's output tiles holding a wide tile (count first)
   void* ctl;                  // moduli count, error flag, counters
   __nv_bfloat16* planesA;
   __nv_bfloat16* planesB;

@@ -244,6 +244,10 @@ struct ResGemmArgs {
   // computed; rows and columns past the entry's are not written.
   int64_t entry_rows = 0;
   int64_t entry0 = 0;
+  // (plain tiling only) a device list of the output tiles to compute, count
+  // first, as tile indices of the launch's own tiling (row-major over the
+  // whole M x N); null: every tile
+  const int* tile_list = nullptr;
 };
 cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
 
@@ -251,25 +255,34 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream);
 __host__ __device__ inline int64_t gemm_b_rows(const ResGemmArgs& a) {
   return a.entry_rows > 0 ? (a.entry0 + a.M / a.entry_rows) * a.N : a.N;
 }
+// How a launch enumerates its output tiles: every tile of M x N, each
+// strided-batch entry's own (entry_rows > 0), or a device-side list
+// (tile_list).  Each is its own compiled variant of the tensor-core kernels,
+// so the plain one keeps its register allocation.
+constexpr int kTilingPlain = 0, kTilingEntries = 1, kTilingListed = 2;
+__host__ __device__ inline int tiling_of(const ResGemmArgs& a) {
+  return a.entry_rows > 0 ? kTilingEntries : (a.tile_list != nullptr ? kTilingListed : kTilingPlain);
+}
 // Entries a TM x TN tile packs (a strided batch whose entries' rows and
 // columns both divide the tile's): tile k takes entries kG .. kG + G - 1, A's
 // rows and B's rows of those entries side by side, and only the diagonal
 // blocks (an entry's rows with its own columns) are outputs.  1: one entry
 // per tile.
-template <int TM, int TN, bool kGrouped = true>
+template <int TM, int TN, int kTiling>
 __host__ __device__ inline int64_t gemm_pack(const ResGemmArgs& a) {
-  if (!kGrouped || a.entry_rows <= 0 || a.entry_rows > TM || a.N > TN || TM % a.entry_rows != 0 ||
-      TN % a.N != 0)
+  if (kTiling != kTilingEntries || a.entry_rows <= 0 || a.entry_rows > TM || a.N > TN ||
+      TM % a.entry_rows != 0 || TN % a.N != 0)
     return 1;
   const int64_t gm = TM / a.entry_rows, gn = TN / a.N;
   return gm < gn ? gm : gn;
 }
-// Output tiles of TM x TN of a launch: the whole M x N, or each entry's own
+// Output tiles of TM x TN of a launch: the whole M x N (also the bound of a
+// listed launch, whose own count is on the device), or each entry's own
 // (pack entries per tile where they fit).
-template <int TM, int TN, bool kGrouped = true>
+template <int TM, int TN, int kTiling>
 __host__ __device__ inline int64_t gemm_tiles(const ResGemmArgs& a, int64_t pack) {
   const int64_t tn = (a.N + TN - 1) / TN;
-  if (!kGrouped || a.entry_rows <= 0) return ((a.M + TM - 1) / TM) * tn;
+  if (kTiling != kTilingEntries || a.entry_rows <= 0) return ((a.M + TM - 1) / TM) * tn;
   const int64_t entries = a.M / a.entry_rows;
   if (pack > 1) return (entries + pack - 1) / pack;
   return entries * ((a.entry_rows + TM - 1) / TM) * tn;
@@ -277,18 +290,18 @@ __host__ __device__ inline int64_t gemm_tiles(const ResGemmArgs& a, int64_t pack
 // Tile t: its first row of A (in the launch), first row of B's planes, first
 // output column, and the end of its rows' entry (rows from there on are
 // another entry's, or past M: computed but not written).  A packed tile's
-// first column is 0 and m_end the end of its last entry.
-// (kGrouped false: the plain tiling, whatever the arguments hold)
-template <int TM, int TN, bool kGrouped = true>
+// first column is 0 and m_end the end of its last entry; a listed launch's
+// t-th tile is the list's t-th entry.
+template <int TM, int TN, int kTiling>
 __host__ __device__ inline void gemm_tile(const ResGemmArgs& a, int64_t pack, int64_t t, int64_t& m0,
                                           int64_t& nb0, int64_t& n0, int64_t& m_end) {
   const int64_t tn = (a.N + TN - 1) / TN;
-  if (kGrouped && a.entry_rows > 0 && pack > 1) {
+  if (kTiling == kTilingEntries && a.entry_rows > 0 && pack > 1) {
     m0 = t * pack * a.entry_rows;
     n0 = 0;
     nb0 = (a.entry0 + t * pack) * a.N;
     m_end = m0 + pack * a.entry_rows < a.M ? m0 + pack * a.entry_rows : a.M;
-  } else if (kGrouped && a.entry_rows > 0) {
+  } else if (kTiling == kTilingEntries && a.entry_rows > 0) {
     const int64_t tm = (a.entry_rows + TM - 1) / TM;
     const int64_t e = t / (tm * tn), r = t - e * (tm * tn);
     const int64_t i = r / tn;
@@ -297,6 +310,7 @@ __host__ __device__ inline void gemm_tile(const ResGemmArgs& a, int64_t pack, in
     nb0 = (a.entry0 + e) * a.N + n0;
     m_end = (e + 1) * a.entry_rows;
   } else {
+    if (kTiling == kTilingListed) t = a.tile_list[1 + t];
     m0 = (t / tn) * TM;
     n0 = (t - (t / tn) * tn) * TN;
     nb0 = n0;

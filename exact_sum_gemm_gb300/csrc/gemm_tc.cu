@@ -73,7 +73,7 @@ __device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
   tt = J - c * T;
 }
 
-template <bool kGrouped>
+template <int kTiling>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB, ResGemmArgs a) {
@@ -92,8 +92,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // work units: (modulus, pair of neighbouring output tiles), modulus-major so
   // that the CTAs in flight share one plane of A and one of B in L2
   // (a strided batch: each entry's own tiles, or several entries per tile)
-  const int64_t pack = gemm_pack<kBlockM, kBlockN, kGrouped>(a);
-  const int64_t tiles = gemm_tiles<kBlockM, kBlockN, kGrouped>(a, pack);
+  const int64_t pack = gemm_pack<kBlockM, kBlockN, kTiling>(a);
+  const int64_t tiles = kTiling == kTilingListed ? int64_t(a.tile_list[0])    // (the count first)
+                                                 : gemm_tiles<kBlockM, kBlockN, kTiling>(a, pack);
   const int64_t tile_pairs = (tiles + 1) / 2;
   const int64_t units = tile_pairs * planes_used(a);
   if (units == 0) return;                  // nothing to compute: leave before any set-up
@@ -141,7 +142,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int tt, c;
         job_at(J, T, tt, c);
         int64_t m0, nb0, n0, m_end;
-        gemm_tile<kBlockM, kBlockN, kGrouped>(a, pack, t0 + tt, m0, nb0, n0, m_end);
+        gemm_tile<kBlockM, kBlockN, kTiling>(a, pack, t0 + tt, m0, nb0, n0, m_end);
         const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
         for (int kb = c * kKbPerChunk; kb < kb_end; ++kb) {
           const uint32_t s = it % kStages, ph = (it / kStages) & 1u;
@@ -229,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int tt, c;
       job_at(J, T, tt, c);
       int64_t m0, nb0, n0, m_end;
-      gemm_tile<kBlockM, kBlockN, kGrouped>(a, pack, t0 + tt, m0, nb0, n0, m_end);
+      gemm_tile<kBlockM, kBlockN, kTiling>(a, pack, t0 + tt, m0, nb0, n0, m_end);
       const int64_t row = m0 + 32 * g + lane;
       // a packed tile: this row's entry within the tile (only its own columns)
       const int64_t row_entry = pack > 1 ? entry_div(row - m0, a.entry_rows) : 0;
@@ -346,12 +347,13 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   if (a.M == 0 || a.N == 0 || a.Kp == 0 || a.nplanes <= 0) return cudaSuccess;
   static PerDeviceOnce configured;                 // the attribute is per device
   cudaError_t ce = configured.run([](int) {
-    cudaError_t r = cudaFuncSetAttribute(residue_gemm_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    return r != cudaSuccess ? r : cudaFuncSetAttribute(residue_gemm_kernel<true>,
-                                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       static_cast<int>(kSmemBytes));
+    cudaError_t r = cudaSuccess;
+    for (auto kern : {residue_gemm_kernel<kTilingPlain>, residue_gemm_kernel<kTilingEntries>,
+                      residue_gemm_kernel<kTilingListed>})
+      if (r == cudaSuccess)
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
+    return r;
   });
   if (ce != cudaSuccess) return ce;
   CUtensorMap tmA, tmB;
@@ -363,13 +365,19 @@ cudaError_t launch_residue_gemm(const ResGemmArgs& a, cudaStream_t stream) {
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (sms <= 0) sms = 1;
-  const int64_t tiles = gemm_tiles<kBlockM, kBlockN>(a, gemm_pack<kBlockM, kBlockN>(a));
+  // (a listed launch: every tile as the bound; its CTAs past the list's work return)
+  const int64_t tiles = a.entry_rows > 0
+                            ? gemm_tiles<kBlockM, kBlockN, kTilingEntries>(a, gemm_pack<kBlockM, kBlockN, kTilingEntries>(a))
+                            : gemm_tiles<kBlockM, kBlockN, kTilingPlain>(a, 1);
   // sized for the fewest moduli the launch may compute (every CTA has a unit)
   const int64_t units = (tiles + 1) / 2 *
       (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const unsigned grid = static_cast<unsigned>(units < sms ? units : sms);
-  if (a.entry_rows > 0) residue_gemm_kernel<true><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
-  else residue_gemm_kernel<false><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a);
+  switch (tiling_of(a)) {
+    case kTilingEntries: residue_gemm_kernel<kTilingEntries><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a); break;
+    case kTilingListed: residue_gemm_kernel<kTilingListed><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a); break;
+    default: residue_gemm_kernel<kTilingPlain><<<grid, kThreads, kSmemBytes, stream>>>(tmA, tmB, a); break;
+  }
   note_launch();
   return cudaGetLastError();
 }

@@ -73,7 +73,7 @@ __device__ __forceinline__ void job_at(int J, int T, int& tt, int& c) {
   tt = J - c * T;
 }
 
-template <bool kGrouped>
+template <int kTiling>
 __global__ void __launch_bounds__(kThreads, 1)
     residue_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                              const __grid_constant__ CUtensorMap tmB, ResGemmArgs a) {
@@ -93,8 +93,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int nkb = static_cast<int>(a.Kp / kStageK);
   const int nch = (nkb + kKbPerChunk - 1) / kKbPerChunk;
   // (a strided batch: each entry's own tiles, or several entries per tile)
-  const int64_t pack = gemm_pack<kPairM, kTileN, kGrouped>(a);
-  const int64_t tiles = gemm_tiles<kPairM, kTileN, kGrouped>(a, pack);
+  const int64_t pack = gemm_pack<kPairM, kTileN, kTiling>(a);
+  const int64_t tiles = kTiling == kTilingListed ? int64_t(a.tile_list[0])    // (the count first)
+                                                 : gemm_tiles<kPairM, kTileN, kTiling>(a, pack);
   const int64_t singles = tiles * planes_used(a);  // (modulus, tile), modulus-major
   // a cluster with no item (a launch sized for more moduli than it computes)
   // issues no MMA, so it neither commits nor waits for the final commit
@@ -157,7 +158,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           job_at(J, T, tt, c);
           int64_t t, m0, nb0, n0, m_end;
           single_at(sg[tt], u, t);
-          gemm_tile<kPairM, kTileN, kGrouped>(a, pack, t, m0, nb0, n0, m_end);
+          gemm_tile<kPairM, kTileN, kTiling>(a, pack, t, m0, nb0, n0, m_end);
           const int ga = static_cast<int>((m0 + kHalfM * rank) / kPlaneRows);
           const int gb = static_cast<int>((nb0 + (kTileN / 2) * rank) / kPlaneRows);
           const int kb_end = min(nkb, (c + 1) * kKbPerChunk);
@@ -252,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         job_at(J, T, tt, c);
         int64_t t, m0, nb0, n0, m_end;
         single_at(sg[tt], u, t);
-        gemm_tile<kPairM, kTileN, kGrouped>(a, pack, t, m0, nb0, n0, m_end);
+        gemm_tile<kPairM, kTileN, kTiling>(a, pack, t, m0, nb0, n0, m_end);
         const int64_t row = m0 + kHalfM * rank + 32 * g + lane;
         // a packed tile: this row's entry within the tile (only its own columns)
         const int64_t row_entry = pack > 1 ? entry_div(row - m0, a.entry_rows) : 0;
@@ -351,16 +352,16 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   cudaError_t e = queried.run([&](int d) {
     int n = 0, sms = 0;
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, d);
-    cudaError_t r = cudaFuncSetAttribute(residue_gemm_pair_kernel<false>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kSmemBytes));
-    if (r == cudaSuccess)
-      r = cudaFuncSetAttribute(residue_gemm_pair_kernel<true>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(kSmemBytes));
+    cudaError_t r = cudaSuccess;
+    for (auto kern : {residue_gemm_pair_kernel<kTilingPlain>, residue_gemm_pair_kernel<kTilingEntries>,
+                      residue_gemm_pair_kernel<kTilingListed>})
+      if (r == cudaSuccess)
+        r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kSmemBytes));
     cudaLaunchConfig_t q = cfg;
     q.gridDim = dim3(static_cast<unsigned>(sms > 1 ? sms / 2 * 2 : 2), 1, 1);
-    if (r == cudaSuccess) r = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<false>, &q);
+    if (r == cudaSuccess)
+      r = cudaOccupancyMaxActiveClusters(&n, residue_gemm_pair_kernel<kTilingPlain>, &q);
     max_clusters[d] = (r == cudaSuccess && n > 0) ? n : -1;
     cudaGetLastError();                                 // a failed query is not the caller's error
     return cudaSuccess;
@@ -374,17 +375,23 @@ cudaError_t launch_residue_gemm_pair(const ResGemmArgs& a, cudaStream_t stream) 
   if (!make_plane_map(&tmA, a.A, a.M, a.Kp, a.nplanes, kHalfM) ||
       !make_plane_map(&tmB, a.B, gemm_b_rows(a), a.Kp, a.nplanes, kTileN / 2))
     return cudaErrorInvalidValue;
-  const int64_t tiles = gemm_tiles<kPairM, kTileN>(a, gemm_pack<kPairM, kTileN>(a));
+  // (a listed launch: every tile as the bound; its CTAs past the list's work return)
+  const int64_t tiles = a.entry_rows > 0
+                            ? gemm_tiles<kPairM, kTileN, kTilingEntries>(a, gemm_pack<kPairM, kTileN, kTilingEntries>(a))
+                            : gemm_tiles<kPairM, kTileN, kTilingPlain>(a, 1);
   // sized for the fewest moduli the launch may compute, so every cluster
   // has at least one item whatever count the device chooses
   const int64_t singles =
       tiles * (a.grid_moduli > 0 ? a.grid_moduli : (a.used != nullptr ? a.used_min : a.nplanes));
   const int64_t clusters = singles < max_clusters[dev] ? singles : max_clusters[dev];
   cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters), 1, 1);
-  // (a strided batch's band: the entry-aware tiling, compiled apart so that
-  // plain launches keep their own register allocation)
-  e = a.entry_rows > 0 ? cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<true>, tmA, tmB, a)
-                       : cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<false>, tmA, tmB, a);
+  // (a strided batch's band, or a listed launch: their tilings compiled
+  // apart, so that plain launches keep their own register allocation)
+  switch (tiling_of(a)) {
+    case kTilingEntries: e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<kTilingEntries>, tmA, tmB, a); break;
+    case kTilingListed: e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<kTilingListed>, tmA, tmB, a); break;
+    default: e = cudaLaunchKernelEx(&cfg, residue_gemm_pair_kernel<kTilingPlain>, tmA, tmB, a); break;
+  }
   note_launch();
   return e;
 }

@@ -91,6 +91,7 @@ struct WideOperand {
   unsigned long long* norm;     // [rows] zeroed: bound of sum (X 2^-(b+W))^2, units of 2^-40
   __nv_bfloat16* planes;        // [rows/32][Kp/64][pmax][32][64]
   int pmax;                     // planes' stride (the worst-case count)
+  const int* use;               // [rows/64] zeroed: 1 where the 64-row block is in a wide tile
 };
 
 // Exponent keys: zero means "no nonzero element", so every per-row statistic
@@ -125,7 +126,7 @@ __device__ __forceinline__ WideDecoded wide_decode(uint32_t bits) {
 // or a spread beyond the window).
 constexpr int kNoBase = 0x7FFFFFFF;
 template <int kBf16>
-__device__ __forceinline__ int row_base(const WideOperand& o, int64_t r) {
+__device__ __forceinline__ int qualifying_base(const WideOperand& o, int64_t r) {
   const int lo = o.lo_key[r], hi = o.hi_key[r];
   if (o.nonfinite[r] != 0 || lo == 0) return kNoBase;
   const int emin = kKeyBias - lo, emax = hi - kKeyBias;
@@ -133,7 +134,15 @@ __device__ __forceinline__ int row_base(const WideOperand& o, int64_t r) {
 }
 template <int kBf16>
 __device__ __forceinline__ bool row_ok(const WideOperand& o, int64_t r) {
-  return o.nonfinite[r] == 0 && (o.lo_key[r] == 0 || row_base<kBf16>(o, r) != kNoBase);
+  return o.nonfinite[r] == 0 && (o.lo_key[r] == 0 || qualifying_base<kBf16>(o, r) != kNoBase);
+}
+// The base of a row the wide GEMM needs: one that qualifies and lies in a
+// 64-row block of some wide tile (the routing's flags; a row of no wide tile
+// gets no norm and no planes).
+template <int kBf16>
+__device__ __forceinline__ int row_base(const WideOperand& o, int64_t r) {
+  if (o.use != nullptr && o.use[r / kTile] == 0) return kNoBase;
+  return qualifying_base<kBf16>(o, r);
 }
 
 // Work split of a pass over both operands in one launch: K-contiguous rows,
@@ -223,7 +232,8 @@ __global__ void __launch_bounds__(kThreads) wide_stats_kernel(WideOperand a, Wid
                                                               int64_t blocks_a, int64_t blocks_all,
                                                               const int* general,
                                                               int* block_ok, int* wide, int* rest,
-                                                              WideCtl* ctl) {
+                                                              WideCtl* ctl, int* use, int* gflag,
+                                                              int* glist, int gemm_rows) {
   const int64_t tiles_m = (a.rows + kTile - 1) / kTile, tiles_n = (b.rows + kTile - 1) / kTile;
   if (general[0] == 0) {
     if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -281,6 +291,20 @@ __global__ void __launch_bounds__(kThreads) wide_stats_kernel(WideOperand a, Wid
     const int64_t tm = t / tiles_n, tn = t - (t / tiles_n) * tiles_n;
     if (block_ok[tm] && block_ok[tiles_m + tn]) wide[1 + atomicAdd(wide, 1)] = t;
     else rest[1 + atomicAdd(rest, 1)] = t;
+  }
+  __syncthreads();
+  // what the wide GEMM needs: the 64-row blocks of A and of B that some wide
+  // tile holds (their rows get norms and planes), and the GEMM's own output
+  // tiles (gemm_rows x 256) holding a wide tile, listed once each
+  const int64_t gemm_tiles_n = (b.rows + 255) / 256;
+  const int64_t nw = wide[0];
+  for (int64_t i = threadIdx.x; i < nw; i += kThreads) {
+    const int t = wide[1 + i];
+    const int64_t tm = t / tiles_n, tn = t - (t / tiles_n) * tiles_n;
+    use[tm] = 1;
+    use[tiles_m + tn] = 1;
+    const int64_t gt = (tm * kTile / gemm_rows) * gemm_tiles_n + (tn * kTile) / 256;
+    if (atomicExch(gflag + gt, 1) == 0) glist[1 + atomicAdd(glist, 1)] = static_cast<int>(gt);
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -420,6 +444,7 @@ __global__ void __launch_bounds__(kThreads) wide_planes_kernel(WideOperand a, Wi
     const WideOperand& o = is_a ? a : b;
     const int64_t g = is_a ? gg : gg - groups_a;
     const int64_t r0 = g * kTileRows, k0 = kb * kTileK;
+    if (o.use != nullptr && o.use[r0 / kTile] == 0) continue;   // no wide tile holds these rows
     __syncthreads();                                // tables ready / previous tile done
 #pragma unroll
     for (int u = 0; u < kTileRows * kTileK / kThreads; ++u) {
@@ -831,6 +856,12 @@ cudaError_t wide_prepare(const GemmArgs& g, const Scratch& s, cudaStream_t strea
   const size_t o_wide = off;         off = align_up(off + 4 * size_t(tiles + 1), 256);
   const size_t o_rest = off;         off = align_up(off + 4 * size_t(tiles + 1), 256);
   const size_t o_ctl = off;          off = align_up(off + sizeof(WideCtl), 256);
+  // the wide GEMM's tiles: gemm_rows x 256 (CTA pairs, or one CTA for M <= 128)
+  const int gemm_rows = g.M > 128 ? 256 : 128;
+  const int64_t gemm_tiles = ((g.M + gemm_rows - 1) / gemm_rows) * ((g.N + 255) / 256);
+  const size_t o_use = off;          off = align_up(off + 4 * size_t(tiles_m + tiles_n), 256);
+  const size_t o_gflag = off;        off = align_up(off + 4 * size_t(gemm_tiles), 256);
+  const size_t o_glist = off;        off = align_up(off + 4 * size_t(gemm_tiles + 1), 256);
   const size_t zero_bytes = off;
   off = align_up(off, 1024);
   const size_t o_pa = off;           off = align_up(off + 2 * size_t(pmax) * plane_rows(g.M) * Kp, 1024);
@@ -856,9 +887,12 @@ cudaError_t wide_prepare(const GemmArgs& g, const Scratch& s, cudaStream_t strea
   w.pmax = pmax;
   w.Kp = Kp;
 
-  WideOperand oa{g.A, g.lda, g.opA, g.M, g.K, Kp, lo, hi, nf, norm, w.planesA, pmax};
+  int* use = reinterpret_cast<int*>(base + o_use);
+  int* gflag = reinterpret_cast<int*>(base + o_gflag);
+  w.glist = reinterpret_cast<int*>(base + o_glist);
+  WideOperand oa{g.A, g.lda, g.opA, g.M, g.K, Kp, lo, hi, nf, norm, w.planesA, pmax, use};
   WideOperand ob{g.B, g.ldb, g.opB, g.N, g.K, Kp, lo + g.M, hi + g.M, nf + g.M, norm + g.M,
-                 w.planesB, pmax};
+                 w.planesB, pmax, use + tiles_m};
   const WideTables tables = make_tables();
   const int sms = sm_count();
   // the kernels with shared memory prefer the largest carveout, so that they
@@ -887,8 +921,12 @@ cudaError_t wide_prepare(const GemmArgs& g, const Scratch& s, cudaStream_t strea
       // persistent: at most four blocks per SM walk the passes' blocks
       const int64_t all = ba + bb;
       const unsigned grid = static_cast<unsigned>(all < int64_t(sms) * 4 ? all : int64_t(sms) * 4);
-      if (bf16) wide_stats_kernel<1><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, s.general, blk, w.wide, w.rest, ctl);
-      else wide_stats_kernel<0><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, s.general, blk, w.wide, w.rest, ctl);
+      if (bf16)
+        wide_stats_kernel<1><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, s.general, blk, w.wide,
+                                                            w.rest, ctl, use, gflag, w.glist, gemm_rows);
+      else
+        wide_stats_kernel<0><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, s.general, blk, w.wide,
+                                                            w.rest, ctl, use, gflag, w.glist, gemm_rows);
       if (bf16) wide_norm_kernel<1><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, w.wide, pmax, ctl, tables);
       else wide_norm_kernel<0><<<grid, kThreads, 0, stream>>>(oa, ob, ba, all, w.wide, pmax, ctl, tables);
       note_launch(2);
@@ -935,8 +973,12 @@ cudaError_t wide_finish(const GemmArgs& g, const WidePlan& w, cudaStream_t tail,
     // once); with no wide tile the count is 0 and every CTA returns at entry
     ResGemmArgs rg{w.planesA, w.planesB, g.M, g.N, w.Kp, w.pmax, w.res, g.M * g.N, &ctl->error,
                    status, &ctl->used, 1, w.pmax};
+    rg.tile_list = w.glist;                // only the output tiles holding a wide tile
     e = g.M > 128 ? launch_residue_gemm_pair(rg, tail) : cudaErrorNotSupported;
-    if (e == cudaErrorNotSupported) e = launch_residue_gemm(rg, tail);
+    if (e == cudaErrorNotSupported) {
+      if (g.M > 128) rg.tile_list = nullptr;   // the list names 256-row tiles: every tile instead
+      e = launch_residue_gemm(rg, tail);
+    }
   }
   if (e == cudaSuccess) {
     StageScope t(kStageWideReconstruct, tail);

@@ -117,3 +117,28 @@ def test_wide_path_switch_gives_identical_results(oracle_mod):
     assert np.array_equal(on, off)
     assert_bits_equal(off, np_bits(oracle_mod.gemm(A, B)), "wide path off")
     np.testing.assert_array_equal(off_digits, oracle_mod.gemm_digits(A, B))
+
+
+def test_a_few_wide_rows_and_columns_in_narrow_data(oracle_mod):
+    # N(0,1) operands with 64 rows of A and 64 rows of B spanning 80 binades:
+    # only the tiles holding them are wide.  The wide GEMM computes just the
+    # 256 x 256 output tiles that hold a wide tile (a device-side list), and
+    # the wide norms and planes cover only the 64-row blocks such tiles hold;
+    # the other outputs come from the narrow path.  Rows on both sides of the
+    # wide ones are compared with the oracle, as are the wide rows themselves,
+    # and partial digits alike.
+    M, N, K = 1024, 768, 512
+    A = wl.normal_f32((M, K), 73, 0)
+    B = wl.normal_f32((N, K), 73, 1)
+    A[320:384] = wl.loguniform_f32((64, K), 73, 2, lo=-40, hi=40)
+    B[448:512] = wl.loguniform_f32((64, K), 73, 3, lo=-40, hi=40)
+    a, b = dev_f32(A), dev_f32(B)
+    got = bits_of(dg.det_gemm(a, b))
+    r = _native.tile_routes()
+    # the wide rows make 12 x 16 tiles wide (every tile of A's wide block and
+    # of B's), and no tile is left for the general kernel
+    assert r["wide"] == (N // 64) + (M // 64) - 1 and r["kulisch"] == 0, r
+    rows = np.array([0, 255, 319, 320, 351, 383, 384, 511, 512, 1023])
+    assert_bits_equal(got[rows], np_bits(oracle_mod.gemm(A[rows], B)), "sampled rows")
+    P = dg.det_gemm_partial(a, b).cpu().numpy()
+    np.testing.assert_array_equal(P[:, rows], oracle_mod.gemm_digits(A[rows], B), err_msg="digits")
