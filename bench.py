@@ -827,6 +827,20 @@ def measure_workloads(args, dev, pipes=None, with_cpu=True):
     entry("wide_4096", "det_gemm f32 4096^3, |x| = 2^U[-40,40], seed 0",
           timed(lambda: dg.det_gemm(aw, bw), n=3), 2.0 * 4096 ** 3, cpu)
     del aw, bw, Aw, Bw
+    # the headline shape with a few wide rows: N(0,1), rows 1024..1151 of A
+    # with |x| = 2^U[-40,40] (their tiles go to the wide path, the rest stay
+    # on the narrow one)
+    Am = wl.normal_f32((4096, 4096), 0, 0)
+    Am[1024:1152] = wl.loguniform_f32((128, 4096), 5, 0, lo=-40, hi=40)
+    Bm = wl.normal_f32((4096, 4096), 0, 1)
+    am, bm = f32(Am), f32(Bm)
+    cpu = oracle_time(lambda: oracle.gemm(np.ascontiguousarray(Am[1024:1088]), Bm, nthreads=cores),
+                      64 * 4096 * 4096, cores, "64 of the wide rows of the 4096^3 problem") \
+        if with_cpu else None
+    entry("mixed_4096", "det_gemm f32 4096^3, A,B N(0,1) seed 0 with rows 1024..1151 of A "
+          "|x| = 2^U[-40,40] (seed 5)", timed(lambda: dg.det_gemm(am, bm), n=5),
+          2.0 * 4096 ** 3, cpu)
+    del am, bm, Am, Bm
     # one training step of the 1024 -> 4096 -> 1024 MLP, batch 256 (targets
     # from the teacher through det_gemm, forward, backward, SGD update)
     relu = lambda t: torch.clamp_min(t, 0.0)
