@@ -307,7 +307,9 @@ __global__ void __launch_bounds__(kThreads) residue_rows_kernel(ResidueOperand o
 // atomicMax per warp on a zeroed slot, read back after a barrier: no shared
 // memory, so the launch for a later band can run beside a tensor-core GEMM),
 // then writes the residues exactly as residue_rows_kernel does, lists the
-// deep elements, and adds the row's norm bound.  Once the row's norm is
+// deep elements (a warp holding some counts them first; one holding more than
+// the list's capacity writes nothing for the row), and adds the row's norm
+// bound.  Once the row's norm is
 // complete the block folds it into its operand's maximum; the launch's last
 // block then picks the band's moduli count.  Blocks at or beyond `split`
 // take o1.  Rows past `rows` (up to the plane layout's multiple of 32) get
@@ -326,6 +328,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   const int64_t row0 = kGrouped && live_row ? operand_row_offset(o, r) : 0;
   uint32_t bits[kFusedRuns][4];
   int key = 0;
+  unsigned low = ~0u;                               // the smallest finite nonzero key, less one
 #pragma unroll
   for (int v = 0; v < kFusedRuns; ++v) {
     const int64_t k = (int64_t(v) * kThreads + tid) * 4;
@@ -355,7 +358,11 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
       }
     }
 #pragma unroll
-    for (int h = 0; h < 4; ++h) key = max(key, exp_key(bits[v][h]));
+    for (int h = 0; h < 4; ++h) {
+      const int kh = exp_key(bits[v][h]);           // 0 for zero and non-finite elements
+      key = max(key, kh);
+      low = min(low, static_cast<unsigned>(kh) - 1u);
+    }
   }
   key = __reduce_max_sync(0xFFFFFFFFu, key);
   if (lane == 0 && key != 0 && live_row) atomicMax(o.keymax + r, static_cast<unsigned>(key));
@@ -363,35 +370,76 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   const int kmax = live_row ? static_cast<int>(__ldcg(o.keymax + r)) : 0;
   if (tid == 0 && live_row) o.emax[r] = kmax != 0 ? kmax - 150 : kEmaxEmpty;
   const int em = kmax != 0 ? kmax - 150 : 0;
+  // A finite element is deep when its key is below kmax - kDeepGap.  A warp
+  // whose elements include one counts its deep elements first and takes
+  // their list slots with one atomicAdd (nearly every warp of N(0,1) data
+  // has none and skips this).  A warp that finds more deep elements than the
+  // row's list holds leaves the row past the capacity, general on every tile
+  // (the routing sends every tile holding it to the general tiles), so it
+  // writes nothing for it: the row's planes, list and norm are never read.
+  // Non-finite elements elsewhere take their slots one by one.
+  const unsigned wlow = __reduce_min_sync(0xFFFFFFFFu, low);
+  const bool counted = live_row && wlow != ~0u && static_cast<int>(wlow) + 1 < kmax - kDeepGap;
+  int slot = 0;                                     // this thread's next list slot
+  int warp_deep = 0;                                // the warp's deep elements (if counted)
+  int deep_seen = 0;                                // largest list slot + 1 this thread took
+  if (counted) {                                    // (the same for the whole warp)
+    int mine = 0;
+#pragma unroll
+    for (int v = 0; v < kFusedRuns; ++v) {
+      const int64_t k = (int64_t(v) * kThreads + tid) * 4;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const Decoded d = decode_f32_bits(bits[v][h]);
+        const bool deep = d.nonfinite || (d.m != 0 && d.e - em + kDeepGap < 0);
+        mine += deep && k + h < o.K ? 1 : 0;
+      }
+    }
+    int incl = mine;                                // inclusive prefix over the warp
+#pragma unroll
+    for (int w = 1; w < 32; w *= 2) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, incl, w);
+      if (lane >= w) incl += t;
+    }
+    int base = 0;
+    if (lane == 31 && incl > 0) base = atomicAdd(o.list_count + r, incl);
+    base = __shfl_sync(0xFFFFFFFFu, base, 31);
+    warp_deep = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    slot = base + incl - mine;
+    deep_seen = base + warp_deep;                   // (the row's count once this warp's are in)
+  }
   const int64_t nkb = o.Kp / kStageK;
   float sum = 0.0f;                                 // this thread's X_int^2 / 2^norm_shift
-  int deep_seen = 0;                                // largest list slot + 1 this thread took
   constexpr float kHalfShift = kBf16 ? 0x1p-8f : 0x1p-26f;
+  if (warp_deep <= o.cap) {                         // (the same for the whole warp)
 #pragma unroll
-  for (int v = 0; v < kFusedRuns; ++v) {
-    const int64_t k = (int64_t(v) * kThreads + tid) * 4;
-    if (k >= o.Kp) break;                           // the whole run lies past the padded K
-    float x[4], pw[4];
+    for (int v = 0; v < kFusedRuns; ++v) {
+      const int64_t k = (int64_t(v) * kThreads + tid) * 4;
+      if (k >= o.Kp) break;                         // the whole run lies past the padded K
+      float x[4], pw[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const Decoded d = decode_f32_bits(bits[v][h]);
-      const int sh = d.e - em + kDeepGap;
-      const bool deep = d.nonfinite || (d.m != 0 && sh < 0);
-      const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
-      x[h] = static_cast<float>(deep ? 0 : mi);
-      pw[h] = __int_as_float((deep || d.m == 0 ? 127 : sh + 127) << 23);
-      if (deep && k + h < o.K && live_row) {
-        const int slot = take_deep_slot(o.list_count + r, o.cap);
-        if (slot < o.cap) o.list[r * o.cap + slot] = make_uint2(static_cast<uint32_t>(k + h), bits[v][h]);
-        deep_seen = max(deep_seen, slot + 1);
+      for (int h = 0; h < 4; ++h) {
+        const Decoded d = decode_f32_bits(bits[v][h]);
+        const int sh = d.e - em + kDeepGap;
+        const bool deep = d.nonfinite || (d.m != 0 && sh < 0);
+        const int32_t mi = kBf16 ? (d.m >> 16) : d.m;
+        x[h] = static_cast<float>(deep ? 0 : mi);
+        pw[h] = __int_as_float((deep || d.m == 0 ? 127 : sh + 127) << 23);
+        if (deep && k + h < o.K && live_row) {
+          // a counted warp's slots in the order they were counted; else a
+          // non-finite element's own
+          const int at = counted ? slot++ : take_deep_slot(o.list_count + r, o.cap);
+          if (at < o.cap) o.list[r * o.cap + at] = make_uint2(static_cast<uint32_t>(k + h), bits[v][h]);
+          deep_seen = max(deep_seen, at + 1);
+        }
+        const float f = __fmul_rn(__fmul_rn(x[h], pw[h]), kHalfShift);   // exact
+        sum = __fmaf_rn(f, f, sum);
       }
-      const float f = __fmul_rn(__fmul_rn(x[h], pw[h]), kHalfShift);   // exact
-      sum = __fmaf_rn(f, f, sum);
+      uint2* dst = reinterpret_cast<uint2*>(
+          o.planes + ((r / kPlaneRows) * nkb + k / kStageK) * P * kPlaneRows * kStageK +
+          (r % kPlaneRows) * kStageK + (k % kStageK));
+      write_residue_quads<0, P>(dst, x, pw);
     }
-    uint2* dst = reinterpret_cast<uint2*>(
-        o.planes + ((r / kPlaneRows) * nkb + k / kStageK) * P * kPlaneRows * kStageK +
-        (r % kPlaneRows) * kStageK + (k % kStageK));
-    write_residue_quads<0, P>(dst, x, pw);
   }
   // the row's norm bound: 16 roundings in the thread, 5 in the warp (all to
   // nearest, positive values: relative error below 2^-19), scaled by
@@ -400,7 +448,7 @@ __global__ void __launch_bounds__(kThreads) residue_fused_kernel(ResidueOperand 
   for (int w = 16; w >= 1; w /= 2) sum = __fadd_rn(sum, __shfl_xor_sync(0xFFFFFFFFu, sum, w));
   if (lane == 0 && live_row && sum > 0.0f)
     atomicAdd(o.norm + r, __float2ull_ru(__fmul_ru(sum, 1.0f + 0x1p-16f)));
-  // the row's deep count is the largest slot + 1 any thread took: one
+  // the row's deep count is the largest of these over its warps: one
   // atomicMax per warp that found a deep element into its 64-row block
   deep_seen = __reduce_max_sync(0xFFFFFFFFu, deep_seen);
   if (lane == 0 && deep_seen > 0 && o.dmax != nullptr)

@@ -86,7 +86,7 @@ def test_wide_headline_shape_sampled_rows(oracle_mod):
     B = wl.loguniform_f32((4096, 4096), 0, 1, lo=-40, hi=40)
     got = bits_of(dg.det_gemm(dev_f32(A), dev_f32(B)))
     _all_wide([_native.tile_routes()])
-    rows = np.array(sorted({0, 1, 127, 128, 255, 256, 2047, 2048, 2815, 2816, 4094, 4095} |
+    rows = np.array(sorted({0, 1, 127, 128, 255, 256, 2047, 2048, 2559, 2560, 2815, 2816, 4094, 4095} |
                            set(wl.rng(75, 0).integers(0, 4096, size=52).tolist())))
     assert_bits_equal(got[rows], np_bits(oracle_mod.gemm(A[rows], B)), "wide 4096^3 rows")
 
@@ -142,3 +142,31 @@ def test_a_few_wide_rows_and_columns_in_narrow_data(oracle_mod):
     assert_bits_equal(got[rows], np_bits(oracle_mod.gemm(A[rows], B)), "sampled rows")
     P = dg.det_gemm_partial(a, b).cpu().numpy()
     np.testing.assert_array_equal(P[:, rows], oracle_mod.gemm_digits(A[rows], B), err_msg="digits")
+
+
+@pytest.mark.parametrize("wide_rows", ["all", "upper", "lower"])
+def test_wide_rows_in_a_tall_output(oracle_mod, wide_rows):
+    # 2304 rows (two narrow row bands, split at row 1024): wide tiles
+    # everywhere, or only in 64 rows of A in the lower or the upper part of
+    # C.  Every output of the wide rows and the rows around them, and the
+    # rows at the narrow band edge, equal the oracle's, and so do their
+    # digits.
+    M, N, K = 2304, 320, 300
+    if wide_rows == "all":
+        A = wl.loguniform_f32((M, K), 78, 0, lo=-40, hi=40)
+        B = wl.loguniform_f32((N, K), 78, 1, lo=-40, hi=40)
+        check = np.arange(M)
+    else:
+        A = wl.normal_f32((M, K), 79, 0)
+        B = wl.normal_f32((N, K), 79, 1)
+        lo = 1984 if wide_rows == "lower" else 640
+        A[lo:lo + 64] = wl.loguniform_f32((64, K), 79, 2, lo=-40, hi=40)
+        check = np.array(sorted(set(range(lo - 2, lo + 66)) | {0, 1023, 1024, 1025, M - 1}))
+    a, b = dev_f32(A), dev_f32(B)
+    got = bits_of(dg.det_gemm(a, b))
+    r = _native.tile_routes()
+    assert r["wide"] > 0 and r["kulisch"] == 0, r
+    assert_bits_equal(got[check], np_bits(oracle_mod.gemm(A[check], B)), f"wide rows: {wide_rows}")
+    edge = np.array([0, 1023, 1024, M - 1] + ([640, 700] if wide_rows == "upper" else [2000]))
+    P = dg.det_gemm_partial(a, b).cpu().numpy()
+    np.testing.assert_array_equal(P[:, edge], oracle_mod.gemm_digits(A[edge], B), err_msg="digits")
