@@ -61,8 +61,10 @@ bool rows_layout(const ResidueOperand& o, int bf16) {
 constexpr int kThreads = 256;
 constexpr int kTileRows = 32;
 
-// A row's deep-element list slot.  The count saturates a little past the
-// list's capacity: once a row holds more deep elements than its list takes,
+// A row's deep-element list slot, taken one by one.  Taken this way the
+// count saturates a little past the list's capacity (the fused kernel's
+// warps that count their deep elements first add them all at once): once a
+// row holds more deep elements than its list takes,
 // every tile of the row goes to the general tiles, and every reader of the
 // count only asks whether it exceeds the capacity (or is nonzero), so further
 // increments are skipped.  Without this, data whose elements are nearly all
